@@ -1,0 +1,212 @@
+/*
+ * oracle.c - plain, slow, single-threaded fp64 CPU reference for the
+ * row-wise LayerNorm and RMSNorm forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may load this library. The product path
+ * (the CUDA library and its Python binding) never links, imports or calls
+ * it, and shares no code, header or table with it.
+ *
+ * Sources (page title, section):
+ *   [Ch7]  "第 7 章 LayerNorm 与 RMSNorm" (CUDA 算子工程)
+ *   [RMS2] "CUDA算子优化(2)：RMSNorm"
+ *   [T3]   "T3 讲解：LayerNorm / RMSNorm 的 forward"
+ *
+ * Every routine below is the textbook definition written out, accumulating
+ * in double precision: no blocking, no fusion, no reordering.
+ *
+ * Element types of the inputs: 0 = fp32, 1 = bf16 (raw 16-bit patterns),
+ * 2 = fp64. Every input is widened exactly to double before any arithmetic.
+ *
+ * Parity pins: each routine is pinned in tests/test_oracle_pins.py against
+ * the pages' worked examples, closed forms, exact rational arithmetic on tiny
+ * rows and an independent library routine (torch fp64 on the CPU).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F64 = 2 };
+
+/* Widen element i of a row to double. bf16 is the upper half of an fp32
+ * bit pattern, so the widening is exact for all three types. */
+static double orc_load(const void *p, int dtype, int64_t i)
+{
+    if (dtype == ORC_F32)
+        return (double)((const float *)p)[i];
+    if (dtype == ORC_BF16) {
+        uint32_t bits = (uint32_t)((const uint16_t *)p)[i] << 16;
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return (double)f;
+    }
+    return ((const double *)p)[i];
+}
+
+static int64_t orc_elem_size(int dtype)
+{
+    return dtype == ORC_F32 ? 4 : dtype == ORC_BF16 ? 2 : 8;
+}
+
+/*
+ * Mean and biased variance of one row of N elements, by the two-pass
+ * definition: [Ch7] §7.1 (mu = sum/H, sigma^2 = sum (x - mu)^2 / H) and the
+ * two-pass algorithm of [Ch7] §7.2; divisor N, not N-1 ([T3] §⑥).
+ */
+void oracle_row_moments(const void *x, int dtype, int64_t N,
+                        double *mean, double *var)
+{
+    double sum = 0.0;
+    for (int64_t i = 0; i < N; ++i)
+        sum += orc_load(x, dtype, i);
+    const double mu = sum / (double)N;
+
+    double sq = 0.0;
+    for (int64_t i = 0; i < N; ++i) {
+        const double d = orc_load(x, dtype, i) - mu;
+        sq += d * d;
+    }
+    *mean = mu;
+    *var = sq / (double)N;
+}
+
+/*
+ * LayerNorm forward over an [M, N] row-major matrix ([Ch7] §7.1):
+ *   y = (x - mu) / sqrt(var + eps) * gamma + beta,  rstd = 1/sqrt(var + eps).
+ * x, gamma and beta share `dtype`. Outputs are double; mean and rstd may be
+ * NULL.
+ */
+void oracle_ln_fwd(const void *x, const void *gamma, const void *beta,
+                   int dtype, int64_t M, int64_t N, double eps,
+                   double *y, double *mean, double *rstd)
+{
+    const int64_t es = orc_elem_size(dtype);
+    for (int64_t r = 0; r < M; ++r) {
+        const void *xr = (const char *)x + r * N * es;
+        double mu, var;
+        oracle_row_moments(xr, dtype, N, &mu, &var);
+        const double rs = 1.0 / sqrt(var + eps);
+        for (int64_t i = 0; i < N; ++i) {
+            const double xi = orc_load(xr, dtype, i);
+            y[r * N + i] = (xi - mu) * rs * orc_load(gamma, dtype, i)
+                           + orc_load(beta, dtype, i);
+        }
+        if (mean)
+            mean[r] = mu;
+        if (rstd)
+            rstd[r] = rs;
+    }
+}
+
+/*
+ * RMSNorm forward over an [M, N] row-major matrix ([Ch7] §7.5; [RMS2] §1):
+ *   rstd = 1/sqrt(sum x^2 / N + eps),  y = x * rstd * w.
+ * No mean is subtracted and there is no bias. rstd may be NULL.
+ */
+void oracle_rms_fwd(const void *x, const void *w, int dtype, int64_t M,
+                    int64_t N, double eps, double *y, double *rstd)
+{
+    const int64_t es = orc_elem_size(dtype);
+    for (int64_t r = 0; r < M; ++r) {
+        const void *xr = (const char *)x + r * N * es;
+        double ss = 0.0;
+        for (int64_t i = 0; i < N; ++i) {
+            const double xi = orc_load(xr, dtype, i);
+            ss += xi * xi;
+        }
+        const double rs = 1.0 / sqrt(ss / (double)N + eps);
+        for (int64_t i = 0; i < N; ++i)
+            y[r * N + i] = orc_load(xr, dtype, i) * rs * orc_load(w, dtype, i);
+        if (rstd)
+            rstd[r] = rs;
+    }
+}
+
+/* Round each double to the nearest fp32, ties to even (C's conversion under
+ * the default rounding mode is the single IEEE rounding). */
+void oracle_round_f32(const double *v, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = (float)v[i];
+}
+
+/* Round one double to bf16 (8 significant bits, fp32 exponent range),
+ * nearest with ties to even, returned as the raw 16-bit pattern. The value
+ * is scaled onto an integer grid whose spacing is one bf16 ulp of its
+ * binade, rounded with rint(), and scaled back; all steps but rint() are
+ * exact. */
+static uint16_t orc_bf16(double v)
+{
+    if (isnan(v))
+        return 0x7FC0;
+    const int neg = signbit(v) != 0;
+    const double a = fabs(v);
+    if (isinf(a))
+        return neg ? 0xFF80 : 0x7F80;
+    double res = 0.0;
+    if (a != 0.0) {
+        int e;
+        (void)frexp(a, &e);       /* a = m * 2^e with m in [0.5, 1) */
+        int ex = e - 1;           /* floor(log2 a) */
+        if (ex < -126)
+            ex = -126;            /* subnormal binade keeps the fixed spacing */
+        res = ldexp(rint(ldexp(a, 7 - ex)), ex - 7);
+    }
+    float f = (float)res;
+    if (res >= 0x1p128)
+        f = INFINITY;
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    bits >>= 16;
+    if (neg)
+        bits |= 0x8000u;
+    return (uint16_t)bits;
+}
+
+void oracle_round_bf16(const double *v, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_bf16(v[i]);
+}
+
+/*
+ * Welford's running state and Chan's merge, in double precision. They are
+ * not used by the reference outputs above (which follow the definition);
+ * they exist so that the pins can show, on tiny rows and under every merge
+ * order, that the algorithm the GPU path uses reaches the two-pass result.
+ */
+typedef struct {
+    double n, mean, m2;
+} orc_welford;
+
+/* One-element update, [Ch7] §7.4: n' = n+1; d = x - mean; mean += d/n';
+ * m2 += d * (x - mean'). */
+void oracle_welford_update(orc_welford *s, double x)
+{
+    const double n1 = s->n + 1.0;
+    const double d = x - s->mean;
+    s->mean += d / n1;
+    s->m2 += d * (x - s->mean);
+    s->n = n1;
+}
+
+/* Parallel merge of two partial states, [Ch7] §7.4.1:
+ * n = na+nb; d = mb - ma; mean = ma + d*nb/n; m2 = m2a + m2b + d^2*na*nb/n.
+ * The merge of two empty states is empty. */
+void oracle_chan_combine(const orc_welford *a, const orc_welford *b,
+                         orc_welford *out)
+{
+    const double n = a->n + b->n;
+    if (n == 0.0) {
+        out->n = out->mean = out->m2 = 0.0;
+        return;
+    }
+    const double d = b->mean - a->mean;
+    orc_welford r;
+    r.n = n;
+    r.mean = a->mean + d * b->n / n;
+    r.m2 = a->m2 + b->m2 + d * d * a->n * b->n / n;
+    *out = r;
+}
+
+int oracle_abi_version(void) { return 1; }

@@ -1,0 +1,113 @@
+"""Seeded synthetic inputs for the LayerNorm / RMSNorm forward workloads.
+
+This module only draws numbers: it holds none of the normalisation
+arithmetic. Both the CUDA path (tests, benchmark) and the CPU oracle read the
+very same tensors produced here, so the choice of generator does not affect
+parity.
+
+Workloads (shapes and value distributions of the source pages):
+  ln_f32_128x1024          LayerNorm fp32, M=128 N=1024 (the ROCm LayerNorm
+                           README's usage example); x ~ N(0,1), gamma ~ U(.5,1.5),
+                           beta ~ U(-.1,.1), eps 1e-5.
+  rms_f32_8192x4096        RMSNorm fp32, B=8 T=1024 C=4096 ("CUDA算子优化(2)：
+                           RMSNorm" §2); x ~ U(-1,1), w ~ U(0,1), eps 1e-6.
+  ln_bf16_4096x8192_outliers  LayerNorm bf16, M=4096 N=8192 (the T3 drill's
+                           N); row offset ~ U(100,1000) + N(0, 0.01^2) noise,
+                           1 % of channels (fixed per seed) replaced by +-300.
+  rms_bf16_65536x2048      RMSNorm bf16, B=64 T=1024 C=2048 (the RMSNorm
+                           post's V0/V2 sizes); x ~ U(-1,1), w ~ U(0,1), eps 1e-6.
+  ln_f32_2048x65536        LayerNorm fp32 long rows; x ~ N(3,1).
+  ln_f32_8192x5000         LayerNorm fp32, N not a power of two; x ~ N(3,1).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    op: str        # "ln" or "rms"
+    dtype: str     # "f32" or "bf16"
+    M: int
+    N: int
+    eps: float
+    recipe: str    # key of the value distribution below
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    @property
+    def elem_size(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    def algorithmic_bytes(self, M: int | None = None) -> int:
+        """HBM bytes one forward call must move: read x, write y, read the
+        per-column parameters, write 8 B of statistics per row (LayerNorm)."""
+        M = self.M if M is None else M
+        s = self.elem_size
+        params = 2 if self.op == "ln" else 1
+        stats = 8 * M if self.op == "ln" else 0
+        return 2 * M * self.N * s + params * self.N * s + stats
+
+    def scaled(self, M: int | None = None, N: int | None = None) -> "Workload":
+        return Workload(self.name, self.op, self.dtype, M or self.M, N or self.N, self.eps, self.recipe)
+
+
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("ln_f32_128x1024", "ln", "f32", 128, 1024, 1e-5, "normal01"),
+        Workload("rms_f32_8192x4096", "rms", "f32", 8192, 4096, 1e-6, "uniform_pm1"),
+        Workload("ln_bf16_4096x8192_outliers", "ln", "bf16", 4096, 8192, 1e-5, "offset_outliers"),
+        Workload("rms_bf16_65536x2048", "rms", "bf16", 65536, 2048, 1e-6, "uniform_pm1"),
+        Workload("ln_f32_2048x65536", "ln", "f32", 2048, 65536, 1e-5, "normal31"),
+        Workload("ln_f32_8192x5000", "ln", "f32", 8192, 5000, 1e-5, "normal31"),
+    ]
+}
+
+BENCH_WORKLOAD = "rms_f32_8192x4096"
+
+
+def generate(w: Workload, seed: int = 0) -> dict[str, torch.Tensor]:
+    """CPU tensors for one workload: {"x", "gamma", "beta"} (LayerNorm) or
+    {"x", "w"} (RMSNorm), all in the workload's dtype, drawn in a fixed order
+    from one seeded CPU generator."""
+    g = torch.Generator().manual_seed(seed)
+    M, N = w.M, w.N
+    if w.recipe == "normal01":
+        x = torch.randn(M, N, generator=g)
+    elif w.recipe == "normal31":
+        x = torch.randn(M, N, generator=g) + 3.0
+    elif w.recipe == "uniform_pm1":
+        x = torch.rand(M, N, generator=g) * 2.0 - 1.0
+    elif w.recipe == "offset_outliers":
+        offset = torch.rand(M, 1, generator=g) * 900.0 + 100.0
+        x = offset + torch.randn(M, N, generator=g) * 0.01
+        n_out = max(1, round(0.01 * N))
+        cols = torch.randperm(N, generator=g)[:n_out]
+        signs = torch.where(torch.rand(n_out, generator=g) < 0.5, -1.0, 1.0)
+        x[:, cols] = signs * 300.0
+    else:
+        raise KeyError(w.recipe)
+    out = {"x": x}
+    if w.op == "ln":
+        out["gamma"] = torch.rand(N, generator=g) + 0.5
+        out["beta"] = torch.rand(N, generator=g) * 0.2 - 0.1
+    else:
+        out["w"] = torch.rand(N, generator=g)
+    return {k: v.to(w.torch_dtype).contiguous() for k, v in out.items()}
+
+
+def lattice(rows: int, N: int, row0: int = 0, device="cpu", dtype=torch.float32) -> torch.Tensor:
+    """Deterministic counter-based pattern for inputs too large to draw on the
+    host: value(r, c) = ((r*7919 + c*104729) mod 65536)/16384 + 1, in [1, 5), computed
+    in exact int64 arithmetic, so the host and the device produce bit-identical
+    rows. Used for sampled checks of very large launches."""
+    r = torch.arange(row0, row0 + rows, device=device, dtype=torch.int64).unsqueeze(1)
+    c = torch.arange(N, device=device, dtype=torch.int64).unsqueeze(0)
+    v = (r * 7919 + c * 104729) % 65536
+    return (v.to(torch.float32) / 16384.0 + 1.0).to(dtype)

@@ -1,0 +1,350 @@
+"""Pins for the fp64 CPU oracle: each check ties it to something other than
+itself (the pages' worked examples, closed forms, exact rational arithmetic,
+an independent library routine, or invariants of the definition), chosen so
+that a dropped term, a wrong sign, a wrong index, a swapped gamma/beta, an
+N-1 divisor or a missing eps fails at least one of them. CPU only."""
+import itertools
+import math
+import random
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+
+# ---------------------------------------------------------------- worked examples
+
+def test_series_true_variance(golden):
+    """'第 7 章 LayerNorm 与 RMSNorm' §7.3: mean 1000.0055, var 8.25e-6."""
+    g = golden("series_1000.txt")
+    x = np.array(g["values"], np.float64)
+    mean, var = oracle.row_moments(x)
+    assert abs(mean - g["mean"][0]) <= 1e-9
+    assert abs(var - g["var"][0]) <= 1e-15
+
+
+def test_series_fp32_inputs_exact(golden):
+    """The same series rounded to fp32 first: the oracle's fp32-input path
+    equals the exact rational moments of those fp32 values."""
+    xs = np.array(golden("series_1000.txt")["values"], np.float32)
+    fr = [Fraction(float(v)) for v in xs]
+    mu = sum(fr) / len(fr)
+    var = sum((v - mu) ** 2 for v in fr) / len(fr)
+    m, v = oracle.row_moments(xs)
+    assert abs(m - float(mu)) <= 1e-12
+    assert abs(v - float(var)) <= 1e-12 * float(var)
+    # the fp32 rounding of the inputs moves the variance off 8.25e-6
+    assert abs(float(var) - 8.248128e-6) < 1e-12
+
+
+def _naive_f32_var(values):
+    """E[x^2] - E[x]^2 with every operation rounded to fp32 (the formula the
+    pages forbid); used only as a negative control."""
+    s = np.float32(0)
+    q = np.float32(0)
+    for v in values:
+        s = np.float32(s + v)
+        q = np.float32(q + np.float32(v * v))
+    n = np.float32(len(values))
+    m = np.float32(s / n)
+    return float(np.float32(np.float32(q / n) - np.float32(m * m)))
+
+
+def test_series_naive_fp32_negative_control(golden):
+    """The naive fp32 formula gives only 0 or 0.25 on the series (§7.3), far
+    outside any tolerance the parity tests use, while the oracle is exact."""
+    g = golden("series_1000.txt")
+    xs = [np.float32(v) for v in g["values"]]
+    rng = random.Random(0)
+    seen = set()
+    for _ in range(500):
+        rng.shuffle(xs)
+        seen.add(_naive_f32_var(xs))
+    assert seen <= set(g["naive_f32_outcomes"])
+    _, var = oracle.row_moments(np.array(xs, np.float32))
+    for bad in seen:
+        assert abs(bad - var) > 0.5 * var
+
+
+def test_mask_example(golden):
+    """'T3 讲解' §②, trap 1: N=5 gives var 1.2; the unmasked padded sum 10.8."""
+    g = golden("mask_n5.txt")
+    x = np.array(g["values"], np.float64)
+    mean, var = oracle.row_moments(x)
+    assert mean == g["mean"][0]
+    assert abs(var - g["var"][0]) <= 1e-15
+    # negative control: the padding bug the page describes
+    pad = np.zeros(int(g["block_n"][0]))
+    pad[: x.size] = x
+    unmasked = float(np.sum((pad - pad.sum() / x.size) ** 2) / x.size)
+    assert abs(unmasked - g["unmasked_var"][0]) <= 1e-12
+    assert abs(unmasked - var) > 1.0
+
+
+# ---------------------------------------------------------------- Welford / Chan
+
+def _two_pass(vals):
+    mu = sum(vals) / len(vals)
+    return mu, sum((v - mu) ** 2 for v in vals) / len(vals)
+
+
+def _trees(items):
+    """Every binary merge tree over `items` in the given leaf order."""
+    if len(items) == 1:
+        yield items[0]
+        return
+    for k in range(1, len(items)):
+        for left in _trees(items[:k]):
+            for right in _trees(items[k:]):
+                yield (left, right)
+
+
+def _eval_tree(t):
+    if isinstance(t, tuple):
+        return oracle.chan_combine(_eval_tree(t[0]), _eval_tree(t[1]))
+    return oracle.welford_update(oracle.Welford(0.0, 0.0, 0.0), t)
+
+
+def test_welford_update_matches_two_pass():
+    rng = np.random.default_rng(1)
+    for N in range(1, 9):
+        for _ in range(20):
+            x = rng.normal(rng.uniform(-50, 50), rng.uniform(0.01, 5), N)
+            s = oracle.Welford(0.0, 0.0, 0.0)
+            for v in x:
+                s = oracle.welford_update(s, v)
+            mu, var = oracle.row_moments(x)
+            assert s.n == N
+            assert abs(s.mean - mu) <= 1e-12 * max(1.0, abs(mu))
+            assert abs(s.m2 / N - var) <= 1e-12 * max(var, 1e-300) + 1e-13
+
+
+def test_chan_combine_every_merge_order():
+    """Every permutation of the leaves and every tree shape reach the
+    two-pass result (the merge is a monoid, '第 7 章' §7.4.1)."""
+    rng = np.random.default_rng(2)
+    for N in range(1, 6):
+        x = list(rng.normal(10.0, 2.0, N))
+        mu, var = oracle.row_moments(np.array(x))
+        for perm in itertools.permutations(x):
+            for t in _trees(list(perm)):
+                s = _eval_tree(t)
+                assert s.n == N
+                assert abs(s.mean - mu) <= 1e-12 * abs(mu)
+                assert abs(s.m2 / N - var) <= 1e-11 * var
+
+
+def test_chan_combine_empty_is_identity():
+    a = oracle.Welford(3.0, 1.5, 2.0)
+    e = oracle.Welford(0.0, 0.0, 0.0)
+    for r in (oracle.chan_combine(a, e), oracle.chan_combine(e, a)):
+        assert (r.n, r.mean, r.m2) == (3.0, 1.5, 2.0)
+    r = oracle.chan_combine(e, e)
+    assert (r.n, r.mean, r.m2) == (0.0, 0.0, 0.0)
+
+
+# ---------------------------------------------------------------- closed forms
+
+@pytest.mark.parametrize("eps", [1e-5, 1e-6])
+@pytest.mark.parametrize("N", [1, 7, 4096])
+def test_constant_rows(eps, N):
+    """var = 0 exactly, rstd = eps^-1/2, LayerNorm y = beta exactly."""
+    rng = np.random.default_rng(N)
+    for c in (0.0, 1.0, -3.25, 812.5):
+        x = np.full((2, N), c, np.float32)
+        gamma = rng.uniform(0.5, 1.5, N).astype(np.float32)
+        beta = rng.uniform(-0.1, 0.1, N).astype(np.float32)
+        e = oracle.eps_as_f32(eps)
+        y, mean, rstd = oracle.ln_fwd(x, gamma, beta, e)
+        assert np.all(mean == c)
+        assert np.all(rstd == 1.0 / math.sqrt(e))
+        assert np.array_equal(y, np.broadcast_to(beta.astype(np.float64), y.shape))
+        yr, rr = oracle.rms_fwd(x, gamma, e)
+        assert np.allclose(rr, 1.0 / math.sqrt(c * c + e), rtol=1e-15)
+
+
+def test_textbook_cases():
+    # [0, 2]: mean 1, var 1; with gamma=1, beta=0, eps=0 the output is [-1, 1]
+    x = np.array([[0.0, 2.0]])
+    one, zero = np.ones(2), np.zeros(2)
+    y, mean, rstd = oracle.ln_fwd(x, one, zero, 0.0)
+    assert mean[0] == 1.0 and rstd[0] == 1.0 and list(y[0]) == [-1.0, 1.0]
+    # RMS of a row of +-a is 1/sqrt(a^2 + eps) whatever the signs
+    a, eps = 3.0, 1e-6
+    x = np.array([[a, -a, -a, a, a]])
+    w = np.array([1.0, 2.0, 0.5, 1.0, -1.0])
+    y, rstd = oracle.rms_fwd(x, w, eps)
+    r = 1.0 / math.sqrt(a * a + eps)
+    assert abs(rstd[0] - r) <= 1e-16
+    assert np.allclose(y[0], x[0] * r * w, rtol=1e-15, atol=0)
+
+
+@pytest.mark.parametrize("N", [2, 3, 10, 257, 1000])
+def test_arithmetic_progression_closed_form(N):
+    """x_i = a + b*i: mean = a + b(N-1)/2, var = b^2 (N^2-1)/12."""
+    a, b = 3.0, 0.5
+    x = a + b * np.arange(N, dtype=np.float64)
+    mean, var = oracle.row_moments(x)
+    assert abs(mean - (a + b * (N - 1) / 2)) <= 1e-13 * abs(mean)
+    assert abs(var - b * b * (N * N - 1) / 12) <= 1e-13 * var
+
+
+def test_exact_rational_tiny_rows():
+    """Brute force: moments of random fp32 rows in exact rational arithmetic."""
+    rng = np.random.default_rng(3)
+    for N in range(1, 13):
+        for _ in range(10):
+            x = rng.normal(rng.uniform(-1000, 1000), rng.uniform(1e-3, 10), N).astype(np.float32)
+            fr = [Fraction(float(v)) for v in x]
+            mu = sum(fr) / N
+            var = sum((v - mu) ** 2 for v in fr) / N
+            m, v = oracle.row_moments(x)
+            assert abs(m - float(mu)) <= 1e-15 * abs(float(mu)) + 1e-300
+            assert abs(v - float(var)) <= 1e-9 * float(var) + 1e-18
+
+
+# ---------------------------------------------------------------- library routine
+
+@pytest.mark.parametrize("N", [1, 5, 33, 1000, 4099])
+def test_ln_matches_torch_fp64(N):
+    """Independent library routine: torch's CPU LayerNorm in fp64 returns the
+    same y, mean and rstd (its mean/rstd via native_layer_norm)."""
+    g = torch.Generator().manual_seed(N)
+    x = torch.randn(6, N, generator=g, dtype=torch.float64) * 4 + 7
+    gamma = torch.rand(N, generator=g, dtype=torch.float64) + 0.5
+    beta = torch.rand(N, generator=g, dtype=torch.float64) - 0.5
+    eps = 1e-5
+    y_t, mean_t, rstd_t = torch.native_layer_norm(x, [N], gamma, beta, eps)
+    y, mean, rstd = oracle.ln_fwd(x.numpy(), gamma.numpy(), beta.numpy(), eps)
+    assert np.allclose(y, y_t.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(mean, mean_t.numpy().ravel(), rtol=1e-13, atol=1e-13)
+    assert np.allclose(rstd, rstd_t.numpy().ravel(), rtol=1e-12, atol=0)
+
+
+@pytest.mark.parametrize("N", [1, 5, 64, 4099])
+def test_rms_matches_torch_fp64(N):
+    if not hasattr(torch.nn.functional, "rms_norm"):
+        pytest.skip("torch without F.rms_norm")
+    g = torch.Generator().manual_seed(100 + N)
+    x = torch.rand(6, N, generator=g, dtype=torch.float64) * 2 - 1
+    w = torch.rand(N, generator=g, dtype=torch.float64)
+    eps = 1e-6
+    y_t = torch.nn.functional.rms_norm(x, [N], w, eps)
+    y, rstd = oracle.rms_fwd(x.numpy(), w.numpy(), eps)
+    assert np.allclose(y, y_t.numpy(), rtol=1e-12, atol=1e-13)
+    ms = (x * x).mean(dim=1)
+    assert np.allclose(rstd, (1.0 / torch.sqrt(ms + eps)).numpy(), rtol=1e-13)
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_ln_invariants_and_affine_roles():
+    """gamma scales and beta shifts (not the other way round); with gamma=1,
+    beta=0 each row has mean 0 and mean square var/(var+eps)."""
+    rng = np.random.default_rng(4)
+    M, N, eps = 5, 300, 1e-5
+    x = rng.normal(2.0, 0.01, (M, N))
+    one, zero = np.ones(N), np.zeros(N)
+    xhat, mean, rstd = oracle.ln_fwd(x, one, zero, eps)
+    var = 1.0 / rstd ** 2 - eps
+    assert np.allclose(xhat.mean(axis=1), 0.0, atol=1e-12)
+    assert np.allclose((xhat ** 2).mean(axis=1), var / (var + eps), rtol=1e-12)
+    gamma = rng.uniform(0.5, 1.5, N)
+    beta = rng.uniform(-0.1, 0.1, N)
+    y, _, _ = oracle.ln_fwd(x, gamma, beta, eps)
+    assert np.allclose(y, xhat * gamma + beta, rtol=1e-13, atol=1e-14)
+    # shifting the row leaves the normalised output unchanged
+    y2, mean2, rstd2 = oracle.ln_fwd(x + 1000.0, gamma, beta, eps)
+    assert np.allclose(mean2, mean + 1000.0, rtol=1e-15)
+    assert np.allclose(y2, y, atol=1e-8)
+
+
+def test_rms_invariants():
+    """w=1: mean of y^2 is ms/(ms+eps); scaling x by k>0 and eps by k^2
+    leaves y unchanged; no mean is subtracted."""
+    rng = np.random.default_rng(5)
+    M, N, eps = 4, 513, 1e-6
+    x = rng.uniform(-1, 1, (M, N)) + 5.0
+    y, rstd = oracle.rms_fwd(x, np.ones(N), eps)
+    ms = (x ** 2).mean(axis=1)
+    assert np.allclose((y ** 2).mean(axis=1), ms / (ms + eps), rtol=1e-12)
+    assert np.all(y > 0)  # a positive row stays positive: nothing was subtracted
+    y2, _ = oracle.rms_fwd(x * 8.0, np.ones(N), eps * 64.0)
+    assert np.allclose(y2, y, rtol=1e-13)
+
+
+def test_dtypes_widen_exactly():
+    vals = np.array([[1.0, 2.0, -0.5, 3.75]], np.float32)
+    bits = (vals.view(np.uint32) >> 16).astype(np.uint16)  # exact in bf16
+    g = np.array([1.5, 0.5, 1.0, 2.0], np.float32)
+    b = np.array([0.25, -0.125, 0.0, 1.0], np.float32)
+    gb = (g.view(np.uint32) >> 16).astype(np.uint16)
+    bb = (b.view(np.uint32) >> 16).astype(np.uint16)
+    r32 = oracle.ln_fwd(vals, g, b, 1e-5)
+    r16 = oracle.ln_fwd(bits, gb, bb, 1e-5)
+    r64 = oracle.ln_fwd(vals.astype(np.float64), g.astype(np.float64), b.astype(np.float64), 1e-5)
+    for a, c, d in zip(r32, r16, r64):
+        assert np.array_equal(a, c) and np.array_equal(a, d)
+
+
+# ---------------------------------------------------------------- rounding
+
+def _bf16_to_f64(bits):
+    return (np.asarray(bits, np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def test_round_bf16_ties_and_specials():
+    cases = [
+        (1.0, 0x3F80),
+        (1.0 + 2.0 ** -8, 0x3F80),                 # tie -> even (down)
+        (1.0 + 3 * 2.0 ** -8, 0x3F82),             # tie -> even (up)
+        (-(1.0 + 2.0 ** -8), 0xBF80),
+        (1.0 + 2.0 ** -8 + 2.0 ** -30, 0x3F81),    # just above the tie
+        (0.0, 0x0000),
+        (-0.0, 0x8000),
+        (2.0 ** -133, 0x0001),                     # smallest bf16 subnormal
+        (2.0 ** -134, 0x0000),                     # half of it: tie -> even (zero)
+        (3 * 2.0 ** -134, 0x0002),
+        (float("inf"), 0x7F80),
+        (-float("inf"), 0xFF80),
+        (3.3961e38, 0x7F7F),                       # below the overflow midpoint
+        ((2 - 2.0 ** -8) * 2.0 ** 127, 0x7F80),    # the midpoint: tie -> even = inf
+        (3.3963e38, 0x7F80),                       # past the midpoint
+        (3.3895313892515355e38, 0x7F7F),           # largest finite bf16
+    ]
+    got = oracle.round_bf16(np.array([v for v, _ in cases]))
+    assert [int(v) for v in got] == [b for _, b in cases]
+    assert int(oracle.round_bf16(np.array([float("nan")]))[0]) & 0x7FC0 == 0x7FC0
+
+
+def test_round_bf16_matches_torch_on_fp32_values():
+    """Library routine: torch's fp32->bf16 conversion is round-to-nearest-even."""
+    rng = np.random.default_rng(6)
+    bits = rng.integers(0, 2 ** 32, 200000, dtype=np.uint64).astype(np.uint32)
+    f = bits.view(np.float32)
+    f = f[np.isfinite(f) & (np.abs(f) < 3.38e38)]
+    t = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    o = oracle.round_bf16(f.astype(np.float64))
+    assert np.array_equal(o, t)
+
+
+def test_round_bf16_nearest_on_doubles():
+    """Doubles with more bits than fp32: the result is the nearest bf16 (ties
+    to an even last bit), checked against both neighbours."""
+    rng = np.random.default_rng(7)
+    v = rng.normal(0, 1, 50000) * np.exp2(rng.integers(-30, 30, 50000))
+    r = _bf16_to_f64(oracle.round_bf16(v))
+    # ulp of the binade of |v|
+    ulp = np.exp2(np.floor(np.log2(np.abs(v))) - 7)
+    assert np.all(np.abs(v - r) <= ulp / 2)
+    tie = np.abs(v - r) == ulp / 2
+    assert np.all((oracle.round_bf16(v[tie]) & 1) == 0)
+
+
+def test_round_f32_matches_numpy():
+    rng = np.random.default_rng(8)
+    v = rng.normal(0, 1, 100000) * np.exp2(rng.integers(-60, 60, 100000))
+    assert np.array_equal(oracle.round_f32(v), v.astype(np.float32))
