@@ -1,0 +1,451 @@
+#!/usr/bin/env python3
+"""Throughput of the row-wise LayerNorm / RMSNorm forward on GB300.
+
+One step = one forward call over the benchmark workload (RMSNorm fp32,
+B=8 T=1024 C=4096: M=8192 rows of N=4096), inputs resident in HBM. Several
+input/output sets are rotated so that no call finds its operands in L2.
+The line printed reports achieved HBM GB/s of algorithmic bytes (read x,
+write y, read the parameters, write 8 B/row of statistics for LayerNorm),
+its fraction of the measured copy bandwidth, µs per call, the end-to-end
+figure with host buffers, and the CPU oracle timed on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libnorm|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+CLOCK_FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", default="libnorm", choices=["libnorm", "reference"])
+    p.add_argument("--workload", default=None)
+    p.add_argument("--e2e-steps", type=int, default=30)
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-table", action="store_true", help="skip the per-workload table")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "row_wise_normalization_ln_gb300", "csrc", "*")))
+    files.append(os.path.join(ROOT, "include", "libnorm.h"))
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(workload: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the kernel sources as they are now."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)[workload]
+    except (OSError, KeyError, ValueError):
+        return None
+    return t["dram_bytes_per_launch"] if t.get("kernel_hash") == kernel_source_hash() else None
+
+
+def kernel_name(w, plan) -> str:
+    kind = "group" if plan["mapping"] == 0 else "cta"
+    t = "float" if w.dtype == "f32" else "__nv_bfloat16"
+    return f"norm_fwd_{kind}<{t},{plan['vec_elems']},{plan['per_thread']},{'LN' if w.op == 'ln' else 'RMS'}>"
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = os.path.join("/tmp", f"libnorm_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.25)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                if self.uuid and self.uuid not in parts[0]:
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        reasons = set()
+        for r in rows:
+            for name, col in (("hw_slowdown", 5), ("hw_thermal_slowdown", 6), ("sw_thermal_slowdown", 7),
+                              ("sw_power_cap", 8)):
+                if r[col].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(rows[0][2]),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+# ------------------------------------------------------------------ the GPU arm
+
+def make_sets(w, inp, n_sets, device):
+    import torch
+    sets = []
+    for _ in range(n_sets):
+        s = {"x": inp["x"].to(device), "y": torch.empty(w.M, w.N, dtype=w.torch_dtype, device=device)}
+        if w.op == "ln":
+            s["mean"] = torch.empty(w.M, dtype=torch.float32, device=device)
+            s["rstd"] = torch.empty(w.M, dtype=torch.float32, device=device)
+        sets.append(s)
+    params = {k: v.to(device) for k, v in inp.items() if k != "x"}
+    return sets, params
+
+
+def step_fn(w, rn, params):
+    if w.op == "ln":
+        g, b = params["gamma"], params["beta"]
+
+        def f(s):
+            rn.ln_fwd(s["x"], g, b, w.eps, out=s["y"], mean=s["mean"], rstd=s["rstd"])
+    else:
+        wt = params["w"]
+
+        def f(s):
+            rn.rms_fwd(s["x"], wt, w.eps, out=s["y"])
+    return f
+
+
+def n_sets_for(w):
+    per_set = 2 * w.M * w.N * w.elem_size
+    return max(3, math.ceil(3 * L2_BYTES / per_set))
+
+
+def time_launches(w, rn, inp, device, steps, warmup, sampler=None, barrier=None):
+    """Run `steps` calls with CUDA events around each; returns (total_ms,
+    per-launch ms list, clock summary)."""
+    import torch
+    sets, params = make_sets(w, inp, n_sets_for(w), device)
+    f = step_fn(w, rn, params)
+    for i in range(warmup):
+        f(sets[i % len(sets)])
+    stream = torch.cuda.current_stream(device)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    if barrier:
+        barrier()
+    clocks = None
+    ctx = sampler if sampler is not None else _Null()
+    with ctx:
+        t0.record(stream)
+        for i in range(steps):
+            starts[i].record(stream)
+            f(sets[i % len(sets)])
+            ends[i].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(device)
+    if barrier:
+        barrier()
+    if sampler is not None:
+        clocks = sampler.summary()
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total = t0.elapsed_time(t1)
+    del sets
+    torch.cuda.empty_cache()
+    return total, per, clocks
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def time_e2e(w, rn, inp, device, steps):
+    """Host buffers in, host buffers out: H2D of x and the parameters, the
+    call, D2H of y (and the statistics), every step, on one stream."""
+    import torch
+    hx = inp["x"].pin_memory()
+    hp = {k: v.pin_memory() for k, v in inp.items() if k != "x"}
+    dx = torch.empty_like(hx, device=device)
+    dp = {k: torch.empty_like(v, device=device) for k, v in hp.items()}
+    dy = torch.empty_like(dx)
+    hy = torch.empty_like(hx).pin_memory()
+    ln = w.op == "ln"
+    if ln:
+        dm = torch.empty(w.M, dtype=torch.float32, device=device)
+        dr = torch.empty_like(dm)
+        hm = torch.empty(w.M, dtype=torch.float32).pin_memory()
+        hr = torch.empty_like(hm).pin_memory()
+    h2d = hx.numel() * hx.element_size() + sum(v.numel() * v.element_size() for v in hp.values())
+    d2h = hy.numel() * hy.element_size() + (8 * w.M if ln else 0)
+
+    def one():
+        dx.copy_(hx, non_blocking=True)
+        for k in hp:
+            dp[k].copy_(hp[k], non_blocking=True)
+        if ln:
+            rn.ln_fwd(dx, dp["gamma"], dp["beta"], w.eps, out=dy, mean=dm, rstd=dr)
+            hm.copy_(dm, non_blocking=True)
+            hr.copy_(dr, non_blocking=True)
+        else:
+            rn.rms_fwd(dx, dp["w"], w.eps, out=dy)
+        hy.copy_(dy, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize(device)
+    stream = torch.cuda.current_stream(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        one()
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = t0.elapsed_time(t1) / steps
+    return ms, h2d, d2h
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_rows(w, inp, rows: int):
+    """One call of the fp64 oracle over the first `rows` rows."""
+    import numpy as np
+    import oracle
+
+    def npx(t):
+        import torch
+        t = t.contiguous()
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+
+    x = npx(inp["x"][:rows])
+    if w.op == "ln":
+        return lambda: oracle.ln_fwd(x, npx(inp["gamma"]), npx(inp["beta"]), oracle.eps_as_f32(w.eps))
+    return lambda: oracle.rms_fwd(x, npx(inp["w"]), oracle.eps_as_f32(w.eps))
+
+
+def cpu_baseline(w, inp, seconds: float):
+    """The oracle as it stands, single-threaded, over whole passes of the
+    workload until about `seconds` have elapsed."""
+    run = oracle_rows(w, inp, w.M)
+    passes = 0
+    t0 = time.perf_counter()
+    while True:
+        run()
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    gbs = w.algorithmic_bytes() * passes / el / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{passes} full pass(es) of {w.M}x{w.N} {w.dtype} in {el:.1f} s, fp64, 1 thread",
+            "host_cores": os.cpu_count()}
+
+
+# ------------------------------------------------------------------ main
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def run_reference(args, w):
+    """The reference arm: the fp64 CPU oracle (the only reference this
+    method has), on this host's cores, same workload, metric and unit."""
+    import torch
+    from row_wise_normalization_ln_gb300 import workloads as wl
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    inp = wl.generate(w)
+    probe_rows = max(1, min(w.M, 64))
+    t0 = time.perf_counter()
+    oracle_rows(w, inp, probe_rows)()
+    per_row = (time.perf_counter() - t0) / probe_rows
+    budget = 90.0
+    rows = max(1, min(w.M, int(budget / (args.steps + args.warmup) / per_row)))
+    run = oracle_rows(w, inp, rows)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    el = time.perf_counter() - t0
+    gbs = w.algorithmic_bytes(rows) * args.steps / el / 1e9
+    line = {
+        "impl": "reference", "metric": "LN/RMSNorm fwd achieved HBM GB/s", "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "op": w.op, "io_dtype": w.dtype, "eps": w.eps,
+                   "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{rows} of {w.M} rows per step, fp64, 1 thread"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    from row_wise_normalization_ln_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload or wl.BENCH_WORKLOAD]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    import row_wise_normalization_ln_gb300 as rn
+    rn.library()  # fails loudly if the CUDA library is not built
+    rank, world, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+        barrier = dist.barrier
+
+    # Weak scaling: every rank normalises its own full workload (rows are
+    # independent, so a row-sharded job needs no exchange at all).
+    inp = wl.generate(w)
+    props = torch.cuda.get_device_properties(device)
+    uuid = str(getattr(props, "uuid", "")) or None
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    total_ms, per, clocks = time_launches(w, rn, inp, device, args.steps, args.warmup, sampler, barrier)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    bytes_per_call = w.algorithmic_bytes()
+    ms_per_step = total_ms / args.steps
+    value = bytes_per_call * args.steps * world / (total_ms / 1e3) / 1e9
+    kern_ms = statistics.mean(per)
+    achieved = bytes_per_call / (kern_ms / 1e3) / 1e9
+    peak, peak_src = measured_peak()
+    traffic = ncu_traffic(w.name)
+
+    e2e_ms, h2d, d2h = time_e2e(w, rn, inp, device, args.e2e_steps)
+
+    table = None
+    if not args.no_table and rank == 0:
+        table = {}
+        for name, wk in wl.WORKLOADS.items():
+            wi = inp if name == w.name else wl.generate(wk)
+            tot, pl, _ = time_launches(wk, rn, wi, device, 300, 20)
+            us = statistics.median(pl) * 1e3
+            gbs = wk.algorithmic_bytes() / (us / 1e6) / 1e9
+            table[name] = {"us_median": round(us, 3), "us_mean": round(statistics.mean(pl) * 1e3, 3),
+                           "GBps": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4),
+                           "rows_per_s": round(wk.M / (us / 1e6)), "plan": rn.make_plan(
+                               wk.M, wk.N, wk.torch_dtype, True, props.multi_processor_count)}
+            del wi
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    cpu = cpu_baseline(w, inp, args.cpu_seconds)
+    line = {
+        "metric": "LN/RMSNorm fwd achieved HBM GB/s", "value": round(value, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "us_per_call": round(kern_ms * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "op": w.op, "M": w.M, "N": w.N, "io_dtype": w.dtype, "eps": w.eps,
+                   "algorithmic_bytes_per_call": bytes_per_call,
+                   "l2": f"{n_sets_for(w)} rotating input/output sets of {2 * w.M * w.N * w.elem_size >> 20} MiB "
+                         f"(> L2 between reuses)",
+                   "parallelism": f"replicas x{world} (rows independent)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": traffic,
+                     "kernel": kernel_name(w, rn.make_plan(w.M, w.N, w.torch_dtype, True, props.multi_processor_count)),
+                     "kernel_hash": kernel_source_hash()},
+        "e2e": {"value": round(bytes_per_call / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "workloads": table,
+        "gpu": props.name,
+    }
+    if w.dtype == "bf16":
+        line["dtype"] = "bf16 io, f32 compute"
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

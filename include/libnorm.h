@@ -1,0 +1,143 @@
+/*
+ * libnorm - row-wise LayerNorm and RMSNorm forward for NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations (page title, section):
+ *   [Ch7]  "第 7 章 LayerNorm 与 RMSNorm" (CUDA 算子工程): §7.1 LayerNorm
+ *          definition, §7.4 Welford, §7.4.1 parallel merge, §7.5 RMSNorm,
+ *          §7.6 fused kernel structure (per-row statistics, mean/rstd saved).
+ *   [RMS2] "CUDA算子优化(2)：RMSNorm": §1 formula, §2 [B*T, C] layout.
+ *   [T3]   "T3 讲解：LayerNorm / RMSNorm 的 forward": §② masking, biased
+ *          variance, fp32 statistics; §④ host reshape to [M, N].
+ *
+ * Conventions shared by every entry point:
+ *   - All pointers are DEVICE pointers on the current CUDA device, owned by
+ *     the caller. The library allocates nothing and keeps no state between
+ *     calls; work is enqueued asynchronously on `stream` (NULL = the legacy
+ *     default stream). The caller keeps buffers alive until the stream has
+ *     finished the call.
+ *   - x and y are [M, N] row-major and contiguous (row stride N elements).
+ *     gamma, beta and w are [N]. x, y, gamma, beta and w all have the element
+ *     type `dtype`; mean and rstd are always fp32 [M] ([T3] §⑥).
+ *   - Statistics and all arithmetic are fp32; bf16 inputs are widened
+ *     exactly and bf16 outputs are rounded to nearest-even.
+ *   - y may equal x exactly (in place). Any other overlap between outputs and
+ *     inputs, or between outputs, is undefined.
+ *   - Pointers need no particular alignment. When x, y and the parameter
+ *     vectors are 16-byte aligned and a row is a multiple of 16 bytes, the
+ *     kernels use 128-bit accesses; otherwise they use element accesses.
+ *   - Argument errors are detected on the host before any CUDA call and
+ *     nothing is launched. M == 0 is a no-op that returns NORM_OK (pointers
+ *     may then be NULL). Limits: 1 <= N <= 2^24 (the largest count fp32
+ *     holds exactly, [Ch7] §7.8), M >= 0, M*N < 2^63, eps finite and >= 0.
+ *   - A CUDA error during the device query or the launch returns
+ *     NORM_ERR_CUDA; norm_last_cuda_error() then gives the cudaError_t.
+ */
+#ifndef LIBNORM_H
+#define LIBNORM_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { NORM_F32 = 0, NORM_BF16 = 1 } norm_dtype;
+
+typedef enum {
+    NORM_OK = 0,
+    NORM_ERR_ARG = -1,    /* bad size, NULL pointer or eps */
+    NORM_ERR_DTYPE = -2,  /* dtype not one of norm_dtype */
+    NORM_ERR_CUDA = -3,   /* CUDA runtime error (device query or launch) */
+    NORM_ERR_PLAN = -4    /* an explicit plan is inconsistent with the call */
+} norm_status;
+
+/* How rows map onto the GPU. */
+typedef enum {
+    NORM_MAP_GROUP = 0,   /* `group` lanes of a warp own one row; a CTA of
+                             `threads` threads holds threads/group rows */
+    NORM_MAP_CTA = 1      /* `cluster` CTAs of `threads` threads own one row;
+                             statistics meet in shared memory, and across the
+                             cluster in distributed shared memory */
+} norm_mapping;
+
+/*
+ * A launch plan. Each thread keeps `per_thread` accesses of `vec_elems`
+ * elements of its row in registers. If one pass of the row's owners cannot
+ * hold the whole row (CTA mapping only), the row is walked in `rounds`
+ * register-sized rounds: x is read once for the statistics and the earlier
+ * rounds are read again for the output (served from L2 when they fit).
+ */
+typedef struct {
+    int32_t mapping;     /* norm_mapping */
+    int32_t vec_elems;   /* elements per access: 16/sizeof(element) or 1 */
+    int32_t per_thread;  /* accesses per thread per round: 1, 2, 4 or 8 */
+    int32_t group;       /* GROUP mapping: lanes per row, power of 2 <= 32 */
+    int32_t threads;     /* threads per CTA, multiple of 32, <= 1024 */
+    int32_t cluster;     /* CTA mapping: CTAs per row, 1, 2, 4 or 8 */
+    int32_t rounds;      /* derived by norm_make_plan; ignored on input */
+    int32_t reserved;
+    int64_t grid;        /* CTAs launched (a multiple of `cluster`); rows
+                            are walked in a grid-stride loop */
+} norm_plan;
+
+/*
+ * LayerNorm forward ([Ch7] §7.1, §7.6; [T3] §②):
+ *   mean_r = sum_i x_ri / N
+ *   var_r  = sum_i (x_ri - mean_r)^2 / N        (biased, never E[x^2]-E[x]^2)
+ *   rstd_r = 1 / sqrt(var_r + eps)
+ *   y_ri   = (x_ri - mean_r) * rstd_r * gamma_i + beta_i
+ * mean and rstd may each be NULL (not written). gamma and beta are required.
+ */
+norm_status ln_fwd(const void* x, const void* gamma, const void* beta, void* y,
+                   float* mean, float* rstd, int64_t M, int64_t N, float eps,
+                   norm_dtype dtype, cudaStream_t stream);
+
+/*
+ * RMSNorm forward ([Ch7] §7.5; [RMS2] §1; [T3] §③):
+ *   rstd_r = 1 / sqrt(sum_i x_ri^2 / N + eps)
+ *   y_ri   = x_ri * rstd_r * w_i
+ * No statistics are written.
+ */
+norm_status rms_fwd(const void* x, const void* w, void* y, int64_t M, int64_t N,
+                    float eps, norm_dtype dtype, cudaStream_t stream);
+
+/*
+ * The plan ln_fwd / rms_fwd would choose for M rows of N elements of
+ * `dtype` on a device with `num_sms` SMs, with `aligned16` != 0 when every
+ * pointer is 16-byte aligned. Host only: makes no CUDA call. Fills `plan`
+ * (including `rounds`) and returns NORM_OK, or an argument error.
+ */
+norm_status norm_make_plan(int64_t M, int64_t N, norm_dtype dtype, int aligned16,
+                           int num_sms, norm_plan* plan);
+
+/*
+ * ln_fwd / rms_fwd with an explicit plan (plan == NULL: choose as the plain
+ * calls do). The plan is checked against the call on the host; a plan whose
+ * accesses would not cover the row, whose vector width does not match the
+ * dtype and alignment, or whose shape is out of range returns NORM_ERR_PLAN
+ * and launches nothing. For tuning and for tests of every kernel variant.
+ */
+norm_status ln_fwd_planned(const void* x, const void* gamma, const void* beta, void* y,
+                           float* mean, float* rstd, int64_t M, int64_t N, float eps,
+                           norm_dtype dtype, cudaStream_t stream, const norm_plan* plan);
+
+norm_status rms_fwd_planned(const void* x, const void* w, void* y, int64_t M, int64_t N,
+                            float eps, norm_dtype dtype, cudaStream_t stream,
+                            const norm_plan* plan);
+
+/* Static description of a status code. */
+const char* norm_status_string(norm_status status);
+
+/* cudaError_t of the last NORM_ERR_CUDA returned on the calling thread
+ * (0 if none). */
+int norm_last_cuda_error(void);
+
+/* Version of this interface (bumped on any incompatible change). */
+int norm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBNORM_H */

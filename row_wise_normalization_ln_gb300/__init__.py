@@ -1,0 +1,199 @@
+"""GB300-native row-wise LayerNorm / RMSNorm forward: Python binding of the
+libnorm C ABI (include/libnorm.h).
+
+The binding only marshals arguments: it reshapes ``[..., N]`` inputs to
+``[M, N]`` rows (the T3 drill's host wrapper, §④), allocates outputs with
+torch, and passes raw device pointers and the current CUDA stream to the
+C library. Every step of the computation runs in the library's CUDA
+kernels; there is no fallback. If ``libnorm.so`` has not been built the
+first call raises ``LibraryNotBuilt``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "ln_fwd", "rms_fwd", "make_plan", "NormPlan", "NormError", "LibraryNotBuilt", "library",
+    "NORM_F32", "NORM_BF16", "NORM_MAP_GROUP", "NORM_MAP_CTA",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnorm.so")
+
+NORM_F32, NORM_BF16 = 0, 1
+NORM_OK, NORM_ERR_ARG, NORM_ERR_DTYPE, NORM_ERR_CUDA, NORM_ERR_PLAN = 0, -1, -2, -3, -4
+NORM_MAP_GROUP, NORM_MAP_CTA = 0, 1
+
+
+class NormPlan(ctypes.Structure):
+    """Mirror of ``norm_plan`` in include/libnorm.h."""
+    _fields_ = [
+        ("mapping", ctypes.c_int32),
+        ("vec_elems", ctypes.c_int32),
+        ("per_thread", ctypes.c_int32),
+        ("group", ctypes.c_int32),
+        ("threads", ctypes.c_int32),
+        ("cluster", ctypes.c_int32),
+        ("rounds", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("grid", ctypes.c_int64),
+    ]
+
+    def as_dict(self) -> dict:
+        return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
+
+    @classmethod
+    def from_dict(cls, d: dict) -> "NormPlan":
+        p = cls()
+        for k, v in d.items():
+            setattr(p, k, int(v))
+        return p
+
+
+class NormError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = library().norm_status_string(status).decode()
+        if status == NORM_ERR_CUDA:
+            msg += f" (cudaError {library().norm_last_cuda_error()})"
+        super().__init__(f"{what}: {msg} [status {status}]")
+
+
+class LibraryNotBuilt(ImportError):
+    pass
+
+
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """The loaded libnorm.so with its C signatures declared."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise LibraryNotBuilt(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64, f32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+    L.ln_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, f32, i32, vp]
+    L.rms_fwd.argtypes = [vp, vp, vp, i64, i64, f32, i32, vp]
+    L.ln_fwd_planned.argtypes = L.ln_fwd.argtypes + [ctypes.POINTER(NormPlan)]
+    L.rms_fwd_planned.argtypes = L.rms_fwd.argtypes + [ctypes.POINTER(NormPlan)]
+    L.norm_make_plan.argtypes = [i64, i64, i32, i32, i32, ctypes.POINTER(NormPlan)]
+    for f in ("ln_fwd", "rms_fwd", "ln_fwd_planned", "rms_fwd_planned", "norm_make_plan",
+              "norm_last_cuda_error", "norm_abi_version"):
+        getattr(L, f).restype = ctypes.c_int
+    L.norm_status_string.argtypes = [ctypes.c_int]
+    L.norm_status_string.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return NORM_F32
+    if t == torch.bfloat16:
+        return NORM_BF16
+    raise TypeError(f"libnorm supports float32 and bfloat16, got {t}")
+
+
+def make_plan(M: int, N: int, dtype: torch.dtype, aligned: bool = True, num_sms: int = 152) -> dict:
+    """The launch plan the library would choose (host-only, no CUDA call)."""
+    p = NormPlan()
+    st = library().norm_make_plan(M, N, _dtype_code(dtype), int(aligned), num_sms, ctypes.byref(p))
+    if st != NORM_OK:
+        raise NormError(st, "norm_make_plan")
+    return p.as_dict()
+
+
+def _rows(x: torch.Tensor) -> torch.Tensor:
+    if x.dim() == 0:
+        raise ValueError("input must have at least one dimension")
+    x2 = x.reshape(-1, x.shape[-1])
+    return x2 if x2.is_contiguous() else x2.contiguous()
+
+
+def _param(p: torch.Tensor, x: torch.Tensor, name: str) -> torch.Tensor:
+    if p.device != x.device or p.dtype != x.dtype:
+        raise ValueError(f"{name} must be on {x.device} with dtype {x.dtype}")
+    if p.numel() != x.shape[-1]:
+        raise ValueError(f"{name} must have {x.shape[-1]} elements, got {p.numel()}")
+    return p.reshape(-1).contiguous()
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device: torch.device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def _plan_ptr(plan):
+    if plan is None:
+        return None
+    p = plan if isinstance(plan, NormPlan) else NormPlan.from_dict(plan)
+    return ctypes.byref(p)
+
+
+def ln_fwd(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float = 1e-5, *,
+           out: Optional[torch.Tensor] = None, mean: Optional[torch.Tensor] = None,
+           rstd: Optional[torch.Tensor] = None, stats: bool = True,
+           stream: Optional[torch.cuda.Stream] = None, plan=None):
+    """LayerNorm forward over the last dimension of a CUDA tensor.
+
+    Returns ``(y, mean, rstd)``; mean and rstd are fp32 ``[M]`` (None when
+    ``stats=False``). ``out`` may be ``x`` itself (in place)."""
+    if not x.is_cuda:
+        raise ValueError("ln_fwd needs a CUDA tensor")
+    code = _dtype_code(x.dtype)
+    x2 = _rows(x)
+    M, N = x2.shape
+    g = _param(gamma, x, "gamma")
+    b = _param(beta, x, "beta")
+    y = out if out is not None else torch.empty_like(x2)
+    if y.shape != x.shape and y.shape != x2.shape or not y.is_contiguous() or y.dtype != x.dtype:
+        raise ValueError("out must be a contiguous tensor of x's shape and dtype")
+    if stats:
+        mean = mean if mean is not None else torch.empty(M, device=x.device, dtype=torch.float32)
+        rstd = rstd if rstd is not None else torch.empty(M, device=x.device, dtype=torch.float32)
+        for t, n in ((mean, "mean"), (rstd, "rstd")):
+            if t.dtype != torch.float32 or t.numel() != M or not t.is_contiguous():
+                raise ValueError(f"{n} must be a contiguous fp32 tensor of {M} elements")
+    else:
+        mean = rstd = None
+    L = library()
+    args = (x2.data_ptr(), g.data_ptr(), b.data_ptr(), y.data_ptr(),
+            mean.data_ptr() if mean is not None else None,
+            rstd.data_ptr() if rstd is not None else None,
+            M, N, float(eps), code)
+    with torch.cuda.device(x.device):
+        h = _stream_handle(stream, x.device)
+        st = (L.ln_fwd(*args, h) if plan is None else L.ln_fwd_planned(*args, h, _plan_ptr(plan)))
+    if st != NORM_OK:
+        raise NormError(st, "ln_fwd")
+    return y.view(x.shape), mean, rstd
+
+
+def rms_fwd(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6, *, out: Optional[torch.Tensor] = None,
+            stream: Optional[torch.cuda.Stream] = None, plan=None) -> torch.Tensor:
+    """RMSNorm forward over the last dimension of a CUDA tensor."""
+    if not x.is_cuda:
+        raise ValueError("rms_fwd needs a CUDA tensor")
+    code = _dtype_code(x.dtype)
+    x2 = _rows(x)
+    M, N = x2.shape
+    wv = _param(w, x, "w")
+    y = out if out is not None else torch.empty_like(x2)
+    if y.shape != x.shape and y.shape != x2.shape or not y.is_contiguous() or y.dtype != x.dtype:
+        raise ValueError("out must be a contiguous tensor of x's shape and dtype")
+    L = library()
+    args = (x2.data_ptr(), wv.data_ptr(), y.data_ptr(), M, N, float(eps), code)
+    with torch.cuda.device(x.device):
+        h = _stream_handle(stream, x.device)
+        st = (L.rms_fwd(*args, h) if plan is None else L.rms_fwd_planned(*args, h, _plan_ptr(plan)))
+    if st != NORM_OK:
+        raise NormError(st, "rms_fwd")
+    return y.view(x.shape)

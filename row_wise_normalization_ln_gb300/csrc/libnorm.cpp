@@ -1,0 +1,260 @@
+// libnorm C ABI: argument checks, the launch planner (which mapping, access
+// width and register footprint a row gets) and dispatch to the kernels.
+//
+// Every argument error is caught here, before any CUDA call; nothing is
+// launched on an error. The library allocates no memory and keeps no state
+// between calls apart from a per-device cache of the SM count.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime_api.h>
+
+#include "libnorm.h"
+#include "norm_args.h"
+
+namespace {
+
+using libnorm::NormArgs;
+
+constexpr int64_t kMaxN = int64_t(1) << 24;  // fp32 counts are exact up to 2^24
+constexpr int64_t kMaxGrid = int64_t(1) << 30;
+constexpr int kMaxThreads = 1024;
+constexpr int kMaxCluster = 8;               // portable cluster size
+constexpr int kMaxPerThread = 8;
+
+thread_local int g_last_cuda_error = 0;
+
+bool dtype_ok(norm_dtype d) { return d == NORM_F32 || d == NORM_BF16; }
+int elem_size(norm_dtype d) { return d == NORM_BF16 ? 2 : 4; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
+int64_t pow2_ceil(int64_t v) {
+    int64_t p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks shared by every entry point; M == 0 is legal.
+norm_status check_sizes(int64_t M, int64_t N, norm_dtype dtype) {
+    if (!dtype_ok(dtype)) return NORM_ERR_DTYPE;
+    if (N < 1 || N > kMaxN || M < 0) return NORM_ERR_ARG;
+    if (M > INT64_MAX / N) return NORM_ERR_ARG;
+    return NORM_OK;
+}
+
+// Elements per access for this row shape: a 16-byte vector when every
+// pointer is 16-byte aligned and rows are whole vectors, else one element.
+int vec_for(int64_t N, norm_dtype dtype, bool all_aligned) {
+    const int s = elem_size(dtype);
+    return (all_aligned && (N * s) % 16 == 0) ? 16 / s : 1;
+}
+
+norm_status make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_aligned, int num_sms, norm_plan* p) {
+    std::memset(p, 0, sizeof *p);
+    const int vec = vec_for(N, dtype, all_aligned);
+    const int64_t nacc = ceil_div(N, vec);
+    const int64_t busy_threads = int64_t(num_sms) * 1024;  // half of the resident-thread capacity
+    p->vec_elems = vec;
+
+    // Short rows: a group of lanes per row, up to 8 accesses per lane.
+    if (nacc <= 32 * kMaxPerThread) {
+        int64_t g = pow2_ceil(ceil_div(nacc, kMaxPerThread));
+        if (g < 4) g = pow2_ceil(nacc < 4 ? nacc : 4);
+        if (g > 32) g = 32;
+        if (M * g >= busy_threads || nacc <= 32) {
+            p->mapping = NORM_MAP_GROUP;
+            p->group = static_cast<int32_t>(g);
+            p->per_thread = static_cast<int32_t>(pow2_ceil(ceil_div(nacc, g)));
+            p->threads = 256;
+            p->cluster = 1;
+            p->rounds = 1;
+            const int64_t rows_per_cta = p->threads / g;
+            p->grid = std::min<int64_t>(ceil_div(M, rows_per_cta), kMaxGrid);
+            if (p->grid < 1) p->grid = 1;
+            return NORM_OK;
+        }
+    }
+
+    // Longer rows (or too few rows to fill the GPU by groups): a CTA, or a
+    // cluster of CTAs, per row.
+    int per = 4;
+    int64_t threads = round_up(ceil_div(nacc, per), 32);
+    if (threads > kMaxThreads) {
+        per = kMaxPerThread;
+        threads = round_up(ceil_div(nacc, per), 32);
+    }
+    int64_t cluster = 1;
+    if (threads > kMaxThreads) {
+        cluster = pow2_ceil(ceil_div(nacc, int64_t(kMaxThreads) * per));
+        if (cluster > kMaxCluster) cluster = kMaxCluster;
+        threads = std::min<int64_t>(round_up(ceil_div(nacc, cluster * per), 32), kMaxThreads);
+    }
+    // Few rows: trade registers per thread for more threads per row.
+    while (per > 1 && M * cluster * threads < busy_threads) {
+        const int64_t t2 = round_up(ceil_div(nacc, cluster * (per / 2)), 32);
+        if (t2 > kMaxThreads) break;
+        per /= 2;
+        threads = t2;
+    }
+    if (threads < 32) threads = 32;
+    p->mapping = NORM_MAP_CTA;
+    p->per_thread = per;
+    p->threads = static_cast<int32_t>(threads);
+    p->cluster = static_cast<int32_t>(cluster);
+    p->group = 0;
+    p->rounds = static_cast<int32_t>(ceil_div(nacc, cluster * threads * per));
+    p->grid = std::max<int64_t>(std::min<int64_t>(M, kMaxGrid / cluster), 1) * cluster;
+    return NORM_OK;
+}
+
+// Validate an explicit plan against the call; derive `rounds`.
+norm_status check_plan(const norm_plan& in, int64_t N, norm_dtype dtype, bool all_aligned, norm_plan* out) {
+    norm_plan p = in;
+    const int s = elem_size(dtype);
+    if (p.mapping != NORM_MAP_GROUP && p.mapping != NORM_MAP_CTA) return NORM_ERR_PLAN;
+    if (p.vec_elems != 1) {
+        if (p.vec_elems != 16 / s || !all_aligned || (N * s) % 16 != 0) return NORM_ERR_PLAN;
+    }
+    if (!is_pow2(p.per_thread) || p.per_thread > kMaxPerThread) return NORM_ERR_PLAN;
+    if (p.threads < 32 || p.threads > kMaxThreads || p.threads % 32 != 0) return NORM_ERR_PLAN;
+    const int64_t nacc = ceil_div(N, p.vec_elems);
+    if (p.mapping == NORM_MAP_GROUP) {
+        if (!is_pow2(p.group) || p.group > 32) return NORM_ERR_PLAN;
+        if (int64_t(p.group) * p.per_thread < nacc) return NORM_ERR_PLAN;
+        p.cluster = 1;
+        p.rounds = 1;
+    } else {
+        if (!is_pow2(p.cluster) || p.cluster > kMaxCluster) return NORM_ERR_PLAN;
+        p.group = 0;
+        p.rounds = static_cast<int32_t>(ceil_div(nacc, int64_t(p.cluster) * p.threads * p.per_thread));
+    }
+    if (p.grid < p.cluster || p.grid > kMaxGrid || p.grid % p.cluster != 0) return NORM_ERR_PLAN;
+    *out = p;
+    return NORM_OK;
+}
+
+int device_sm_count() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = static_cast<int>(e);
+        return -1;
+    }
+    if (dev >= 0 && dev < 64) {
+        const int v = cache[dev].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess || n <= 0) {
+        g_last_cuda_error = static_cast<int>(e);
+        return -1;
+    }
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+using Launcher = cudaError_t (*)(const norm_plan&, const NormArgs&, cudaStream_t);
+
+norm_status run(bool ln, const NormArgs& a, norm_dtype dtype, bool all_aligned, cudaStream_t stream,
+                const norm_plan* user_plan) {
+    norm_plan plan;
+    if (user_plan) {
+        const norm_status st = check_plan(*user_plan, a.N, dtype, all_aligned, &plan);
+        if (st != NORM_OK) return st;
+    } else {
+        const int sms = device_sm_count();
+        if (sms <= 0) return NORM_ERR_CUDA;
+        make_plan(a.M, a.N, dtype, all_aligned, sms, &plan);
+    }
+    NormArgs args = a;
+    args.group = plan.group;
+    args.rounds = plan.rounds;
+    Launcher launch = ln ? (dtype == NORM_F32 ? libnorm::launch_ln_f32 : libnorm::launch_ln_bf16)
+                         : (dtype == NORM_F32 ? libnorm::launch_rms_f32 : libnorm::launch_rms_bf16);
+    const cudaError_t e = launch(plan, args, stream);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = static_cast<int>(e);
+        return NORM_ERR_CUDA;
+    }
+    return NORM_OK;
+}
+
+norm_status ln_impl(const void* x, const void* gamma, const void* beta, void* y, float* mean, float* rstd,
+                    int64_t M, int64_t N, float eps, norm_dtype dtype, cudaStream_t stream, const norm_plan* plan) {
+    norm_status st = check_sizes(M, N, dtype);
+    if (st != NORM_OK) return st;
+    if (!std::isfinite(eps) || eps < 0.f) return NORM_ERR_ARG;
+    if (M == 0) return NORM_OK;
+    if (!x || !gamma || !beta || !y) return NORM_ERR_ARG;
+    const bool al = aligned16(x) && aligned16(y) && aligned16(gamma) && aligned16(beta);
+    NormArgs a{x, gamma, beta, y, mean, rstd, M, static_cast<int32_t>(N), eps, 0, 1};
+    return run(true, a, dtype, al, stream, plan);
+}
+
+norm_status rms_impl(const void* x, const void* w, void* y, int64_t M, int64_t N, float eps, norm_dtype dtype,
+                     cudaStream_t stream, const norm_plan* plan) {
+    norm_status st = check_sizes(M, N, dtype);
+    if (st != NORM_OK) return st;
+    if (!std::isfinite(eps) || eps < 0.f) return NORM_ERR_ARG;
+    if (M == 0) return NORM_OK;
+    if (!x || !w || !y) return NORM_ERR_ARG;
+    const bool al = aligned16(x) && aligned16(y) && aligned16(w);
+    NormArgs a{x, w, nullptr, y, nullptr, nullptr, M, static_cast<int32_t>(N), eps, 0, 1};
+    return run(false, a, dtype, al, stream, plan);
+}
+
+}  // namespace
+
+extern "C" {
+
+norm_status ln_fwd(const void* x, const void* gamma, const void* beta, void* y, float* mean, float* rstd,
+                   int64_t M, int64_t N, float eps, norm_dtype dtype, cudaStream_t stream) {
+    return ln_impl(x, gamma, beta, y, mean, rstd, M, N, eps, dtype, stream, nullptr);
+}
+
+norm_status rms_fwd(const void* x, const void* w, void* y, int64_t M, int64_t N, float eps, norm_dtype dtype,
+                    cudaStream_t stream) {
+    return rms_impl(x, w, y, M, N, eps, dtype, stream, nullptr);
+}
+
+norm_status ln_fwd_planned(const void* x, const void* gamma, const void* beta, void* y, float* mean, float* rstd,
+                           int64_t M, int64_t N, float eps, norm_dtype dtype, cudaStream_t stream,
+                           const norm_plan* plan) {
+    return ln_impl(x, gamma, beta, y, mean, rstd, M, N, eps, dtype, stream, plan);
+}
+
+norm_status rms_fwd_planned(const void* x, const void* w, void* y, int64_t M, int64_t N, float eps,
+                            norm_dtype dtype, cudaStream_t stream, const norm_plan* plan) {
+    return rms_impl(x, w, y, M, N, eps, dtype, stream, plan);
+}
+
+norm_status norm_make_plan(int64_t M, int64_t N, norm_dtype dtype, int aligned, int num_sms, norm_plan* plan) {
+    const norm_status st = check_sizes(M, N, dtype);
+    if (st != NORM_OK) return st;
+    if (!plan || num_sms < 1) return NORM_ERR_ARG;
+    return make_plan(M, N, dtype, aligned != 0, num_sms, plan);
+}
+
+const char* norm_status_string(norm_status s) {
+    switch (s) {
+        case NORM_OK: return "ok";
+        case NORM_ERR_ARG: return "invalid argument (size, pointer or eps)";
+        case NORM_ERR_DTYPE: return "unsupported dtype";
+        case NORM_ERR_CUDA: return "CUDA runtime error (see norm_last_cuda_error)";
+        case NORM_ERR_PLAN: return "plan inconsistent with the call";
+        default: return "unknown status";
+    }
+}
+
+int norm_last_cuda_error(void) { return g_last_cuda_error; }
+
+int norm_abi_version(void) { return 1; }
+
+}  // extern "C"

@@ -1,0 +1,11 @@
+// RMSNorm forward kernels, bf16 rows: every (mapping, access width,
+// accesses per thread) variant the planner can name.
+#include "norm_kernels.cuh"
+
+namespace libnorm {
+
+cudaError_t launch_rms_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s) {
+    return launch_norm<__nv_bfloat16, false>(plan, a, s);
+}
+
+}  // namespace libnorm

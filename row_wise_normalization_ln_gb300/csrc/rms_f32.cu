@@ -1,0 +1,11 @@
+// RMSNorm forward kernels, f32 rows: every (mapping, access width,
+// accesses per thread) variant the planner can name.
+#include "norm_kernels.cuh"
+
+namespace libnorm {
+
+cudaError_t launch_rms_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t s) {
+    return launch_norm<float, false>(plan, a, s);
+}
+
+}  // namespace libnorm

@@ -1,0 +1,187 @@
+"""Host-side checks of the libnorm C ABI that need no GPU: the library loads,
+exports every entry point its header declares, rejects bad arguments before
+any CUDA call, and plans every row shape consistently."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import row_wise_normalization_ln_gb300 as rn
+from row_wise_normalization_ln_gb300 import _build
+from row_wise_normalization_ln_gb300.workloads import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "libnorm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return rn.library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:norm_status|const char\*|int)\s+(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_abi():
+    assert set(declared_functions()) == {
+        "ln_fwd", "rms_fwd", "ln_fwd_planned", "rms_fwd_planned", "norm_make_plan",
+        "norm_status_string", "norm_last_cuda_error", "norm_abi_version"}
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.norm_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4):
+        assert lib.norm_status_string(code)
+    assert lib.norm_status_string(0) == b"ok"
+
+
+# Fake device addresses: every call below must fail (or no-op) on the host
+# before any CUDA call could touch them.
+P = ctypes.c_void_p(0x1000)
+
+
+@pytest.mark.parametrize("M,N", [(-1, 8), (4, 0), (4, -3), (4, (1 << 24) + 1), (2 ** 62, 4)])
+def test_bad_sizes_rejected(lib, M, N):
+    assert lib.ln_fwd(P, P, P, P, None, None, M, N, 1e-5, rn.NORM_F32, None) == rn.NORM_ERR_ARG
+    assert lib.rms_fwd(P, P, P, M, N, 1e-6, rn.NORM_BF16, None) == rn.NORM_ERR_ARG
+
+
+def test_bad_dtype_rejected(lib):
+    assert lib.ln_fwd(P, P, P, P, None, None, 4, 8, 1e-5, 7, None) == rn.NORM_ERR_DTYPE
+    assert lib.rms_fwd(P, P, P, 4, 8, 1e-6, -1, None) == rn.NORM_ERR_DTYPE
+
+
+@pytest.mark.parametrize("eps", [-1e-5, float("nan"), float("inf")])
+def test_bad_eps_rejected(lib, eps):
+    assert lib.ln_fwd(P, P, P, P, None, None, 4, 8, eps, rn.NORM_F32, None) == rn.NORM_ERR_ARG
+    assert lib.rms_fwd(P, P, P, 4, 8, eps, rn.NORM_F32, None) == rn.NORM_ERR_ARG
+
+
+def test_null_pointers_rejected(lib):
+    for args in [(None, P, P, P), (P, None, P, P), (P, P, None, P), (P, P, P, None)]:
+        assert lib.ln_fwd(*args, None, None, 4, 8, 1e-5, rn.NORM_F32, None) == rn.NORM_ERR_ARG
+    for args in [(None, P, P), (P, None, P), (P, P, None)]:
+        assert lib.rms_fwd(*args, 4, 8, 1e-6, rn.NORM_F32, None) == rn.NORM_ERR_ARG
+
+
+def test_zero_rows_is_a_noop(lib):
+    # M == 0: OK, nothing launched, pointers may be NULL
+    assert lib.ln_fwd(None, None, None, None, None, None, 0, 8, 1e-5, rn.NORM_F32, None) == rn.NORM_OK
+    assert lib.rms_fwd(None, None, None, 0, 8, 1e-6, rn.NORM_BF16, None) == rn.NORM_OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
+def test_no_device_reports_cuda_error(lib):
+    assert lib.rms_fwd(P, P, P, 4, 8, 1e-6, rn.NORM_F32, None) == rn.NORM_ERR_CUDA
+    assert lib.norm_last_cuda_error() != 0
+
+
+def _plan(**kw):
+    base = dict(mapping=rn.NORM_MAP_CTA, vec_elems=4, per_thread=4, group=0, threads=256, cluster=1, grid=8)
+    base.update(kw)
+    return rn.NormPlan.from_dict(base)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(mapping=5),
+    dict(vec_elems=8),                          # fp32 vectors hold 4
+    dict(vec_elems=2),
+    dict(per_thread=3), dict(per_thread=16), dict(per_thread=0),
+    dict(threads=48), dict(threads=0), dict(threads=2048),
+    dict(cluster=3), dict(cluster=16),
+    dict(cluster=4, grid=6),                    # grid not a multiple of the cluster
+    dict(grid=0), dict(grid=1 << 31),
+    dict(mapping=rn.NORM_MAP_GROUP, group=3),
+    dict(mapping=rn.NORM_MAP_GROUP, group=64),
+    dict(mapping=rn.NORM_MAP_GROUP, group=8, per_thread=2),   # 8*2*4 < N: does not cover the row
+])
+def test_bad_plans_rejected(lib, kw):
+    p = _plan(**kw)
+    st = lib.rms_fwd_planned(P, P, P, 4, 1000, 1e-6, rn.NORM_F32, None, ctypes.byref(p))
+    assert st == rn.NORM_ERR_PLAN
+
+
+def test_vector_plan_needs_alignment(lib):
+    # 0x1004 is not 16-byte aligned: a 128-bit plan is refused
+    q = ctypes.c_void_p(0x1004)
+    p = _plan()
+    assert lib.rms_fwd_planned(q, P, P, 4, 1000, 1e-6, rn.NORM_F32, None, ctypes.byref(p)) == rn.NORM_ERR_PLAN
+    # rows of 1001 fp32 are not whole 16-byte vectors
+    assert lib.rms_fwd_planned(P, P, P, 4, 1001, 1e-6, rn.NORM_F32, None, ctypes.byref(p)) == rn.NORM_ERR_PLAN
+
+
+def _covers(plan, N):
+    cap = plan["per_thread"] * plan["vec_elems"]
+    if plan["mapping"] == rn.NORM_MAP_GROUP:
+        return plan["group"] * cap >= N and plan["rounds"] == 1
+    per_round = plan["cluster"] * plan["threads"] * cap
+    return plan["rounds"] * per_round >= N > (plan["rounds"] - 1) * per_round
+
+
+NS = [1, 2, 3, 4, 5, 7, 8, 9, 31, 32, 33, 64, 100, 255, 256, 257, 1000, 1023, 1024, 1025, 2048, 4095,
+      4096, 4999, 5000, 8192, 16384, 32768, 65535, 65536, 100000, 262144, 262145, 1 << 20, (1 << 24)]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("aligned", [True, False])
+@pytest.mark.parametrize("M", [1, 3, 128, 8192, 65536])
+def test_plans_are_consistent(lib, dtype, aligned, M):
+    s = 4 if dtype == torch.float32 else 2
+    for N in NS:
+        p = rn.make_plan(M, N, dtype, aligned, 152)
+        vec = 16 // s if aligned and (N * s) % 16 == 0 else 1
+        assert p["vec_elems"] == vec
+        assert p["per_thread"] in (1, 2, 4, 8)
+        assert p["threads"] % 32 == 0 and 32 <= p["threads"] <= 1024
+        assert _covers(p, N), (N, p)
+        if p["mapping"] == rn.NORM_MAP_GROUP:
+            assert p["group"] in (1, 2, 4, 8, 16, 32) and p["threads"] % p["group"] == 0
+            rows_per_cta = p["threads"] // p["group"]
+            assert p["grid"] == max(1, -(-M // rows_per_cta))
+        else:
+            assert p["cluster"] in (1, 2, 4, 8)
+            assert p["grid"] % p["cluster"] == 0 and p["grid"] == M * p["cluster"]
+
+
+def test_plans_for_the_workloads(lib):
+    """The mapping each benchmark workload gets (152 SMs, aligned buffers)."""
+    got = {name: rn.make_plan(w.M, w.N, w.torch_dtype, True, 152) for name, w in WORKLOADS.items()}
+    want = {
+        "ln_f32_128x1024": dict(mapping=rn.NORM_MAP_CTA, per_thread=1, threads=256, cluster=1, rounds=1),
+        "rms_f32_8192x4096": dict(mapping=rn.NORM_MAP_CTA, per_thread=4, threads=256, cluster=1, rounds=1),
+        "ln_bf16_4096x8192_outliers": dict(mapping=rn.NORM_MAP_CTA, per_thread=4, threads=256, cluster=1,
+                                           rounds=1),
+        "rms_bf16_65536x2048": dict(mapping=rn.NORM_MAP_GROUP, per_thread=8, group=32, threads=256, rounds=1),
+        "ln_f32_2048x65536": dict(mapping=rn.NORM_MAP_CTA, per_thread=8, threads=1024, cluster=2, rounds=1),
+        "ln_f32_8192x5000": dict(mapping=rn.NORM_MAP_CTA, per_thread=4, threads=320, cluster=1, rounds=1),
+    }
+    for name, w in want.items():
+        for k, v in w.items():
+            assert got[name][k] == v, (name, k, got[name])
+
+
+def test_make_plan_rejects_bad_arguments(lib):
+    p = rn.NormPlan()
+    assert lib.norm_make_plan(4, 0, 0, 1, 152, ctypes.byref(p)) == rn.NORM_ERR_ARG
+    assert lib.norm_make_plan(4, 8, 0, 1, 0, ctypes.byref(p)) == rn.NORM_ERR_ARG
+    assert lib.norm_make_plan(4, 8, 9, 1, 152, ctypes.byref(p)) == rn.NORM_ERR_DTYPE
+    assert lib.norm_make_plan(4, 8, 0, 1, 152, None) == rn.NORM_ERR_ARG
+
+
+def test_binding_rejects_cpu_tensors():
+    x = torch.zeros(2, 8)
+    with pytest.raises(ValueError):
+        rn.ln_fwd(x, torch.ones(8), torch.zeros(8))
+    with pytest.raises(ValueError):
+        rn.rms_fwd(x, torch.ones(8))
