@@ -67,6 +67,12 @@ typedef enum {
  * hold the whole row (CTA mapping only), the row is walked in `rounds`
  * register-sized rounds: x is read once for the statistics and the earlier
  * rounds are read again for the output (served from L2 when they fit).
+ *
+ * With `stages` >= 2 (CTA mapping, 16-byte vectors, one round) the CTAs are
+ * persistent and keep the next stages-1 rows of their share in flight in a
+ * ring of shared-memory stages (cp.async) while they reduce and store the
+ * current row; `grid` 0 then means "as many CTAs as fit on the device",
+ * resolved at launch from the kernel's occupancy.
  */
 typedef struct {
     int32_t mapping;     /* norm_mapping */
@@ -76,7 +82,7 @@ typedef struct {
     int32_t threads;     /* threads per CTA, multiple of 32, <= 1024 */
     int32_t cluster;     /* CTA mapping: CTAs per row, 1, 2, 4 or 8 */
     int32_t rounds;      /* derived by norm_make_plan; ignored on input */
-    int32_t reserved;
+    int32_t stages;      /* 0: registers only; 2..4: shared-memory ring */
     int64_t grid;        /* CTAs launched (a multiple of `cluster`); rows
                             are walked in a grid-stride loop */
 } norm_plan;
@@ -115,8 +121,9 @@ norm_status norm_make_plan(int64_t M, int64_t N, norm_dtype dtype, int aligned16
  * ln_fwd / rms_fwd with an explicit plan (plan == NULL: choose as the plain
  * calls do). The plan is checked against the call on the host; a plan whose
  * accesses would not cover the row, whose vector width does not match the
- * dtype and alignment, or whose shape is out of range returns NORM_ERR_PLAN
- * and launches nothing. For tuning and for tests of every kernel variant.
+ * dtype and alignment, whose ring would not fit in 227 KB of shared memory,
+ * or whose shape is out of range returns NORM_ERR_PLAN and launches nothing.
+ * For tuning and for tests of every kernel variant.
  */
 norm_status ln_fwd_planned(const void* x, const void* gamma, const void* beta, void* y,
                            float* mean, float* rstd, int64_t M, int64_t N, float eps,

@@ -38,12 +38,12 @@ class NormPlan(ctypes.Structure):
         ("threads", ctypes.c_int32),
         ("cluster", ctypes.c_int32),
         ("rounds", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("stages", ctypes.c_int32),
         ("grid", ctypes.c_int64),
     ]
 
     def as_dict(self) -> dict:
-        return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
+        return {k: getattr(self, k) for k, _ in self._fields_}
 
     @classmethod
     def from_dict(cls, d: dict) -> "NormPlan":

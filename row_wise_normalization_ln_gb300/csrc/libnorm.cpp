@@ -24,6 +24,8 @@ constexpr int64_t kMaxGrid = int64_t(1) << 30;
 constexpr int kMaxThreads = 1024;
 constexpr int kMaxCluster = 8;               // portable cluster size
 constexpr int kMaxPerThread = 8;
+constexpr int64_t kMaxSmem = 225 * 1024;     // dynamic shared memory per CTA (below the 227 KB opt-in)
+constexpr int kMaxStages = 4;
 
 thread_local int g_last_cuda_error = 0;
 
@@ -54,6 +56,10 @@ int vec_for(int64_t N, norm_dtype dtype, bool all_aligned) {
     return (all_aligned && (N * s) % 16 == 0) ? 16 / s : 1;
 }
 
+// The planner. Measured on GB300 (see the sweep notes of the design
+// document): rows do best with 8 accesses (128 bytes) in registers per
+// thread, CTAs of 64 to 256 threads, and long rows split over a cluster of
+// up to 8 such CTAs; lane groups only pay off below 64 accesses per row.
 norm_status make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_aligned, int num_sms, norm_plan* p) {
     std::memset(p, 0, sizeof *p);
     const int vec = vec_for(N, dtype, all_aligned);
@@ -62,35 +68,30 @@ norm_status make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_aligned, 
     p->vec_elems = vec;
 
     // Short rows: a group of lanes per row, up to 8 accesses per lane.
-    if (nacc <= 32 * kMaxPerThread) {
+    if (nacc < 64) {
         int64_t g = pow2_ceil(ceil_div(nacc, kMaxPerThread));
         if (g < 4) g = pow2_ceil(nacc < 4 ? nacc : 4);
-        if (g > 32) g = 32;
-        if (M * g >= busy_threads || nacc <= 32) {
-            p->mapping = NORM_MAP_GROUP;
-            p->group = static_cast<int32_t>(g);
-            p->per_thread = static_cast<int32_t>(pow2_ceil(ceil_div(nacc, g)));
-            p->threads = 256;
-            p->cluster = 1;
-            p->rounds = 1;
-            const int64_t rows_per_cta = p->threads / g;
-            p->grid = std::min<int64_t>(ceil_div(M, rows_per_cta), kMaxGrid);
-            if (p->grid < 1) p->grid = 1;
-            return NORM_OK;
-        }
+        p->mapping = NORM_MAP_GROUP;
+        p->group = static_cast<int32_t>(g);
+        p->per_thread = static_cast<int32_t>(pow2_ceil(ceil_div(nacc, g)));
+        p->threads = 256;
+        p->cluster = 1;
+        p->rounds = 1;
+        p->grid = std::max<int64_t>(std::min<int64_t>(ceil_div(M, p->threads / g), kMaxGrid), 1);
+        return NORM_OK;
     }
 
-    // Longer rows (or too few rows to fill the GPU by groups): a CTA, or a
-    // cluster of CTAs, per row.
-    int per = 4;
+    // A CTA, or a cluster of CTAs, per row.
+    int per = kMaxPerThread;
     int64_t threads = round_up(ceil_div(nacc, per), 32);
-    if (threads > kMaxThreads) {
-        per = kMaxPerThread;
+    if (threads < 64) {
+        per = 4;
         threads = round_up(ceil_div(nacc, per), 32);
     }
     int64_t cluster = 1;
-    if (threads > kMaxThreads) {
-        cluster = pow2_ceil(ceil_div(nacc, int64_t(kMaxThreads) * per));
+    if (threads > 256) {
+        cluster = std::min<int64_t>(ceil_div(threads, 256), kMaxCluster);
+        cluster = pow2_ceil(cluster);
         if (cluster > kMaxCluster) cluster = kMaxCluster;
         threads = std::min<int64_t>(round_up(ceil_div(nacc, cluster * per), 32), kMaxThreads);
     }
@@ -126,6 +127,7 @@ norm_status check_plan(const norm_plan& in, int64_t N, norm_dtype dtype, bool al
     if (p.mapping == NORM_MAP_GROUP) {
         if (!is_pow2(p.group) || p.group > 32) return NORM_ERR_PLAN;
         if (int64_t(p.group) * p.per_thread < nacc) return NORM_ERR_PLAN;
+        if (p.stages != 0) return NORM_ERR_PLAN;
         p.cluster = 1;
         p.rounds = 1;
     } else {
@@ -133,12 +135,23 @@ norm_status check_plan(const norm_plan& in, int64_t N, norm_dtype dtype, bool al
         p.group = 0;
         p.rounds = static_cast<int32_t>(ceil_div(nacc, int64_t(p.cluster) * p.threads * p.per_thread));
     }
+    if (p.stages != 0) {
+        if (p.stages < 2 || p.stages > kMaxStages || p.vec_elems == 1 || p.rounds != 1) return NORM_ERR_PLAN;
+        const int64_t smem = int64_t(p.stages) * p.per_thread * p.threads * 16 + p.stages * 32 * 4;
+        if (smem > kMaxSmem) return NORM_ERR_PLAN;
+        if (p.grid == 0) {  // resolved at launch
+            *out = p;
+            return NORM_OK;
+        }
+    }
     if (p.grid < p.cluster || p.grid > kMaxGrid || p.grid % p.cluster != 0) return NORM_ERR_PLAN;
     *out = p;
     return NORM_OK;
 }
 
-int device_sm_count() {
+// SM count of the current device (cached per device); `dev` receives the
+// device ordinal.
+int device_sm_count(int* dev_out) {
     static std::atomic<int> cache[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -146,6 +159,7 @@ int device_sm_count() {
         g_last_cuda_error = static_cast<int>(e);
         return -1;
     }
+    *dev_out = dev;
     if (dev >= 0 && dev < 64) {
         const int v = cache[dev].load(std::memory_order_relaxed);
         if (v > 0) return v;
@@ -160,7 +174,7 @@ int device_sm_count() {
     return n;
 }
 
-using Launcher = cudaError_t (*)(const norm_plan&, const NormArgs&, cudaStream_t);
+using Launcher = cudaError_t (*)(const norm_plan&, const NormArgs&, cudaStream_t, int, int);
 
 norm_status run(bool ln, const NormArgs& a, norm_dtype dtype, bool all_aligned, cudaStream_t stream,
                 const norm_plan* user_plan) {
@@ -168,17 +182,18 @@ norm_status run(bool ln, const NormArgs& a, norm_dtype dtype, bool all_aligned, 
     if (user_plan) {
         const norm_status st = check_plan(*user_plan, a.N, dtype, all_aligned, &plan);
         if (st != NORM_OK) return st;
-    } else {
-        const int sms = device_sm_count();
-        if (sms <= 0) return NORM_ERR_CUDA;
-        make_plan(a.M, a.N, dtype, all_aligned, sms, &plan);
     }
+    int dev = 0;
+    const int sms = device_sm_count(&dev);
+    if (sms <= 0) return NORM_ERR_CUDA;
+    if (!user_plan) make_plan(a.M, a.N, dtype, all_aligned, sms, &plan);
     NormArgs args = a;
     args.group = plan.group;
     args.rounds = plan.rounds;
+    args.stages = plan.stages;
     Launcher launch = ln ? (dtype == NORM_F32 ? libnorm::launch_ln_f32 : libnorm::launch_ln_bf16)
                          : (dtype == NORM_F32 ? libnorm::launch_rms_f32 : libnorm::launch_rms_bf16);
-    const cudaError_t e = launch(plan, args, stream);
+    const cudaError_t e = launch(plan, args, stream, sms, dev);
     if (e != cudaSuccess) {
         g_last_cuda_error = static_cast<int>(e);
         return NORM_ERR_CUDA;
@@ -194,7 +209,7 @@ norm_status ln_impl(const void* x, const void* gamma, const void* beta, void* y,
     if (M == 0) return NORM_OK;
     if (!x || !gamma || !beta || !y) return NORM_ERR_ARG;
     const bool al = aligned16(x) && aligned16(y) && aligned16(gamma) && aligned16(beta);
-    NormArgs a{x, gamma, beta, y, mean, rstd, M, static_cast<int32_t>(N), eps, 0, 1};
+    NormArgs a{x, gamma, beta, y, mean, rstd, M, static_cast<int32_t>(N), eps, 0, 1, 0};
     return run(true, a, dtype, al, stream, plan);
 }
 
@@ -206,7 +221,7 @@ norm_status rms_impl(const void* x, const void* w, void* y, int64_t M, int64_t N
     if (M == 0) return NORM_OK;
     if (!x || !w || !y) return NORM_ERR_ARG;
     const bool al = aligned16(x) && aligned16(y) && aligned16(w);
-    NormArgs a{x, w, nullptr, y, nullptr, nullptr, M, static_cast<int32_t>(N), eps, 0, 1};
+    NormArgs a{x, w, nullptr, y, nullptr, nullptr, M, static_cast<int32_t>(N), eps, 0, 1, 0};
     return run(false, a, dtype, al, stream, plan);
 }
 

@@ -21,12 +21,15 @@ struct NormArgs {
     float eps;
     int32_t group;      // GROUP mapping: lanes per row
     int32_t rounds;     // CTA mapping: register-sized rounds per row
+    int32_t stages;     // pipelined CTA mapping: shared-memory ring stages
 };
 
-// Launch the kernel variant `plan` names. The plan has been validated.
-cudaError_t launch_ln_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t s);
-cudaError_t launch_ln_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s);
-cudaError_t launch_rms_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t s);
-cudaError_t launch_rms_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s);
+// Launch the kernel variant `plan` names on the current device `dev` (with
+// `num_sms` SMs). The plan has been validated; a pipelined plan with grid 0
+// gets a persistent grid sized by occupancy.
+cudaError_t launch_ln_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_ln_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_rms_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_rms_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
 
 }  // namespace libnorm

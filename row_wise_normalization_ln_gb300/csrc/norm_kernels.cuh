@@ -1,25 +1,43 @@
 // Row-wise LayerNorm / RMSNorm forward kernels for sm_103a.
 //
-// Both kernels read x from HBM once, keep the row in registers, reduce the
-// statistics in fp32 and write y in the same pass (fused affine and cast):
+// Every kernel reads x from HBM once, keeps its slice of the row in
+// registers, reduces the statistics in fp32 and writes y in the same pass
+// (fused affine and cast):
 //
-//   norm_fwd_group  `group` lanes of a warp own a row (short rows). The
-//                   statistics meet in a xor-shuffle butterfly.
-//   norm_fwd_cta    a CTA, or a cluster of CTAs, owns a row (long rows).
-//                   Warp butterflies, then shared memory across warps, then
-//                   distributed shared memory across the cluster.
+//   norm_fwd_group  `group` lanes of a warp own a row (short rows).
+//   norm_fwd_cta    a CTA, or a thread-block cluster, owns a row; rows longer
+//                   than one pass of the cluster's registers are walked in
+//                   rounds. Also the element-access path for unaligned rows.
+//   norm_fwd_pipe   the CTA mapping on a persistent grid, with the next rows
+//                   of each CTA in flight in a shared-memory ring (cp.async).
 //
-// LayerNorm statistics are Welford states ([Ch7] §7.4): each thread forms
-// (n, mean, M2) of its own register-resident elements, shifted by the row's
-// first element, by a two-pass over its registers ([T3] §② trap 2: the row
-// is in registers, so "two passes" cost no extra memory traffic), and the
-// states are merged with the parallel rule of [Ch7] §7.4.1. The variance is never formed as E[x^2] - E[x]^2. Elements
-// beyond N are never loaded and never counted ([T3] §② trap 1).
+// Inside a CTA's slice the layout is warp-major: warp w holds V runs of 32
+// consecutive accesses, access (w*V + j)*32 + lane, so every instruction
+// touches 32 consecutive accesses and the offset of run j is a compile-time
+// constant.
+//
+// LayerNorm statistics ([Ch7] §7.4, §7.4.1): each thread forms the Welford
+// state (n_t, mean_t, M2_t) of its own elements, shifted by the row's first
+// element K, by two passes over its registers ([T3] §② trap 2: the row is
+// in registers, so "two passes" cost no memory traffic). The states of all
+// threads of the row are then merged with the merge rule in its k-way form,
+//     mean = sum_t n_t mean_t / N,    M2 = sum_t (M2_t + n_t (mean_t - mean)^2),
+// which is what any sequence of pairwise merges reaches; each sum is an xor
+// butterfly inside the warp, then shared memory across warps, then
+// distributed shared memory across the cluster. The variance is never formed
+// as E[x^2] - E[x]^2. Elements beyond N are never loaded and never counted
+// ([T3] §② trap 1). The shift keeps the digits of rows whose mean dwarfs
+// their spread ([Ch7] §7.3): x - K of nearby values is exact and the merged
+// means stay small.
 //
 // Sources (page title, section):
-//   [Ch7] "第 7 章 LayerNorm 与 RMSNorm": §7.1, §7.4-7.6.
+//   [Ch7] "第 7 章 LayerNorm 与 RMSNorm": §7.1, §7.3-7.6.
 //   [T3]  "T3 讲解：LayerNorm / RMSNorm 的 forward": §②, §③.
 #pragma once
+
+#include <algorithm>
+#include <atomic>
+#include <type_traits>
 
 #include "norm_args.h"
 #include "norm_device.cuh"
@@ -31,251 +49,570 @@ struct ElemVec {
     static constexpr int value = 16 / sizeof(T);
 };
 
-// (n, mean, M2) of this thread's valid elements, two-pass over registers,
-// on the row shifted by K (the row's first element, the same for every
-// thread of the row): the variance does not change under a shift, the
-// differences x - K of nearby fp32 values are exact, and the merged means
-// stay small, so a row whose mean dwarfs its spread ([Ch7] §7.3) keeps its
-// digits through every merge. The returned mean is the mean of x - K.
-template <class T, int VEC, int V>
-__device__ __forceinline__ Welford thread_welford(const Frag<T, VEC> (&f)[V], const bool (&ok)[V], float K) {
-    float sum = 0.f;
-    int cnt = 0;
-#pragma unroll
-    for (int j = 0; j < V; ++j)
-        if (ok[j]) {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) sum += f[j].get(e) - K;
-            cnt += VEC;
-        }
-    if (cnt == 0) return welford_empty();
-    const float n = static_cast<float>(cnt);
-    const float mu = sum / n;
-    float m2 = 0.f;
-#pragma unroll
-    for (int j = 0; j < V; ++j)
-        if (ok[j]) {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const float d = (f[j].get(e) - K) - mu;
-                m2 = fmaf(d, d, m2);
-            }
-        }
-    return {n, mu, m2};
+// ================================================================== element math
+// One access is a 16-byte vector (4 fp32 or 8 bf16) held as a uint4, or a
+// single element (VEC = 1) held in the low bits of a uint32. The bf16
+// routines use the sm_100-family mixed-precision instructions, which widen a
+// bf16 operand exactly inside one rounded fp32 add/sub/fma.
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// (lo - K, hi - K) of the two bf16 values packed in w, each rounded once.
+__device__ __forceinline__ float2 bf16x2_minus(uint32_t w, float K) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "sub.rn.f32.bf16 %0, l, %3;\n\tsub.rn.f32.bf16 %1, h, %3;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w), "f"(K));
+    return make_float2(lo, hi);
 }
 
-// Sum of squares of this thread's valid elements (RMSNorm, [Ch7] §7.5.1).
-template <class T, int VEC, int V>
-__device__ __forceinline__ float thread_sumsq(const Frag<T, VEC> (&f)[V], const bool (&ok)[V]) {
-    float ss = 0.f;
-#pragma unroll
-    for (int j = 0; j < V; ++j)
-        if (ok[j]) {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) ss = fmaf(f[j].get(e), f[j].get(e), ss);
-        }
-    return ss;
+// acc + lo^2 + hi^2 (each product exact in fp32, each sum rounded once).
+__device__ __forceinline__ float bf16x2_sumsq(uint32_t w, float acc) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\t"
+        "fma.rn.f32.bf16 %0, l, l, %0;\n\tfma.rn.f32.bf16 %0, h, h, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w));
+    return acc;
 }
 
-// Normalise, apply the affine parameters, round and store one access.
-// LayerNorm: y = ((x - K) - mu) * rstd * gamma + beta, where mu is the mean
-// of the shifted row (so x - mean is formed without the rounding of the
-// fp32 mean); RMSNorm: y = x * rstd * w.
-template <class T, int VEC, bool LN>
-__device__ __forceinline__ void emit(const Frag<T, VEC>& xf, const T* gamma, const T* beta, T* y,
-                                     int elem, float K, float mu, float rs) {
-    Frag<T, VEC> g;
-    g.load_param(gamma + elem);
-    float o[VEC];
-    if constexpr (LN) {
-        Frag<T, VEC> b;
-        b.load_param(beta + elem);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) o[e] = fmaf(((xf.get(e) - K) - mu) * rs, g.get(e), b.get(e));
-    } else {
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) o[e] = (xf.get(e) * rs) * g.get(e);
+// (a_lo * b_lo, a_hi * b_hi): products of bf16 values, exact in fp32.
+__device__ __forceinline__ float2 bf16x2_mul(uint32_t a, uint32_t b) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, 0f00000000;\n\tfma.rn.f32.bf16 %1, ah, bh, 0f00000000;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(a), "r"(b));
+    return make_float2(lo, hi);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);  // round to nearest-even
+    return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// Per-access operations, specialised on element type and width.
+template <class T, int VEC>
+struct Ops;
+
+template <>
+struct Ops<float, 4> {
+    using Raw = uint4;
+    static __device__ __forceinline__ float e(const Raw& r, int i) {
+        return __uint_as_float(i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w);
     }
-    Frag<T, VEC>::store(y + elem, o);
+    // sum of (x - K)
+    static __device__ __forceinline__ float shifted_sum(const Raw& r, float K) {
+        return ((e(r, 0) - K) + (e(r, 1) - K)) + ((e(r, 2) - K) + (e(r, 3) - K));
+    }
+    // acc + sum ((x - K) - mu)^2
+    static __device__ __forceinline__ float dev2(const Raw& r, float K, float mu, float acc) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float d = (e(r, i) - K) - mu;
+            acc = fmaf(d, d, acc);
+        }
+        return acc;
+    }
+    static __device__ __forceinline__ float sumsq(const Raw& r, float acc) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc = fmaf(e(r, i), e(r, i), acc);
+        return acc;
+    }
+    // LayerNorm: ((x - K) * rs + nmr) * gamma + beta with nmr = -mu * rs
+    static __device__ __forceinline__ Raw ln_out(const Raw& r, float K, float rs, float nmr, const Raw& g,
+                                                 const Raw& b) {
+        float o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = fmaf(fmaf(e(r, i) - K, rs, nmr), e(g, i), e(b, i));
+        return make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
+                          __float_as_uint(o[3]));
+    }
+    // RMSNorm: (x * w) * rs
+    static __device__ __forceinline__ Raw rms_out(const Raw& r, float rs, const Raw& w) {
+        float o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = (e(r, i) * e(w, i)) * rs;
+        return make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
+                          __float_as_uint(o[3]));
+    }
+    static __device__ __forceinline__ Raw load(const float* p) { return *reinterpret_cast<const uint4*>(p); }
+    static __device__ __forceinline__ Raw load_param(const float* p) {
+        return __ldg(reinterpret_cast<const uint4*>(p));
+    }
+    static __device__ __forceinline__ void store(float* p, const Raw& v) { *reinterpret_cast<uint4*>(p) = v; }
+};
+
+template <>
+struct Ops<__nv_bfloat16, 8> {
+    using Raw = uint4;
+    static __device__ __forceinline__ uint32_t w(const Raw& r, int i) {
+        return i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w;
+    }
+    static __device__ __forceinline__ float shifted_sum(const Raw& r, float K) {
+        const float2 a = bf16x2_minus(r.x, K), b = bf16x2_minus(r.y, K);
+        const float2 c = bf16x2_minus(r.z, K), d = bf16x2_minus(r.w, K);
+        return ((a.x + a.y) + (b.x + b.y)) + ((c.x + c.y) + (d.x + d.y));
+    }
+    static __device__ __forceinline__ float dev2(const Raw& r, float K, float mu, float acc) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 s = bf16x2_minus(w(r, i), K);
+            const float d0 = s.x - mu, d1 = s.y - mu;
+            acc = fmaf(d0, d0, acc);
+            acc = fmaf(d1, d1, acc);
+        }
+        return acc;
+    }
+    static __device__ __forceinline__ float sumsq(const Raw& r, float acc) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc = bf16x2_sumsq(w(r, i), acc);
+        return acc;
+    }
+    static __device__ __forceinline__ Raw ln_out(const Raw& r, float K, float rs, float nmr, const Raw& g,
+                                                 const Raw& b) {
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 s = bf16x2_minus(w(r, i), K);
+            const uint32_t gi = w(g, i), bi = w(b, i);
+            o[i] = pack_bf16x2(fmaf(fmaf(s.x, rs, nmr), bf16_lo(gi), bf16_lo(bi)),
+                               fmaf(fmaf(s.y, rs, nmr), bf16_hi(gi), bf16_hi(bi)));
+        }
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    static __device__ __forceinline__ Raw rms_out(const Raw& r, float rs, const Raw& wt) {
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 p = bf16x2_mul(w(r, i), w(wt, i));
+            o[i] = pack_bf16x2(p.x * rs, p.y * rs);
+        }
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    static __device__ __forceinline__ Raw load(const __nv_bfloat16* p) { return *reinterpret_cast<const uint4*>(p); }
+    static __device__ __forceinline__ Raw load_param(const __nv_bfloat16* p) {
+        return __ldg(reinterpret_cast<const uint4*>(p));
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16* p, const Raw& v) {
+        *reinterpret_cast<uint4*>(p) = v;
+    }
+};
+
+// Single elements (rows that are not whole 16-byte aligned vectors).
+template <class T>
+struct ScalarOps {
+    using Raw = uint32_t;
+    static __device__ __forceinline__ float e(Raw r) {
+        if constexpr (sizeof(T) == 4)
+            return __uint_as_float(r);
+        else
+            return __uint_as_float(r << 16);
+    }
+    static __device__ __forceinline__ float shifted_sum(Raw r, float K) { return e(r) - K; }
+    static __device__ __forceinline__ float dev2(Raw r, float K, float mu, float acc) {
+        const float d = (e(r) - K) - mu;
+        return fmaf(d, d, acc);
+    }
+    static __device__ __forceinline__ float sumsq(Raw r, float acc) { return fmaf(e(r), e(r), acc); }
+    static __device__ __forceinline__ Raw ln_out(Raw r, float K, float rs, float nmr, Raw g, Raw b) {
+        return from_float(fmaf(fmaf(e(r) - K, rs, nmr), e(g), e(b)));
+    }
+    static __device__ __forceinline__ Raw rms_out(Raw r, float rs, Raw wt) { return from_float((e(r) * e(wt)) * rs); }
+    static __device__ __forceinline__ Raw from_float(float v) {
+        if constexpr (sizeof(T) == 4)
+            return __float_as_uint(v);
+        else
+            return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
+    }
+    static __device__ __forceinline__ Raw load(const T* p) {
+        if constexpr (sizeof(T) == 4)
+            return __float_as_uint(*reinterpret_cast<const float*>(p));
+        else
+            return *reinterpret_cast<const unsigned short*>(p);
+    }
+    static __device__ __forceinline__ Raw load_param(const T* p) {
+        if constexpr (sizeof(T) == 4)
+            return __float_as_uint(__ldg(reinterpret_cast<const float*>(p)));
+        else
+            return __ldg(reinterpret_cast<const unsigned short*>(p));
+    }
+    static __device__ __forceinline__ void store(T* p, Raw v) {
+        if constexpr (sizeof(T) == 4)
+            *reinterpret_cast<float*>(p) = __uint_as_float(v);
+        else
+            *reinterpret_cast<unsigned short*>(p) = static_cast<unsigned short>(v);
+    }
+};
+
+template <class T, int VEC>
+using OpsFor = typename std::conditional<VEC == 1, ScalarOps<T>, Ops<T, VEC>>::type;
+
+// The row's first element, the shift K of LayerNorm.
+template <class T>
+__device__ __forceinline__ float first_elem(const T* row) {
+    return ScalarOps<T>::e(ScalarOps<T>::load(row));
 }
 
-// ------------------------------------------------------------------ GROUP
+// ================================================================== a thread's slice
+// V accesses of one row held in registers as loaded; the first `nvalid` lie
+// inside the row. `stride` is the distance in elements between a thread's
+// consecutive accesses (32*VEC in the warp-major CTA layout, G*VEC in the
+// GROUP layout). LayerNorm works on x - K (K set by set_shift).
+template <class T, int VEC, int V, bool LN>
+struct Slice {
+    using O = OpsFor<T, VEC>;
+    typename O::Raw raw[V];
+    float K;
+
+    __device__ __forceinline__ void set_shift(float k) { K = k; }
+    __device__ __forceinline__ void set(int j, const typename O::Raw& v) { raw[j] = v; }
+    __device__ __forceinline__ void load(const T* p, int stride, int nvalid) {
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            if (j < nvalid) raw[j] = O::load(p + j * stride);
+    }
+    // Welford state of the valid elements, two passes over the registers:
+    // the sum and mean of x - K, then M2 about that mean.
+    __device__ __forceinline__ void welford(int nvalid, float inv_n, float& sum, float& mean, float& m2) const {
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            if (j < nvalid) {
+                if (j & 1)
+                    s1 += O::shifted_sum(raw[j], K);
+                else
+                    s0 += O::shifted_sum(raw[j], K);
+            }
+        sum = s0 + s1;
+        mean = sum * inv_n;
+        float q0 = 0.f, q1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            if (j < nvalid) {
+                if (j & 1)
+                    q1 = O::dev2(raw[j], K, mean, q1);
+                else
+                    q0 = O::dev2(raw[j], K, mean, q0);
+            }
+        m2 = q0 + q1;
+    }
+    // Sum of squares of the valid elements (RMSNorm, [Ch7] §7.5.1).
+    __device__ __forceinline__ float sumsq(int nvalid) const {
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            if (j < nvalid) {
+                if (j & 1)
+                    s1 = O::sumsq(raw[j], s1);
+                else
+                    s0 = O::sumsq(raw[j], s0);
+            }
+        return s0 + s1;
+    }
+    // Normalise, apply the affine parameters, round and store the valid
+    // accesses; `g`, `b` and `y` point at this thread's first access.
+    // LayerNorm: y = ((x - K) * rstd - mu * rstd) * gamma + beta, where mu is
+    // the mean of x - K (so x - mean is never formed from a rounded fp32
+    // mean); RMSNorm: y = (x * w) * rstd.
+    __device__ __forceinline__ void emit(const T* g, const T* b, T* y, int stride, int nvalid, float mu,
+                                         float rs) const {
+        const float nmr = -mu * rs;
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            if (j < nvalid) {
+                if constexpr (LN)
+                    O::store(y + j * stride, O::ln_out(raw[j], K, rs, nmr, O::load_param(g + j * stride),
+                                                       O::load_param(b + j * stride)));
+                else
+                    O::store(y + j * stride, O::rms_out(raw[j], rs, O::load_param(g + j * stride)));
+            }
+    }
+};
+
+// How many of a thread's V runs lie inside a row of `nacc` accesses when its
+// first access is `first` and its runs are `stride_acc` accesses apart.
+__device__ __forceinline__ int valid_runs(int nacc, int first, int stride_acc, int V) {
+    if (first >= nacc) return 0;
+    return min(V, (nacc - first + stride_acc - 1) / stride_acc);
+}
+
+// ================================================================== row reduction
+// Sum of one value per thread over the CTA and, when C > 1, over the
+// cluster: xor butterfly in each warp, per-warp partials in shared memory, a
+// butterfly over them in every warp, then the CTAs' partials over
+// distributed shared memory. Every thread of every CTA of the cluster
+// returns the same bits.
+//
+// A row makes two such sums for LayerNorm (stage 0, then stage 1) and one
+// for RMSNorm (stage 0). Each stage has its own shared-memory slots and the
+// stages alternate, so a slot is written again only after a barrier that
+// every reader of its previous value has passed.
+struct RowReduceSmem {
+    float warp_part[2][32];  // [stage][warp]
+    float cta_part[2];       // [stage], read by cluster peers
+};
+
+__device__ __forceinline__ float row_sum(RowReduceSmem& red, int stage, float v, uint32_t C, int nwarps,
+                                         int wwidth) {
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    v = group_sum(v, 32);
+    if (lane == 0) red.warp_part[stage][tid >> 5] = v;
+    __syncthreads();
+    v = sum_first_lanes(lane < nwarps ? red.warp_part[stage][lane] : 0.f, wwidth);
+    if (C > 1) {
+        if (tid == 0) red.cta_part[stage] = v;
+        cluster_barrier();
+        v = sum_first_lanes(
+            lane < static_cast<int>(C) ? ld_peer_f32(peer_smem_addr(&red.cta_part[stage], lane)) : 0.f,
+            static_cast<int>(C));
+    }
+    return v;
+}
+
+// Row statistics from each thread's Welford state (LayerNorm) or sum of
+// squares (RMSNorm): the shifted mean mu and rstd, identical in every thread.
+template <bool LN>
+__device__ __forceinline__ void row_stats(RowReduceSmem& red, float n_t, float sum_t, float mean_t, float m2_t,
+                                          float ss_t, float invN, float eps, uint32_t C, int nwarps, int wwidth,
+                                          float& mu, float& rs) {
+    if constexpr (LN) {
+        mu = row_sum(red, 0, sum_t, C, nwarps, wwidth) * invN;
+        const float d = mean_t - mu;
+        const float m2 = row_sum(red, 1, fmaf(n_t * d, d, m2_t), C, nwarps, wwidth);
+        rs = rsqrtf(m2 * invN + eps);
+    } else {
+        mu = 0.f;
+        rs = rsqrtf(row_sum(red, 0, ss_t, C, nwarps, wwidth) * invN + eps);
+    }
+}
+
+// ================================================================== GROUP
 // Lanes [k*G, (k+1)*G) of the CTA own row blockIdx*rows_per_cta + k. Lane l
-// of a group holds accesses l, l+G, l+2G, ... of the row (coalesced: the G
-// lanes of a group read G consecutive accesses per instruction).
+// of a group holds accesses l, l+G, l+2G, ... (the G lanes of a group read G
+// consecutive accesses per instruction). The statistics meet in xor
+// butterflies over the group.
 template <class T, int VEC, int V, bool LN>
 __global__ void __launch_bounds__(1024) norm_fwd_group(const NormArgs a) {
-    const T* __restrict__ gamma = static_cast<const T*>(a.gamma);
-    const T* __restrict__ beta = static_cast<const T*>(a.beta);
+    using S = Slice<T, VEC, V, LN>;
     const int G = a.group;
     const int tid = threadIdx.x;
     const int gl = tid & (G - 1);
     const int rows_per_cta = blockDim.x / G;
     const int nacc = (a.N + VEC - 1) / VEC;
+    const int stride = G * VEC;
+    const int nvalid = valid_runs(nacc, gl, G, V);
+    const float n_t = static_cast<float>(nvalid * VEC);
+    const float inv_n = nvalid > 0 ? 1.f / n_t : 0.f;
+    const float invN = 1.f / static_cast<float>(a.N);
+    const T* g = static_cast<const T*>(a.gamma) + gl * VEC;
+    const T* b = static_cast<const T*>(a.beta) + gl * VEC;
 
     for (int64_t rb = blockIdx.x; rb * rows_per_cta < a.M; rb += gridDim.x) {
         const int64_t row = rb * rows_per_cta + tid / G;
         const bool row_ok = row < a.M;
+        const int nv = row_ok ? nvalid : 0;
         const T* xr = static_cast<const T*>(a.x) + row * a.N;
-        T* yr = static_cast<T*>(a.y) + row * a.N;
-
-        Frag<T, VEC> f[V];
-        bool ok[V];
-        float K = 0.f;
-        if (LN && row_ok) {
-            Frag<T, 1> k0;
-            k0.load(xr);
-            K = k0.get(0);
-        }
-#pragma unroll
-        for (int j = 0; j < V; ++j) {
-            const int acc = j * G + gl;
-            ok[j] = row_ok && acc < nacc;
-            if (ok[j]) f[j].load(xr + acc * VEC);
-        }
-
+        S s;
+        const float K = (LN && row_ok) ? first_elem(xr) : 0.f;
+        s.set_shift(K);
+        s.load(xr + gl * VEC, stride, nv);
         float mu = 0.f, rs;
         if constexpr (LN) {
-            const Welford s = group_merge(thread_welford<T, VEC, V>(f, ok, K), G);
-            mu = s.mean;
-            rs = rsqrtf(s.m2 / static_cast<float>(a.N) + a.eps);
+            float sum = 0.f, mean = 0.f, m2 = 0.f;
+            s.welford(nv, inv_n, sum, mean, m2);
+            mu = group_sum(sum, G) * invN;
+            const float d = mean - mu;
+            const float M2 = group_sum(nv > 0 ? fmaf(n_t * d, d, m2) : 0.f, G);
+            rs = rsqrtf(M2 * invN + a.eps);
             if (gl == 0 && row_ok) {
                 if (a.mean) a.mean[row] = K + mu;
                 if (a.rstd) a.rstd[row] = rs;
             }
         } else {
-            const float ss = group_sum(thread_sumsq<T, VEC, V>(f, ok), G);
-            rs = rsqrtf(ss / static_cast<float>(a.N) + a.eps);
+            rs = rsqrtf(group_sum(s.sumsq(nv), G) * invN + a.eps);
         }
-#pragma unroll
-        for (int j = 0; j < V; ++j)
-            if (ok[j]) emit<T, VEC, LN>(f[j], gamma, beta, yr, (j * G + gl) * VEC, K, mu, rs);
+        s.emit(g, b, static_cast<T*>(a.y) + row * a.N + gl * VEC, stride, nv, mu, rs);
     }
 }
 
-// -------------------------------------------------------------------- CTA
+// ================================================================== CTA
 // A cluster of C CTAs (C = 1 without a cluster launch) owns one row per
-// iteration. In round r, thread t of CTA rank k holds accesses
-// ((r*C + k)*V + j)*T + t for j < V. With one round the row stays in
-// registers from load to store. With several rounds every round is read for
-// the statistics; the output pass then walks the rounds backwards, reusing
-// the registers of the last round and re-reading the others.
+// iteration. Round r of the row is the slice of accesses
+// [(r*C + k)*V*T, (r*C + k + 1)*V*T) for CTA rank k, laid out warp-major.
+// With one round the slice stays in registers from load to store. With
+// several rounds each round is read for the statistics (its Welford state
+// folded into the thread's state with the pairwise merge); the output pass
+// then walks the rounds backwards, reusing the registers of the last round
+// and re-reading the others.
 template <class T, int VEC, int V, bool LN>
 __global__ void __launch_bounds__(1024) norm_fwd_cta(const NormArgs a) {
-    __shared__ float warp_part[2][3][32];  // per-warp states, double-buffered by row parity
-    __shared__ float cta_part[2][3];       // this CTA's state, read by cluster peers
+    using S = Slice<T, VEC, V, LN>;
+    __shared__ RowReduceSmem red;
 
-    const T* __restrict__ gamma = static_cast<const T*>(a.gamma);
-    const T* __restrict__ beta = static_cast<const T*>(a.beta);
     const int T_ = blockDim.x;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int nwarps = T_ >> 5;
+    int wwidth = 1;  // power of two >= the number of warps
+    while (wwidth < nwarps) wwidth <<= 1;
     const uint32_t C = cluster_size();
-    const uint32_t rank = cluster_rank();
+    const int rank = static_cast<int>(cluster_rank());
     const int64_t first_row = blockIdx.x / C;
     const int64_t row_step = gridDim.x / C;
     const int nacc = (a.N + VEC - 1) / VEC;
     const int rounds = a.rounds;
+    const int stride = 32 * VEC;
+    const int in_slice = warp * V * 32 + lane;  // this thread's first access within a slice
+    const float invN = 1.f / static_cast<float>(a.N);
 
-    int buf = 0;
-    for (int64_t row = first_row; row < a.M; row += row_step, buf ^= 1) {
+    for (int64_t row = first_row; row < a.M; row += row_step) {
         const T* xr = static_cast<const T*>(a.x) + row * a.N;
         T* yr = static_cast<T*>(a.y) + row * a.N;
-
-        Frag<T, VEC> f[V];
-        bool ok[V];
-        Welford st = welford_empty();
-        float ss = 0.f;
-        float K = 0.f;
-        if constexpr (LN) {
-            Frag<T, 1> k0;
-            k0.load(xr);
-            K = k0.get(0);
-        }
+        S s;
+        const float K = LN ? first_elem(xr) : 0.f;
+        s.set_shift(K);
+        float n_t = 0.f, sum_t = 0.f, mean_t = 0.f, m2_t = 0.f, ss_t = 0.f;
+        int nv = 0;
         for (int r = 0; r < rounds; ++r) {
-            const int base = (r * static_cast<int>(C) + static_cast<int>(rank)) * V * T_ + tid;
-#pragma unroll
-            for (int j = 0; j < V; ++j) {
-                const int acc = base + j * T_;
-                ok[j] = acc < nacc;
-                if (ok[j]) f[j].load(xr + acc * VEC);
-            }
-            if constexpr (LN)
-                st = chan_merge(st, thread_welford<T, VEC, V>(f, ok, K));
-            else
-                ss += thread_sumsq<T, VEC, V>(f, ok);
-        }
-
-        // warps -> shared memory -> every warp merges the per-warp states
-        float mu = 0.f, rs;
-        if constexpr (LN) {
-            st = group_merge(st, 32);
-            if (lane == 0) {
-                warp_part[buf][0][warp] = st.n;
-                warp_part[buf][1][warp] = st.mean;
-                warp_part[buf][2][warp] = st.m2;
-            }
-            __syncthreads();
-            st = lane < nwarps ? Welford{warp_part[buf][0][lane], warp_part[buf][1][lane], warp_part[buf][2][lane]}
-                               : welford_empty();
-            st = group_merge(st, 32);
-            if (C > 1) {
-                if (tid == 0) {
-                    cta_part[buf][0] = st.n;
-                    cta_part[buf][1] = st.mean;
-                    cta_part[buf][2] = st.m2;
+            const int f = (r * static_cast<int>(C) + rank) * V * T_ + in_slice;
+            nv = valid_runs(nacc, f, 32, V);
+            s.load(xr + f * VEC, stride, nv);
+            if constexpr (LN) {
+                const float n = static_cast<float>(nv * VEC);
+                float sum = 0.f, mean = 0.f, m2 = 0.f;
+                s.welford(nv, nv > 0 ? 1.f / n : 0.f, sum, mean, m2);
+                if (r == 0) {
+                    n_t = n, sum_t = sum, mean_t = mean, m2_t = m2;
+                } else if (n > 0.f) {  // pairwise merge ([Ch7] §7.4.1)
+                    const float nn = n_t + n;
+                    const float wb = n / nn;
+                    const float d = mean - mean_t;
+                    m2_t = m2_t + m2 + d * d * n_t * wb;
+                    mean_t = fmaf(d, wb, mean_t);
+                    sum_t += sum;
+                    n_t = nn;
                 }
-                cluster_barrier();
-                Welford p = welford_empty();
-                if (lane < static_cast<int>(C)) {
-                    p.n = ld_peer_f32(peer_smem_addr(&cta_part[buf][0], lane));
-                    p.mean = ld_peer_f32(peer_smem_addr(&cta_part[buf][1], lane));
-                    p.m2 = ld_peer_f32(peer_smem_addr(&cta_part[buf][2], lane));
-                }
-                st = group_merge(p, 32);
+            } else {
+                ss_t += s.sumsq(nv);
             }
-            mu = st.mean;
-            rs = rsqrtf(st.m2 / static_cast<float>(a.N) + a.eps);
-            if (rank == 0 && tid == 0) {
-                if (a.mean) a.mean[row] = K + mu;
-                if (a.rstd) a.rstd[row] = rs;
-            }
-        } else {
-            ss = group_sum(ss, 32);
-            if (lane == 0) warp_part[buf][0][warp] = ss;
-            __syncthreads();
-            ss = group_sum(lane < nwarps ? warp_part[buf][0][lane] : 0.f, 32);
-            if (C > 1) {
-                if (tid == 0) cta_part[buf][0] = ss;
-                cluster_barrier();
-                ss = group_sum(lane < static_cast<int>(C) ? ld_peer_f32(peer_smem_addr(&cta_part[buf][0], lane)) : 0.f,
-                               32);
-            }
-            rs = rsqrtf(ss / static_cast<float>(a.N) + a.eps);
         }
-
+        float mu, rs;
+        row_stats<LN>(red, n_t, sum_t, mean_t, m2_t, ss_t, invN, a.eps, C, nwarps, wwidth, mu, rs);
+        if (LN && rank == 0 && tid == 0) {
+            if (a.mean) a.mean[row] = K + mu;
+            if (a.rstd) a.rstd[row] = rs;
+        }
         for (int r = rounds - 1; r >= 0; --r) {
-            const int base = (r * static_cast<int>(C) + static_cast<int>(rank)) * V * T_ + tid;
+            const int f = (r * static_cast<int>(C) + rank) * V * T_ + in_slice;
             if (r != rounds - 1) {
-#pragma unroll
-                for (int j = 0; j < V; ++j) {
-                    const int acc = base + j * T_;
-                    ok[j] = acc < nacc;
-                    if (ok[j]) f[j].load(xr + acc * VEC);
-                }
+                nv = valid_runs(nacc, f, 32, V);
+                s.load(xr + f * VEC, stride, nv);
             }
-#pragma unroll
-            for (int j = 0; j < V; ++j)
-                if (ok[j]) emit<T, VEC, LN>(f[j], gamma, beta, yr, (base + j * T_) * VEC, K, mu, rs);
+            s.emit(static_cast<const T*>(a.gamma) + f * VEC, static_cast<const T*>(a.beta) + f * VEC, yr + f * VEC,
+                   stride, nv, mu, rs);
         }
     }
     // No CTA may exit while a peer can still read its shared memory.
     if (C > 1) cluster_barrier();
 }
 
-// ----------------------------------------------------------------- launch
+// ================================================================== PIPE
+// The CTA mapping (one CTA or cluster per row, one round) on a persistent
+// grid, with the next S-1 rows of this CTA in flight while it works on the
+// current one: each thread copies its own 16-byte slots of upcoming rows
+// into a ring of S shared-memory stages with cp.async, and reads a stage
+// only after its own copies into it have landed. The bytes in flight live in
+// shared memory, not registers, so HBM stays busy through the reduction and
+// the stores. Needs 16-byte aligned rows of whole vectors.
+template <class T, int V, bool LN>
+__global__ void __launch_bounds__(1024) norm_fwd_pipe(const NormArgs a) {
+    constexpr int VEC = ElemVec<T>::value;
+    using S = Slice<T, VEC, V, LN>;
+    extern __shared__ uint4 ring[];  // [stages][V*T] 16-byte slots, then [stages][32] words for K
+    __shared__ RowReduceSmem red;
+
+    const int stages = a.stages;
+    const int T_ = blockDim.x;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = T_ >> 5;
+    int wwidth = 1;
+    while (wwidth < nwarps) wwidth <<= 1;
+    const uint32_t C = cluster_size();
+    const int rank = static_cast<int>(cluster_rank());
+    const int64_t first_row = blockIdx.x / C;
+    const int64_t row_step = gridDim.x / C;
+    const int nacc = a.N / VEC;
+    const int stride = 32 * VEC;
+    const int in_slice = warp * V * 32 + lane;
+    const int first = rank * V * T_ + in_slice;  // this thread's first access of every row
+    const int nvalid = valid_runs(nacc, first, 32, V);
+    const float n_t = static_cast<float>(nvalid * VEC);
+    const float inv_n = nvalid > 0 ? 1.f / n_t : 0.f;
+    const float invN = 1.f / static_cast<float>(a.N);
+    const int stage_slots = V * T_;
+    float* kslot = reinterpret_cast<float*>(ring + stages * stage_slots);
+    const T* g = static_cast<const T*>(a.gamma) + first * VEC;
+    const T* b = static_cast<const T*>(a.beta) + first * VEC;
+
+    // Copy this thread's slots of `row` into stage `st`, and for LayerNorm
+    // the row's first element (lane 0 of each warp; 4 bytes at the 16-byte
+    // aligned row start). Always commits one group, so groups and rows stay
+    // in step.
+    auto issue = [&](int64_t row, int st) {
+        if (row < a.M) {
+            const T* src = static_cast<const T*>(a.x) + row * a.N + first * VEC;
+            uint4* dst = ring + st * stage_slots + in_slice;
+#pragma unroll
+            for (int j = 0; j < V; ++j)
+                if (j < nvalid) cp_async16(dst + j * 32, src + j * stride);
+            if (LN && lane == 0) cp_async4(&kslot[st * 32 + warp], static_cast<const T*>(a.x) + row * a.N);
+        }
+        cp_async_commit();
+    };
+
+    for (int k = 0; k < stages - 1; ++k) issue(first_row + k * row_step, k);
+    int st = 0;
+    for (int64_t row = first_row; row < a.M; row += row_step) {
+        issue(row + (stages - 1) * row_step, st == 0 ? stages - 1 : st - 1);
+        cp_async_wait(stages - 1);  // this thread's copies of `row` have landed
+
+        S s;
+        float K = 0.f;
+        if constexpr (LN) {
+            const float kw = __shfl_sync(kFullMask, lane == 0 ? kslot[st * 32 + warp] : 0.f, 0);
+            K = sizeof(T) == 4 ? kw : __uint_as_float(__float_as_uint(kw) << 16);
+        }
+        s.set_shift(K);
+        const uint4* src = ring + st * stage_slots + in_slice;
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            if (j < nvalid) s.set(j, src[j * 32]);
+        float sum = 0.f, mean = 0.f, m2 = 0.f, ss = 0.f;
+        if constexpr (LN)
+            s.welford(nvalid, inv_n, sum, mean, m2);
+        else
+            ss = s.sumsq(nvalid);
+        float mu, rs;
+        row_stats<LN>(red, n_t, sum, mean, m2, ss, invN, a.eps, C, nwarps, wwidth, mu, rs);
+        if (LN && rank == 0 && tid == 0) {
+            if (a.mean) a.mean[row] = K + mu;
+            if (a.rstd) a.rstd[row] = rs;
+        }
+        s.emit(g, b, static_cast<T*>(a.y) + row * a.N + first * VEC, stride, nvalid, mu, rs);
+        st = st + 1 == stages ? 0 : st + 1;
+    }
+    cp_async_wait(0);  // nothing of ours may land after exit
+    // No CTA may exit while a peer can still read its shared memory.
+    if (C > 1) cluster_barrier();
+}
+
+// ================================================================== launch
 template <class T, bool LN>
 using KernelFn = void (*)(const NormArgs);
 
@@ -292,14 +629,70 @@ KernelFn<T, LN> pick_kernel(int mapping, int per_thread) {
 }
 
 template <class T, bool LN>
-cudaError_t launch_norm(const norm_plan& p, const NormArgs& a, cudaStream_t stream) {
-    KernelFn<T, LN> k = p.vec_elems == 1 ? pick_kernel<T, LN, 1>(p.mapping, p.per_thread)
-                                         : pick_kernel<T, LN, ElemVec<T>::value>(p.mapping, p.per_thread);
-    if (k == nullptr) return cudaErrorInvalidValue;
+KernelFn<T, LN> pick_pipe(int per_thread) {
+    switch (per_thread) {
+        case 1: return norm_fwd_pipe<T, 1, LN>;
+        case 2: return norm_fwd_pipe<T, 2, LN>;
+        case 4: return norm_fwd_pipe<T, 4, LN>;
+        case 8: return norm_fwd_pipe<T, 8, LN>;
+        default: return nullptr;
+    }
+}
+
+// Bytes of dynamic shared memory a pipelined launch needs.
+inline size_t pipe_smem_bytes(const norm_plan& p, bool ln) {
+    return static_cast<size_t>(p.stages) * p.per_thread * p.threads * 16 + (ln ? p.stages * 32 * 4 : 0);
+}
+
+// Opt the pipelined kernel in to the device's largest dynamic shared memory
+// per block (once per kernel and device; the call is not a stream operation).
+template <class T, int V, bool LN>
+cudaError_t opt_in_smem(int dev) {
+    static std::atomic<unsigned long long> done{0};
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+    if (bit && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
+    int optin = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, norm_fwd_pipe<T, V, LN>);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(norm_fwd_pipe<T, V, LN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - static_cast<int>(fa.sharedSizeBytes));
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_relaxed);
+    return e;
+}
+
+template <class T, bool LN>
+cudaError_t allow_smem(int per_thread, int dev) {
+    switch (per_thread) {
+        case 1: return opt_in_smem<T, 1, LN>(dev);
+        case 2: return opt_in_smem<T, 2, LN>(dev);
+        case 4: return opt_in_smem<T, 4, LN>(dev);
+        case 8: return opt_in_smem<T, 8, LN>(dev);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <class T, bool LN>
+cudaError_t launch_norm(const norm_plan& p, const NormArgs& a, cudaStream_t stream, int num_sms, int dev) {
+    KernelFn<T, LN> k;
+    size_t smem = 0;
+    if (p.stages > 0) {
+        k = pick_pipe<T, LN>(p.per_thread);
+        if (k == nullptr) return cudaErrorInvalidValue;
+        smem = pipe_smem_bytes(p, LN);
+        const cudaError_t e = allow_smem<T, LN>(p.per_thread, dev);
+        if (e != cudaSuccess) return e;
+    } else {
+        k = p.vec_elems == 1 ? pick_kernel<T, LN, 1>(p.mapping, p.per_thread)
+                             : pick_kernel<T, LN, ElemVec<T>::value>(p.mapping, p.per_thread);
+        if (k == nullptr) return cudaErrorInvalidValue;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.grid), 1, 1);
     cfg.blockDim = dim3(static_cast<unsigned>(p.threads), 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     if (p.mapping == NORM_MAP_CTA && p.cluster > 1) {
@@ -309,6 +702,25 @@ cudaError_t launch_norm(const norm_plan& p, const NormArgs& a, cudaStream_t stre
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
+    }
+    if (p.stages > 0 && p.grid == 0) {
+        // Persistent grid: as many CTAs (whole clusters) as can be resident at
+        // once, so that no row waits for a CTA that never finishes early.
+        int64_t clusters;
+        if (p.cluster > 1) {
+            cfg.gridDim = dim3(static_cast<unsigned>(p.cluster), 1, 1);
+            int n = 0;
+            const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, k, &cfg);
+            if (e != cudaSuccess) return e;
+            clusters = n;
+        } else {
+            int per_sm = 0;
+            const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, p.threads, smem);
+            if (e != cudaSuccess) return e;
+            clusters = int64_t(per_sm) * num_sms;
+        }
+        if (clusters < 1) return cudaErrorInvalidConfiguration;
+        cfg.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(a.M, clusters) * p.cluster), 1, 1);
     }
     return cudaLaunchKernelEx(&cfg, k, a);
 }

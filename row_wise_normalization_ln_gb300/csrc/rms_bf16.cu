@@ -4,8 +4,8 @@
 
 namespace libnorm {
 
-cudaError_t launch_rms_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s) {
-    return launch_norm<__nv_bfloat16, false>(plan, a, s);
+cudaError_t launch_rms_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev) {
+    return launch_norm<__nv_bfloat16, false>(plan, a, s, num_sms, dev);
 }
 
 }  // namespace libnorm

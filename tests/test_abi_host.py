@@ -105,6 +105,12 @@ def _plan(**kw):
     dict(mapping=rn.NORM_MAP_GROUP, group=3),
     dict(mapping=rn.NORM_MAP_GROUP, group=64),
     dict(mapping=rn.NORM_MAP_GROUP, group=8, per_thread=2),   # 8*2*4 < N: does not cover the row
+    dict(stages=1), dict(stages=5), dict(stages=-1),
+    dict(stages=3, vec_elems=1),                # the ring needs 16-byte vectors
+    dict(stages=3, threads=64, per_thread=1),   # 64*1*4 < N: two rounds, not allowed with a ring
+    dict(stages=4, threads=1024, per_thread=8, grid=0),  # 4*1024*8*16 B of ring > 225 KB
+    dict(mapping=rn.NORM_MAP_GROUP, group=32, per_thread=8, stages=2),
+    dict(grid=0),                               # grid 0 only for ring plans
 ])
 def test_bad_plans_rejected(lib, kw):
     p = _plan(**kw)
@@ -119,6 +125,15 @@ def test_vector_plan_needs_alignment(lib):
     assert lib.rms_fwd_planned(q, P, P, 4, 1000, 1e-6, rn.NORM_F32, None, ctypes.byref(p)) == rn.NORM_ERR_PLAN
     # rows of 1001 fp32 are not whole 16-byte vectors
     assert lib.rms_fwd_planned(P, P, P, 4, 1001, 1e-6, rn.NORM_F32, None, ctypes.byref(p)) == rn.NORM_ERR_PLAN
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on the fake pointers")
+def test_ring_plan_accepted_before_launch(lib):
+    """A valid ring plan passes the host checks; without a GPU the call then
+    fails at the device query."""
+    p = _plan(stages=3, grid=0)
+    st = lib.rms_fwd_planned(P, P, P, 4, 1000, 1e-6, rn.NORM_F32, None, ctypes.byref(p))
+    assert st == rn.NORM_ERR_CUDA
 
 
 def _covers(plan, N):
@@ -151,7 +166,11 @@ def test_plans_are_consistent(lib, dtype, aligned, M):
             assert p["grid"] == max(1, -(-M // rows_per_cta))
         else:
             assert p["cluster"] in (1, 2, 4, 8)
-            assert p["grid"] % p["cluster"] == 0 and p["grid"] == M * p["cluster"]
+            if p["stages"]:
+                assert p["grid"] == 0 and p["rounds"] == 1 and p["vec_elems"] > 1
+                assert p["stages"] * p["threads"] * p["per_thread"] * 16 + p["stages"] * 128 <= 225 * 1024
+            else:
+                assert p["grid"] % p["cluster"] == 0 and p["grid"] == M * p["cluster"]
 
 
 def test_plans_for_the_workloads(lib):
@@ -159,12 +178,12 @@ def test_plans_for_the_workloads(lib):
     got = {name: rn.make_plan(w.M, w.N, w.torch_dtype, True, 152) for name, w in WORKLOADS.items()}
     want = {
         "ln_f32_128x1024": dict(mapping=rn.NORM_MAP_CTA, per_thread=1, threads=256, cluster=1, rounds=1),
-        "rms_f32_8192x4096": dict(mapping=rn.NORM_MAP_CTA, per_thread=4, threads=256, cluster=1, rounds=1),
-        "ln_bf16_4096x8192_outliers": dict(mapping=rn.NORM_MAP_CTA, per_thread=4, threads=256, cluster=1,
+        "rms_f32_8192x4096": dict(mapping=rn.NORM_MAP_CTA, per_thread=8, threads=128, cluster=1, rounds=1),
+        "ln_bf16_4096x8192_outliers": dict(mapping=rn.NORM_MAP_CTA, per_thread=8, threads=128, cluster=1,
                                            rounds=1),
-        "rms_bf16_65536x2048": dict(mapping=rn.NORM_MAP_GROUP, per_thread=8, group=32, threads=256, rounds=1),
-        "ln_f32_2048x65536": dict(mapping=rn.NORM_MAP_CTA, per_thread=8, threads=1024, cluster=2, rounds=1),
-        "ln_f32_8192x5000": dict(mapping=rn.NORM_MAP_CTA, per_thread=4, threads=320, cluster=1, rounds=1),
+        "rms_bf16_65536x2048": dict(mapping=rn.NORM_MAP_CTA, per_thread=4, threads=64, cluster=1, rounds=1),
+        "ln_f32_2048x65536": dict(mapping=rn.NORM_MAP_CTA, per_thread=8, threads=256, cluster=8, rounds=1),
+        "ln_f32_8192x5000": dict(mapping=rn.NORM_MAP_CTA, per_thread=8, threads=160, cluster=1, rounds=1),
     }
     for name, w in want.items():
         for k, v in w.items():

@@ -60,6 +60,8 @@ def test_workload_rows_with_full_size_plan(name):
     inp = wl.generate(ws, seed=0)
     if plan["mapping"] == rn.NORM_MAP_GROUP:
         plan["grid"] = -(-ws.M // (plan["threads"] // plan["group"]))
+    elif plan["stages"]:
+        plan["grid"] = plan["cluster"] * 4  # few persistent CTAs: every ring stage is reused
     else:
         plan["grid"] = ws.M * plan["cluster"]
     if w.op == "ln":
@@ -157,6 +159,13 @@ def _variants():
                                 continue
                             out.append((dtype, dict(mapping=rn.NORM_MAP_CTA, vec_elems=ve, per_thread=per,
                                                     group=0, threads=T, cluster=C, grid=C * 3), N))
+                        # the shared-memory ring (vector rows, one round)
+                        for S in (2, 3, 4):
+                            if not v or S * T * per * 16 + S * 128 > 225 * 1024 or cap > 300000:
+                                continue
+                            for N, grid in ((cap, C * 2), (max(ve, cap - 3 * ve), 0)):
+                                out.append((dtype, dict(mapping=rn.NORM_MAP_CTA, vec_elems=ve, per_thread=per,
+                                                        group=0, threads=T, cluster=C, stages=S, grid=grid), N))
     return out
 
 
@@ -165,12 +174,14 @@ VARIANTS = _variants()
 
 @pytest.mark.parametrize("dtype,plan,N", VARIANTS,
                          ids=[f"{d}-m{p['mapping']}-v{p['vec_elems']}-p{p['per_thread']}-g{p['group']}"
-                              f"-t{p['threads']}-c{p['cluster']}-N{n}" for d, p, n in VARIANTS])
+                              f"-t{p['threads']}-c{p['cluster']}-s{p.get('stages', 0)}-grid{p['grid']}-N{n}"
+                              for d, p, n in VARIANTS])
 def test_every_variant(dtype, plan, N):
     """Explicit plans: each (mapping, width, registers, group, CTA size,
-    cluster size, rounds) variant with a grid smaller than the row count, so
-    the grid-stride loop takes several turns."""
-    M = 7
+    cluster size, rounds, ring stages) variant with a grid smaller than the
+    row count, so the grid-stride loop takes several turns and the ring
+    wraps."""
+    M = 7 if not plan.get("stages") else 11
     x, g, b = _rand(M, N, DT[dtype], seed=N + plan["threads"], loc=-1.5, scale=2.0)
     y, mean, rstd = run_ln(x, g, b, 1e-5, plan=plan)
     check_ln(x, g, b, 1e-5, y, mean, rstd)
