@@ -70,15 +70,19 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch, from the ncu
+# capture summarised in profiles/ (workload -> (kernel source hash at capture,
+# bytes per launch, summary file)).
+NCU_TRAFFIC = {
+    "rms_f32_8192x4096": ("6bc9852828c29a6c", 213_732_608, "profiles/norm_fwd_cta_rms_f32_8192x4096.md"),
+}
+
+
 def ncu_traffic(workload: str):
-    """dram bytes per launch from the committed ncu summary, if it was taken
-    on the kernel sources as they are now."""
-    try:
-        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            t = json.load(f)[workload]
-    except (OSError, KeyError, ValueError):
-        return None
-    return t["dram_bytes_per_launch"] if t.get("kernel_hash") == kernel_source_hash() else None
+    """DRAM bytes per launch from the committed ncu capture, or None when the
+    kernel sources changed since it was taken."""
+    t = NCU_TRAFFIC.get(workload)
+    return t[1] if t and t[0] == kernel_source_hash() else None
 
 
 def kernel_name(w, plan) -> str:
@@ -328,6 +332,25 @@ def cpu_baseline(w, inp, seconds: float):
             "host_cores": os.cpu_count()}
 
 
+# ------------------------------------------------------------------ ranks
+
+def max_over_ranks(ms: float, device) -> float:
+    """The slowest rank's time (all ranks get it); the value itself alone."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_call: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank normalised `steps` calls' worth of
+    rows (weak scaling), timed by the slowest rank."""
+    return bytes_per_call * steps * world / (max_ms / 1e3) / 1e9
+
+
 # ------------------------------------------------------------------ main
 
 def dist_env():
@@ -397,15 +420,10 @@ def main():
     uuid = str(getattr(props, "uuid", "")) or None
     sampler = ClockSampler(uuid) if rank == 0 else None
     total_ms, kern_ms, clocks = time_launches(w, rn, inp, device, args.steps, args.warmup, sampler, barrier)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-
+    total_ms = max_over_ranks(total_ms, device)
     bytes_per_call = w.algorithmic_bytes()
     ms_per_step = total_ms / args.steps
-    value = bytes_per_call * args.steps * world / (total_ms / 1e3) / 1e9
+    value = job_gbs(bytes_per_call, args.steps, world, total_ms)
     achieved = bytes_per_call / (kern_ms / 1e3) / 1e9
     peak, peak_src = measured_peak()
     traffic = ncu_traffic(w.name)
