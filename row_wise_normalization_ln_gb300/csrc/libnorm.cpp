@@ -56,10 +56,11 @@ int vec_for(int64_t N, norm_dtype dtype, bool all_aligned) {
     return (all_aligned && (N * s) % 16 == 0) ? 16 / s : 1;
 }
 
-// The planner. Measured on GB300 (see the sweep notes of the design
-// document): rows do best with 8 accesses (128 bytes) in registers per
-// thread, CTAs of 64 to 256 threads, and long rows split over a cluster of
-// up to 8 such CTAs; lane groups only pay off below 64 accesses per row.
+// The planner, from plan sweeps on GB300: rows do best with 8 accesses (128
+// bytes) in registers per thread and CTAs of 64 to 256 threads; rows longer
+// than 256 such threads go to a cluster of up to 8 CTAs of 128 threads, each
+// walking its share in two rounds; lane groups only pay off below 64
+// accesses per row.
 norm_status make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_aligned, int num_sms, norm_plan* p) {
     std::memset(p, 0, sizeof *p);
     const int vec = vec_for(N, dtype, all_aligned);
@@ -90,10 +91,13 @@ norm_status make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_aligned, 
     }
     int64_t cluster = 1;
     if (threads > 256) {
-        cluster = std::min<int64_t>(ceil_div(threads, 256), kMaxCluster);
-        cluster = pow2_ceil(cluster);
-        if (cluster > kMaxCluster) cluster = kMaxCluster;
-        threads = std::min<int64_t>(round_up(ceil_div(nacc, cluster * per), 32), kMaxThreads);
+        // Long rows: slices of 128 threads x 8 accesses, two register rounds
+        // per slice, over a cluster of up to 8 CTAs (the second half of each
+        // slice is read again from L2 for the output).
+        const int64_t slices = ceil_div(nacc, int64_t(128) * per);
+        cluster = std::min<int64_t>(pow2_ceil(ceil_div(slices, 2)), kMaxCluster);
+        const int64_t rounds = ceil_div(slices, cluster);
+        threads = std::min<int64_t>(round_up(ceil_div(nacc, cluster * per * rounds), 32), 128);
     }
     // Few rows: trade registers per thread for more threads per row.
     while (per > 1 && M * cluster * threads < busy_threads) {

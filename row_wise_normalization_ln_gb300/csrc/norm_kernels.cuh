@@ -51,46 +51,23 @@ struct ElemVec {
 
 // ================================================================== element math
 // One access is a 16-byte vector (4 fp32 or 8 bf16) held as a uint4, or a
-// single element (VEC = 1) held in the low bits of a uint32. The bf16
-// routines use the sm_100-family mixed-precision instructions, which widen a
-// bf16 operand exactly inside one rounded fp32 add/sub/fma.
+// single element (VEC = 1) held in the low bits of a uint32. bf16 values are
+// widened exactly (a bf16 pattern is the top half of an fp32 pattern).
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-// (lo - K, hi - K) of the two bf16 values packed in w, each rounded once.
-__device__ __forceinline__ float2 bf16x2_minus(uint32_t w, float K) {
-    float lo, hi;
-    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
-        "sub.rn.f32.bf16 %0, l, %3;\n\tsub.rn.f32.bf16 %1, h, %3;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(w), "f"(K));
-    return make_float2(lo, hi);
-}
-
-// acc + lo^2 + hi^2 (each product exact in fp32, each sum rounded once).
-__device__ __forceinline__ float bf16x2_sumsq(uint32_t w, float acc) {
-    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\t"
-        "fma.rn.f32.bf16 %0, l, l, %0;\n\tfma.rn.f32.bf16 %0, h, h, %0;\n\t}"
-        : "+f"(acc)
-        : "r"(w));
-    return acc;
-}
-
-// (a_lo * b_lo, a_hi * b_hi): products of bf16 values, exact in fp32.
-__device__ __forceinline__ float2 bf16x2_mul(uint32_t a, uint32_t b) {
-    float lo, hi;
-    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
-        "fma.rn.f32.bf16 %0, al, bl, 0f00000000;\n\tfma.rn.f32.bf16 %1, ah, bh, 0f00000000;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(a), "r"(b));
-    return make_float2(lo, hi);
-}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);  // round to nearest-even
     return *reinterpret_cast<const uint32_t*>(&b);
 }
+
+// bf16 rows widen each pair of values exactly to an fp32 pair and work on it
+// with the sm_100-family packed instructions (two IEEE fp32 operations, each
+// rounded to nearest-even, per instruction); fp32 rows use scalar fp32
+// instructions (measured faster there).
+__device__ __forceinline__ float2 f2_splat(float v) { return make_float2(v, v); }
+__device__ __forceinline__ float2 bf16x2_widen(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
 
 // Per-access operations, specialised on element type and width.
 template <class T, int VEC>
@@ -151,43 +128,50 @@ struct Ops<__nv_bfloat16, 8> {
         return i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w;
     }
     static __device__ __forceinline__ float shifted_sum(const Raw& r, float K) {
-        const float2 a = bf16x2_minus(r.x, K), b = bf16x2_minus(r.y, K);
-        const float2 c = bf16x2_minus(r.z, K), d = bf16x2_minus(r.w, K);
-        return ((a.x + a.y) + (b.x + b.y)) + ((c.x + c.y) + (d.x + d.y));
+        const float2 nk = f2_splat(-K);
+        const float2 a = __fadd2_rn(__fadd2_rn(bf16x2_widen(r.x), nk), __fadd2_rn(bf16x2_widen(r.y), nk));
+        const float2 b = __fadd2_rn(__fadd2_rn(bf16x2_widen(r.z), nk), __fadd2_rn(bf16x2_widen(r.w), nk));
+        const float2 s = __fadd2_rn(a, b);
+        return s.x + s.y;
     }
     static __device__ __forceinline__ float dev2(const Raw& r, float K, float mu, float acc) {
+        const float2 nk = f2_splat(-K), nm = f2_splat(-mu);
+        float2 q = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float2 s = bf16x2_minus(w(r, i), K);
-            const float d0 = s.x - mu, d1 = s.y - mu;
-            acc = fmaf(d0, d0, acc);
-            acc = fmaf(d1, d1, acc);
+            const float2 d = __fadd2_rn(__fadd2_rn(bf16x2_widen(w(r, i)), nk), nm);
+            q = __ffma2_rn(d, d, q);
         }
-        return acc;
+        return acc + (q.x + q.y);
     }
     static __device__ __forceinline__ float sumsq(const Raw& r, float acc) {
+        float2 q = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc = bf16x2_sumsq(w(r, i), acc);
-        return acc;
+        for (int i = 0; i < 4; ++i) {
+            const float2 x = bf16x2_widen(w(r, i));
+            q = __ffma2_rn(x, x, q);
+        }
+        return acc + (q.x + q.y);
     }
     static __device__ __forceinline__ Raw ln_out(const Raw& r, float K, float rs, float nmr, const Raw& g,
                                                  const Raw& b) {
+        const float2 nk = f2_splat(-K), rs2 = f2_splat(rs), nm2 = f2_splat(nmr);
         uint32_t o[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float2 s = bf16x2_minus(w(r, i), K);
-            const uint32_t gi = w(g, i), bi = w(b, i);
-            o[i] = pack_bf16x2(fmaf(fmaf(s.x, rs, nmr), bf16_lo(gi), bf16_lo(bi)),
-                               fmaf(fmaf(s.y, rs, nmr), bf16_hi(gi), bf16_hi(bi)));
+            const float2 y = __ffma2_rn(__ffma2_rn(__fadd2_rn(bf16x2_widen(w(r, i)), nk), rs2, nm2),
+                                        bf16x2_widen(w(g, i)), bf16x2_widen(w(b, i)));
+            o[i] = pack_bf16x2(y.x, y.y);
         }
         return make_uint4(o[0], o[1], o[2], o[3]);
     }
     static __device__ __forceinline__ Raw rms_out(const Raw& r, float rs, const Raw& wt) {
+        const float2 rs2 = f2_splat(rs);
         uint32_t o[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float2 p = bf16x2_mul(w(r, i), w(wt, i));
-            o[i] = pack_bf16x2(p.x * rs, p.y * rs);
+            const float2 y = __fmul2_rn(__fmul2_rn(bf16x2_widen(w(r, i)), bf16x2_widen(w(wt, i))), rs2);
+            o[i] = pack_bf16x2(y.x, y.y);
         }
         return make_uint4(o[0], o[1], o[2], o[3]);
     }

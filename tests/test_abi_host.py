@@ -182,7 +182,7 @@ def test_plans_for_the_workloads(lib):
         "ln_bf16_4096x8192_outliers": dict(mapping=rn.NORM_MAP_CTA, per_thread=8, threads=128, cluster=1,
                                            rounds=1),
         "rms_bf16_65536x2048": dict(mapping=rn.NORM_MAP_CTA, per_thread=4, threads=64, cluster=1, rounds=1),
-        "ln_f32_2048x65536": dict(mapping=rn.NORM_MAP_CTA, per_thread=8, threads=256, cluster=8, rounds=1),
+        "ln_f32_2048x65536": dict(mapping=rn.NORM_MAP_CTA, per_thread=8, threads=128, cluster=8, rounds=2),
         "ln_f32_8192x5000": dict(mapping=rn.NORM_MAP_CTA, per_thread=8, threads=160, cluster=1, rounds=1),
     }
     for name, w in want.items():
