@@ -67,6 +67,18 @@ __device__ __forceinline__ float ld_peer_f32(uint32_t addr) {
     return v;
 }
 
+// ----------------------------------------------------------- dependent launch
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may be scheduled before the previous kernel
+// in its stream has finished. `grid_wait` blocks until that previous grid has
+// completed and its memory is visible (a no-op without such a dependency), so
+// every kernel calls it before its first global memory access;
+// `grid_release` lets the next such launch be scheduled once every CTA of
+// this grid has issued it. Kernels launched without the attribute (any
+// other library's) still wait for this grid to complete.
+__device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_release() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ----------------------------------------------------------------- cp.async
 // Per-thread asynchronous global -> shared copies. A thread waits for its own
 // copies with cp.async.wait_group, a hardware wait (no polling loop), and

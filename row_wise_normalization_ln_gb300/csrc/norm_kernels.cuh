@@ -393,6 +393,8 @@ __global__ void __launch_bounds__(1024) norm_fwd_group(const NormArgs a) {
     const float invN = 1.f / static_cast<float>(a.N);
     const T* g = static_cast<const T*>(a.gamma) + gl * VEC;
     const T* b = static_cast<const T*>(a.beta) + gl * VEC;
+    grid_release();
+    grid_wait();
 
     for (int64_t rb = blockIdx.x; rb * rows_per_cta < a.M; rb += gridDim.x) {
         const int64_t row = rb * rows_per_cta + tid / G;
@@ -452,6 +454,8 @@ __global__ void __launch_bounds__(1024) norm_fwd_cta(const NormArgs a) {
     const int stride = 32 * VEC;
     const int in_slice = warp * V * 32 + lane;  // this thread's first access within a slice
     const float invN = 1.f / static_cast<float>(a.N);
+    grid_release();
+    grid_wait();
 
     for (int64_t row = first_row; row < a.M; row += row_step) {
         const T* xr = static_cast<const T*>(a.x) + row * a.N;
@@ -560,6 +564,8 @@ __global__ void __launch_bounds__(1024) norm_fwd_pipe(const NormArgs a) {
         cp_async_commit();
     };
 
+    grid_release();
+    grid_wait();
     for (int k = 0; k < stages - 1; ++k) issue(first_row + k * row_step, k);
     int st = 0;
     for (int64_t row = first_row; row < a.M; row += row_step) {
@@ -678,14 +684,17 @@ cudaError_t launch_norm(const norm_plan& p, const NormArgs& a, cudaStream_t stre
     cfg.blockDim = dim3(static_cast<unsigned>(p.threads), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (p.mapping == NORM_MAP_CTA && p.cluster > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     if (p.stages > 0 && p.grid == 0) {
         // Persistent grid: as many CTAs (whole clusters) as can be resident at

@@ -323,3 +323,48 @@ def test_more_than_2_31_elements():
     check_ln(xs, g, b, 1e-5, y[idx], mean[idx], rstd[idx])
     del x, y, mean, rstd
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------ ordering
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_chained_calls_read_the_previous_output(dtype):
+    """Calls that consume the previous call's output, back to back on one
+    stream with no synchronisation (each kernel may be scheduled before its
+    predecessor ends, and must still see its output): each link equals the
+    oracle applied to the previous link's GPU result."""
+    N, M = 4096, 2048
+    x, g, b = _rand(M, N, dtype, seed=21, loc=1.0, scale=2.0)
+    xd, gd, bd = x.cuda(), g.cuda(), b.cuda()
+    outs = [xd]
+    for i in range(6):
+        y, _, _ = rn.ln_fwd(outs[-1], gd, bd, 1e-5)
+        outs.append(rn.rms_fwd(y, gd, 1e-6))
+    torch.cuda.synchronize()
+    for i in range(6):
+        y, mean, rstd = rn.ln_fwd(outs[i], gd, bd, 1e-5)   # recomputed in isolation
+        check_ln(outs[i].cpu(), g, b, 1e-5, y, mean, rstd)
+        check_rms(y.cpu(), g, 1e-6, outs[i + 1])
+
+
+def test_chained_calls_in_a_cuda_graph():
+    N, M = 8192, 512
+    x, g, b = _rand(M, N, torch.float32, seed=22)
+    xd, gd, bd = x.cuda(), g.cuda(), b.cuda()
+    bufs = [torch.empty_like(xd) for _ in range(4)]
+    rn.ln_fwd(xd, gd, bd, 1e-5, out=bufs[0], stats=False)  # warm-up outside capture
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            rn.ln_fwd(xd, gd, bd, 1e-5, out=bufs[0], stats=False)
+            for i in range(3):
+                rn.rms_fwd(bufs[i], gd, 1e-6, out=bufs[i + 1])
+    for _ in range(3):
+        for t in bufs:
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        check_ln(x, g, b, 1e-5, bufs[0])
+        for i in range(3):
+            check_rms(bufs[i].cpu(), g, 1e-6, bufs[i + 1])
