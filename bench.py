@@ -74,7 +74,9 @@ def measured_peak():
 # capture summarised in profiles/ (workload -> (kernel source hash at capture,
 # bytes per launch, summary file)).
 NCU_TRAFFIC = {
-    "rms_f32_8192x4096": ("6bc9852828c29a6c", 213_732_608, "profiles/norm_fwd_cta_rms_f32_8192x4096.md"),
+    "rms_f32_8192x4096": ("2d3d331698cbe55d", 213_520_384, "profiles/norm_fwd_cta_rms_f32_8192x4096.md"),
+    "ln_bf16_4096x8192_outliers": ("2d3d331698cbe55d", 85_777_152, "profiles/norm_fwd_cta_ln_bf16_4096x8192.md"),
+    "ln_f32_2048x65536": ("2d3d331698cbe55d", 1_032_792_576, "profiles/norm_fwd_cta_ln_f32_2048x65536.md"),
 }
 
 
@@ -181,6 +183,35 @@ def step_fn(w, rn, params):
         def f(s):
             rn.rms_fwd(s["x"], wt, w.eps, out=s["y"])
     return f
+
+
+def time_same_bytes_copy(w, inp, device, steps=600, per_graph=60):
+    """Device time of torch's copy of x into y (read M*N, write M*N: the
+    algorithmic bytes minus parameters and statistics), graph-replayed over
+    the same rotating sets: what a plain copy of this size achieves."""
+    import torch
+    sets, _ = make_sets(w, inp, n_sets_for(w), device)
+    for s in sets[:3]:
+        s["y"].copy_(s["x"])
+    side = torch.cuda.Stream(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for i in range(per_graph):
+                sets[i % len(sets)]["y"].copy_(sets[i % len(sets)]["x"])
+    g.replay()
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps // per_graph):
+        g.replay()
+    t1.record()
+    torch.cuda.synchronize(device)
+    ms = t0.elapsed_time(t1) / (steps // per_graph * per_graph)
+    del g, sets
+    torch.cuda.empty_cache()
+    return ms
 
 
 def n_sets_for(w):
@@ -438,8 +469,13 @@ def main():
             _, ms, _ = time_launches(wk, rn, wi, device, 600, 10, per_graph=60)
             us = ms * 1e3
             gbs = wk.algorithmic_bytes() / (us / 1e6) / 1e9
+            copy_us = time_same_bytes_copy(wk, wi, device) * 1e3
             table[name] = {"us_per_call": round(us, 3), "GBps": round(gbs, 1),
                            "frac_of_measured_peak": round(gbs / peak, 4),
+                           "same_size_copy_us": round(copy_us, 3),
+                           # achieved GB/s over the same-size copy's GB/s
+                           "frac_of_same_size_copy": round(gbs / ((2 * wk.M * wk.N * wk.elem_size) / (copy_us / 1e6) / 1e9),
+                                                           4),
                            "rows_per_s": round(wk.M / (us / 1e6)), "plan": rn.make_plan(
                                wk.M, wk.N, wk.torch_dtype, True, props.multi_processor_count)}
             del wi
