@@ -357,7 +357,10 @@ __device__ __forceinline__ float row_sum(RowReduceSmem& red, int stage, float v,
 }
 
 // Row statistics from each thread's Welford state (LayerNorm) or sum of
-// squares (RMSNorm): the shifted mean mu and rstd, identical in every thread.
+// squares (RMSNorm): the shifted mean mu and rstd, identical in every thread
+// of every CTA of the cluster. (Merging each CTA's state first and
+// exchanging one state per CTA, with one cluster barrier per row instead of
+// two, measured slower on GB300.)
 template <bool LN>
 __device__ __forceinline__ void row_stats(RowReduceSmem& red, float n_t, float sum_t, float mean_t, float m2_t,
                                           float ss_t, float invN, float eps, uint32_t C, int nwarps, int wwidth,
@@ -432,8 +435,9 @@ __global__ void __launch_bounds__(1024) norm_fwd_group(const NormArgs a) {
 // several rounds each round is read for the statistics (its Welford state
 // folded into the thread's state with the pairwise merge); the output pass
 // then walks the rounds backwards, reusing the registers of the last round
-// and re-reading the others.
-template <class T, int VEC, int V, bool LN>
+// and re-reading the others. CL: launched with clusters (C > 1); without,
+// every cluster step compiles away.
+template <class T, int VEC, int V, bool LN, bool CL>
 __global__ void __launch_bounds__(1024) norm_fwd_cta(const NormArgs a) {
     using S = Slice<T, VEC, V, LN>;
     __shared__ RowReduceSmem red;
@@ -445,8 +449,8 @@ __global__ void __launch_bounds__(1024) norm_fwd_cta(const NormArgs a) {
     const int nwarps = T_ >> 5;
     int wwidth = 1;  // power of two >= the number of warps
     while (wwidth < nwarps) wwidth <<= 1;
-    const uint32_t C = cluster_size();
-    const int rank = static_cast<int>(cluster_rank());
+    const uint32_t C = CL ? cluster_size() : 1u;  // compile-time 1 without a cluster
+    const int rank = CL ? static_cast<int>(cluster_rank()) : 0;
     const int64_t first_row = blockIdx.x / C;
     const int64_t row_step = gridDim.x / C;
     const int nacc = (a.N + VEC - 1) / VEC;
@@ -516,7 +520,7 @@ __global__ void __launch_bounds__(1024) norm_fwd_cta(const NormArgs a) {
 // only after its own copies into it have landed. The bytes in flight live in
 // shared memory, not registers, so HBM stays busy through the reduction and
 // the stores. Needs 16-byte aligned rows of whole vectors.
-template <class T, int V, bool LN>
+template <class T, int V, bool LN, bool CL>
 __global__ void __launch_bounds__(1024) norm_fwd_pipe(const NormArgs a) {
     constexpr int VEC = ElemVec<T>::value;
     using S = Slice<T, VEC, V, LN>;
@@ -531,8 +535,8 @@ __global__ void __launch_bounds__(1024) norm_fwd_pipe(const NormArgs a) {
     const int nwarps = T_ >> 5;
     int wwidth = 1;
     while (wwidth < nwarps) wwidth <<= 1;
-    const uint32_t C = cluster_size();
-    const int rank = static_cast<int>(cluster_rank());
+    const uint32_t C = CL ? cluster_size() : 1u;  // compile-time 1 without a cluster
+    const int rank = CL ? static_cast<int>(cluster_rank()) : 0;
     const int64_t first_row = blockIdx.x / C;
     const int64_t row_step = gridDim.x / C;
     const int nacc = a.N / VEC;
@@ -606,25 +610,35 @@ __global__ void __launch_bounds__(1024) norm_fwd_pipe(const NormArgs a) {
 template <class T, bool LN>
 using KernelFn = void (*)(const NormArgs);
 
+template <class T, bool LN, int VEC, int V>
+KernelFn<T, LN> pick_cta(bool cl) {
+    return cl ? norm_fwd_cta<T, VEC, V, LN, true> : norm_fwd_cta<T, VEC, V, LN, false>;
+}
+
 template <class T, bool LN, int VEC>
-KernelFn<T, LN> pick_kernel(int mapping, int per_thread) {
+KernelFn<T, LN> pick_kernel(int mapping, int per_thread, bool cl) {
     const bool group = mapping == NORM_MAP_GROUP;
     switch (per_thread) {
-        case 1: return group ? norm_fwd_group<T, VEC, 1, LN> : norm_fwd_cta<T, VEC, 1, LN>;
-        case 2: return group ? norm_fwd_group<T, VEC, 2, LN> : norm_fwd_cta<T, VEC, 2, LN>;
-        case 4: return group ? norm_fwd_group<T, VEC, 4, LN> : norm_fwd_cta<T, VEC, 4, LN>;
-        case 8: return group ? norm_fwd_group<T, VEC, 8, LN> : norm_fwd_cta<T, VEC, 8, LN>;
+        case 1: return group ? norm_fwd_group<T, VEC, 1, LN> : pick_cta<T, LN, VEC, 1>(cl);
+        case 2: return group ? norm_fwd_group<T, VEC, 2, LN> : pick_cta<T, LN, VEC, 2>(cl);
+        case 4: return group ? norm_fwd_group<T, VEC, 4, LN> : pick_cta<T, LN, VEC, 4>(cl);
+        case 8: return group ? norm_fwd_group<T, VEC, 8, LN> : pick_cta<T, LN, VEC, 8>(cl);
         default: return nullptr;
     }
 }
 
+template <class T, bool LN, int V>
+KernelFn<T, LN> pick_pipe_v(bool cl) {
+    return cl ? norm_fwd_pipe<T, V, LN, true> : norm_fwd_pipe<T, V, LN, false>;
+}
+
 template <class T, bool LN>
-KernelFn<T, LN> pick_pipe(int per_thread) {
+KernelFn<T, LN> pick_pipe(int per_thread, bool cl) {
     switch (per_thread) {
-        case 1: return norm_fwd_pipe<T, 1, LN>;
-        case 2: return norm_fwd_pipe<T, 2, LN>;
-        case 4: return norm_fwd_pipe<T, 4, LN>;
-        case 8: return norm_fwd_pipe<T, 8, LN>;
+        case 1: return pick_pipe_v<T, LN, 1>(cl);
+        case 2: return pick_pipe_v<T, LN, 2>(cl);
+        case 4: return pick_pipe_v<T, LN, 4>(cl);
+        case 8: return pick_pipe_v<T, LN, 8>(cl);
         default: return nullptr;
     }
 }
@@ -634,9 +648,9 @@ inline size_t pipe_smem_bytes(const norm_plan& p, bool ln) {
     return static_cast<size_t>(p.stages) * p.per_thread * p.threads * 16 + (ln ? p.stages * 32 * 4 : 0);
 }
 
-// Opt the pipelined kernel in to the device's largest dynamic shared memory
+// Opt a pipelined kernel in to the device's largest dynamic shared memory
 // per block (once per kernel and device; the call is not a stream operation).
-template <class T, int V, bool LN>
+template <class T, int V, bool LN, bool CL>
 cudaError_t opt_in_smem(int dev) {
     static std::atomic<unsigned long long> done{0};
     const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
@@ -645,21 +659,26 @@ cudaError_t opt_in_smem(int dev) {
     cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, norm_fwd_pipe<T, V, LN>);
+    e = cudaFuncGetAttributes(&fa, norm_fwd_pipe<T, V, LN, CL>);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(norm_fwd_pipe<T, V, LN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(norm_fwd_pipe<T, V, LN, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              optin - static_cast<int>(fa.sharedSizeBytes));
     if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_relaxed);
     return e;
 }
 
+template <class T, bool LN, int V>
+cudaError_t allow_smem_v(bool cl, int dev) {
+    return cl ? opt_in_smem<T, V, LN, true>(dev) : opt_in_smem<T, V, LN, false>(dev);
+}
+
 template <class T, bool LN>
-cudaError_t allow_smem(int per_thread, int dev) {
+cudaError_t allow_smem(int per_thread, bool cl, int dev) {
     switch (per_thread) {
-        case 1: return opt_in_smem<T, 1, LN>(dev);
-        case 2: return opt_in_smem<T, 2, LN>(dev);
-        case 4: return opt_in_smem<T, 4, LN>(dev);
-        case 8: return opt_in_smem<T, 8, LN>(dev);
+        case 1: return allow_smem_v<T, LN, 1>(cl, dev);
+        case 2: return allow_smem_v<T, LN, 2>(cl, dev);
+        case 4: return allow_smem_v<T, LN, 4>(cl, dev);
+        case 8: return allow_smem_v<T, LN, 8>(cl, dev);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -668,15 +687,16 @@ template <class T, bool LN>
 cudaError_t launch_norm(const norm_plan& p, const NormArgs& a, cudaStream_t stream, int num_sms, int dev) {
     KernelFn<T, LN> k;
     size_t smem = 0;
+    const bool cl = p.mapping == NORM_MAP_CTA && p.cluster > 1;
     if (p.stages > 0) {
-        k = pick_pipe<T, LN>(p.per_thread);
+        k = pick_pipe<T, LN>(p.per_thread, cl);
         if (k == nullptr) return cudaErrorInvalidValue;
         smem = pipe_smem_bytes(p, LN);
-        const cudaError_t e = allow_smem<T, LN>(p.per_thread, dev);
+        const cudaError_t e = allow_smem<T, LN>(p.per_thread, cl, dev);
         if (e != cudaSuccess) return e;
     } else {
-        k = p.vec_elems == 1 ? pick_kernel<T, LN, 1>(p.mapping, p.per_thread)
-                             : pick_kernel<T, LN, ElemVec<T>::value>(p.mapping, p.per_thread);
+        k = p.vec_elems == 1 ? pick_kernel<T, LN, 1>(p.mapping, p.per_thread, cl)
+                             : pick_kernel<T, LN, ElemVec<T>::value>(p.mapping, p.per_thread, cl);
         if (k == nullptr) return cudaErrorInvalidValue;
     }
     cudaLaunchConfig_t cfg = {};
