@@ -50,8 +50,9 @@ def lib():
         L.oracle_round_bf16.argtypes = [vp, vp, i64]
         L.oracle_welford_update.argtypes = [ctypes.POINTER(Welford), dbl]
         L.oracle_chan_combine.argtypes = [ctypes.POINTER(Welford)] * 3
+        L.oracle_add_round.argtypes = [vp, vp, i32, i64, vp]
         for f in ("oracle_row_moments", "oracle_ln_fwd", "oracle_rms_fwd", "oracle_round_f32",
-                  "oracle_round_bf16", "oracle_welford_update", "oracle_chan_combine"):
+                  "oracle_round_bf16", "oracle_welford_update", "oracle_chan_combine", "oracle_add_round"):
             getattr(L, f).restype = None
         L.oracle_abi_version.restype = ctypes.c_int
         _lib = L
@@ -129,6 +130,28 @@ def round_bf16(v: np.ndarray) -> np.ndarray:
     out = np.empty(v.shape, np.uint16)
     lib().oracle_round_bf16(_ptr(v), _ptr(out), v.size)
     return out
+
+
+def add_round(x: np.ndarray, r: np.ndarray) -> np.ndarray:
+    """Residual add h = x + r rounded to the inputs' type (same shape)."""
+    x, r = _c(x), _c(r)
+    code = _dtype_code(x)
+    assert _dtype_code(r) == code and x.shape == r.shape
+    h = np.empty_like(x)
+    lib().oracle_add_round(_ptr(x), _ptr(r), code, x.size, _ptr(h))
+    return h
+
+
+def ln_fwd_add(x, r, gamma, beta, eps):
+    """Fused residual add + LayerNorm: returns (h, y, mean, rstd)."""
+    h = add_round(x, r)
+    return (h,) + ln_fwd(h, gamma, beta, eps)
+
+
+def rms_fwd_add(x, r, w, eps):
+    """Fused residual add + RMSNorm: returns (h, y, rstd)."""
+    h = add_round(x, r)
+    return (h,) + rms_fwd(h, w, eps)
 
 
 def welford_update(s: Welford, x: float) -> Welford:

@@ -209,4 +209,26 @@ void oracle_chan_combine(const orc_welford *a, const orc_welford *b,
     *out = r;
 }
 
-int oracle_abi_version(void) { return 1; }
+/*
+ * Fused residual add ([Ch7] §7.9-7.10, the fused add + norm of the residual
+ * stream; [T3] §⑤): h = x + residual, rounded to the row type, as an
+ * unfused add that stores h would leave it. The sum is formed in double
+ * (exact for two bf16 values; for fp32 values exact or carrying more than
+ * 2*24+2 bits, so rounding it once more to the row type gives the correctly
+ * rounded sum) and rounded to the row type. The norm of the
+ * fused op is then the norm of h (oracle_ln_fwd / oracle_rms_fwd on h).
+ */
+void oracle_add_round(const void *x, const void *r, int dtype, int64_t n, void *h)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        const double v = orc_load(x, dtype, i) + orc_load(r, dtype, i);
+        if (dtype == ORC_F32)
+            ((float *)h)[i] = (float)v;
+        else if (dtype == ORC_BF16)
+            ((uint16_t *)h)[i] = orc_bf16(v);
+        else
+            ((double *)h)[i] = v;
+    }
+}
+
+int oracle_abi_version(void) { return 2; }

@@ -348,3 +348,42 @@ def test_round_f32_matches_numpy():
     rng = np.random.default_rng(8)
     v = rng.normal(0, 1, 100000) * np.exp2(rng.integers(-60, 60, 100000))
     assert np.array_equal(oracle.round_f32(v), v.astype(np.float32))
+
+
+# ---------------------------------------------------------------- residual add
+
+def test_add_round_matches_torch():
+    """Library routine: torch adds fp32 tensors with one IEEE rounding and
+    bf16 tensors in fp32 then rounds to bf16 (which equals one rounding of
+    the exact sum, fp32 having more than 2*8+2 bits)."""
+    g = torch.Generator().manual_seed(11)
+    x = torch.randn(4096, generator=g) * torch.exp2(torch.randint(-20, 20, (4096,), generator=g).float())
+    r = torch.randn(4096, generator=g) * torch.exp2(torch.randint(-20, 20, (4096,), generator=g).float())
+    h = oracle.add_round(x.numpy(), r.numpy())
+    assert np.array_equal(h, (x + r).numpy())
+    xb, rb = x.to(torch.bfloat16), r.to(torch.bfloat16)
+    hb = oracle.add_round(xb.view(torch.int16).numpy().view(np.uint16), rb.view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(hb, (xb + rb).view(torch.int16).numpy().view(np.uint16))
+
+
+def test_add_round_exact_cases():
+    one = np.array([1.0], np.float32)
+    assert oracle.add_round(one, np.array([2.0 ** -24], np.float32))[0] == 1.0          # tie to even
+    assert oracle.add_round(one, np.array([3 * 2.0 ** -24], np.float32))[0] == np.float32(1 + 2.0 ** -22)
+    b = lambda v: (np.array([v], np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert int(oracle.add_round(b(1.0), b(2.0 ** -8))[0]) == 0x3F80                       # tie to even (down)
+    assert int(oracle.add_round(b(1.0 + 2.0 ** -7), b(2.0 ** -8))[0]) == 0x3F82           # tie to even (up)
+
+
+def test_fused_add_is_norm_of_the_sum():
+    rng = np.random.default_rng(12)
+    x = rng.normal(0, 1, (3, 257)).astype(np.float32)
+    r = rng.normal(5, 2, (3, 257)).astype(np.float32)
+    g = rng.uniform(0.5, 1.5, 257).astype(np.float32)
+    b = rng.uniform(-0.1, 0.1, 257).astype(np.float32)
+    h, y, mean, rstd = oracle.ln_fwd_add(x, r, g, b, 1e-5)
+    assert np.array_equal(h, x + r)
+    y2, mean2, rstd2 = oracle.ln_fwd(x + r, g, b, 1e-5)
+    assert np.array_equal(y, y2) and np.array_equal(mean, mean2) and np.array_equal(rstd, rstd2)
+    h, y, rstd = oracle.rms_fwd_add(x, r, g, 1e-6)
+    assert np.array_equal(y, oracle.rms_fwd(x + r, g, 1e-6)[0])
