@@ -90,7 +90,8 @@ def ncu_traffic(workload: str):
 def kernel_name(w, plan) -> str:
     kind = "group" if plan["mapping"] == 0 else "cta"
     t = "float" if w.dtype == "f32" else "__nv_bfloat16"
-    return f"norm_fwd_{kind}<{t},{plan['vec_elems']},{plan['per_thread']},{'LN' if w.op == 'ln' else 'RMS'}>"
+    op = ("ADD+" if w.add else "") + ("LN" if w.op == "ln" else "RMS")
+    return f"norm_fwd_{kind}<{t},{plan['vec_elems']},{plan['per_thread']},{op}>"
 
 
 class ClockSampler:
@@ -163,16 +164,29 @@ def make_sets(w, inp, n_sets, device):
     sets = []
     for _ in range(n_sets):
         s = {"x": inp["x"].to(device), "y": torch.empty(w.M, w.N, dtype=w.torch_dtype, device=device)}
+        if w.add:
+            s["r"] = inp["r"].to(device)
+            s["h"] = torch.empty(w.M, w.N, dtype=w.torch_dtype, device=device)
         if w.op == "ln":
             s["mean"] = torch.empty(w.M, dtype=torch.float32, device=device)
             s["rstd"] = torch.empty(w.M, dtype=torch.float32, device=device)
         sets.append(s)
-    params = {k: v.to(device) for k, v in inp.items() if k != "x"}
+    params = {k: v.to(device) for k, v in inp.items() if k not in ("x", "r")}
     return sets, params
 
 
 def step_fn(w, rn, params):
-    if w.op == "ln":
+    if w.add and w.op == "ln":
+        g, b = params["gamma"], params["beta"]
+
+        def f(s):
+            rn.ln_fwd_add(s["x"], s["r"], g, b, w.eps, h_out=s["h"], out=s["y"], mean=s["mean"], rstd=s["rstd"])
+    elif w.add:
+        wt = params["w"]
+
+        def f(s):
+            rn.rms_fwd_add(s["x"], s["r"], wt, w.eps, h_out=s["h"], out=s["y"])
+    elif w.op == "ln":
         g, b = params["gamma"], params["beta"]
 
         def f(s):
@@ -186,19 +200,25 @@ def step_fn(w, rn, params):
 
 
 def time_same_bytes_copy(w, inp, device, steps=600, per_graph=60):
-    """Device time of torch's copy of x into y (read M*N, write M*N: the
-    algorithmic bytes minus parameters and statistics), graph-replayed over
-    the same rotating sets: what a plain copy of this size achieves."""
+    """Device time of torch's copy of one buffer into another, each as large
+    as the call's [M, N] inputs (x, or x and r): the algorithmic bytes minus
+    parameters and statistics, graph-replayed over rotating sets larger than
+    L2: what a plain copy of this size achieves."""
     import torch
-    sets, _ = make_sets(w, inp, n_sets_for(w), device)
-    for s in sets[:3]:
-        s["y"].copy_(s["x"])
+    n = w.M * w.N * (w.row_tensors // 2)
+    sets = [(torch.empty(n, dtype=w.torch_dtype, device=device), torch.empty(n, dtype=w.torch_dtype, device=device))
+            for _ in range(n_sets_for(w))]
+    for src, _ in sets:
+        src.fill_(1.0)
+    for src, dst in sets[:3]:
+        dst.copy_(src)
     side = torch.cuda.Stream(device)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(side):
         with torch.cuda.graph(g, stream=side):
             for i in range(per_graph):
-                sets[i % len(sets)]["y"].copy_(sets[i % len(sets)]["x"])
+                src, dst = sets[i % len(sets)]
+                dst.copy_(src)
     g.replay()
     torch.cuda.synchronize(device)
     t0 = torch.cuda.Event(enable_timing=True)
@@ -215,7 +235,7 @@ def time_same_bytes_copy(w, inp, device, steps=600, per_graph=60):
 
 
 def n_sets_for(w):
-    per_set = 2 * w.M * w.N * w.elem_size
+    per_set = w.row_tensors * w.M * w.N * w.elem_size
     return max(3, math.ceil(3 * L2_BYTES / per_set))
 
 
@@ -282,34 +302,41 @@ class _Null:
 
 
 def time_e2e(w, rn, inp, device, steps):
-    """Host buffers in, host buffers out: H2D of x and the parameters, the
-    call, D2H of y (and the statistics), every step, on one stream."""
+    """Host buffers in, host buffers out: H2D of x (and r) and the
+    parameters, the call, D2H of y (and h, and the statistics), every step,
+    on one stream."""
     import torch
-    hx = inp["x"].pin_memory()
-    hp = {k: v.pin_memory() for k, v in inp.items() if k != "x"}
-    dx = torch.empty_like(hx, device=device)
-    dp = {k: torch.empty_like(v, device=device) for k, v in hp.items()}
-    dy = torch.empty_like(dx)
-    hy = torch.empty_like(hx).pin_memory()
+    hin = {k: v.pin_memory() for k, v in inp.items()}
+    din = {k: torch.empty_like(v, device=device) for k, v in hin.items()}
+    dy = torch.empty_like(din["x"])
+    hy = torch.empty_like(hin["x"]).pin_memory()
+    dh = torch.empty_like(dy) if w.add else None
+    hh = torch.empty_like(hy).pin_memory() if w.add else None
     ln = w.op == "ln"
     if ln:
         dm = torch.empty(w.M, dtype=torch.float32, device=device)
         dr = torch.empty_like(dm)
         hm = torch.empty(w.M, dtype=torch.float32).pin_memory()
         hr = torch.empty_like(hm).pin_memory()
-    h2d = hx.numel() * hx.element_size() + sum(v.numel() * v.element_size() for v in hp.values())
-    d2h = hy.numel() * hy.element_size() + (8 * w.M if ln else 0)
+    h2d = sum(v.numel() * v.element_size() for v in hin.values())
+    d2h = hy.numel() * hy.element_size() * (2 if w.add else 1) + (8 * w.M if ln else 0)
 
     def one():
-        dx.copy_(hx, non_blocking=True)
-        for k in hp:
-            dp[k].copy_(hp[k], non_blocking=True)
+        for k in hin:
+            din[k].copy_(hin[k], non_blocking=True)
+        if ln and w.add:
+            rn.ln_fwd_add(din["x"], din["r"], din["gamma"], din["beta"], w.eps, h_out=dh, out=dy, mean=dm, rstd=dr)
+        elif ln:
+            rn.ln_fwd(din["x"], din["gamma"], din["beta"], w.eps, out=dy, mean=dm, rstd=dr)
+        elif w.add:
+            rn.rms_fwd_add(din["x"], din["r"], din["w"], w.eps, h_out=dh, out=dy)
+        else:
+            rn.rms_fwd(din["x"], din["w"], w.eps, out=dy)
         if ln:
-            rn.ln_fwd(dx, dp["gamma"], dp["beta"], w.eps, out=dy, mean=dm, rstd=dr)
             hm.copy_(dm, non_blocking=True)
             hr.copy_(dr, non_blocking=True)
-        else:
-            rn.rms_fwd(dx, dp["w"], w.eps, out=dy)
+        if w.add:
+            hh.copy_(dh, non_blocking=True)
         hy.copy_(dy, non_blocking=True)
 
     for _ in range(3):
@@ -340,6 +367,12 @@ def oracle_rows(w, inp, rows: int):
         return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
 
     x = npx(inp["x"][:rows])
+    e = oracle.eps_as_f32(w.eps)
+    if w.add:
+        r = npx(inp["r"][:rows])
+        if w.op == "ln":
+            return lambda: oracle.ln_fwd_add(x, r, npx(inp["gamma"]), npx(inp["beta"]), e)
+        return lambda: oracle.rms_fwd_add(x, r, npx(inp["w"]), e)
     if w.op == "ln":
         return lambda: oracle.ln_fwd(x, npx(inp["gamma"]), npx(inp["beta"]), oracle.eps_as_f32(w.eps))
     return lambda: oracle.rms_fwd(x, npx(inp["w"]), oracle.eps_as_f32(w.eps))
@@ -415,8 +448,8 @@ def run_reference(args, w):
         "impl": "reference", "metric": "LN/RMSNorm fwd achieved HBM GB/s", "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "op": w.op, "io_dtype": w.dtype, "eps": w.eps,
-                   "sample_rows_per_step": rows},
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "op": ("add+" if w.add else "") + w.op,
+                   "io_dtype": w.dtype, "eps": w.eps, "sample_rows_per_step": rows},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{rows} of {w.M} rows per step, fp64, 1 thread"},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -474,10 +507,10 @@ def main():
                            "frac_of_measured_peak": round(gbs / peak, 4),
                            "same_size_copy_us": round(copy_us, 3),
                            # achieved GB/s over the same-size copy's GB/s
-                           "frac_of_same_size_copy": round(gbs / ((2 * wk.M * wk.N * wk.elem_size) / (copy_us / 1e6) / 1e9),
-                                                           4),
+                           "frac_of_same_size_copy": round(
+                               gbs / ((wk.row_tensors * wk.M * wk.N * wk.elem_size) / (copy_us / 1e6) / 1e9), 4),
                            "rows_per_s": round(wk.M / (us / 1e6)), "plan": rn.make_plan(
-                               wk.M, wk.N, wk.torch_dtype, True, props.multi_processor_count)}
+                               wk.M, wk.N, wk.torch_dtype, True, props.multi_processor_count, add=wk.add)}
             del wi
 
     if world > 1:
@@ -494,14 +527,17 @@ def main():
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "us_per_call": round(kern_ms * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": w.name, "op": w.op, "M": w.M, "N": w.N, "io_dtype": w.dtype, "eps": w.eps,
+        "config": {"workload": w.name, "op": ("add+" if w.add else "") + w.op, "M": w.M, "N": w.N,
+                   "io_dtype": w.dtype, "eps": w.eps,
                    "algorithmic_bytes_per_call": bytes_per_call,
-                   "l2": f"{n_sets_for(w)} rotating input/output sets of {2 * w.M * w.N * w.elem_size >> 20} MiB "
+                   "l2": f"{n_sets_for(w)} rotating input/output sets of "
+                         f"{w.row_tensors * w.M * w.N * w.elem_size >> 20} MiB "
                          f"(> L2 between reuses)",
                    "parallelism": f"replicas x{world} (rows independent)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": traffic,
-                     "kernel": kernel_name(w, rn.make_plan(w.M, w.N, w.torch_dtype, True, props.multi_processor_count)),
+                     "kernel": kernel_name(w, rn.make_plan(w.M, w.N, w.torch_dtype, True, props.multi_processor_count,
+                                                           add=w.add)),
                      "kernel_hash": kernel_source_hash()},
         "e2e": {"value": round(bytes_per_call / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},

@@ -7,7 +7,8 @@
  *          §7.6 fused kernel structure (per-row statistics, mean/rstd saved).
  *   [RMS2] "CUDA算子优化(2)：RMSNorm": §1 formula, §2 [B*T, C] layout.
  *   [T3]   "T3 讲解：LayerNorm / RMSNorm 的 forward": §② masking, biased
- *          variance, fp32 statistics; §④ host reshape to [M, N].
+ *          variance, fp32 statistics; §④ host reshape to [M, N]; §⑤ fusion
+ *          with the residual add.
  *
  * Conventions shared by every entry point:
  *   - All pointers are DEVICE pointers on the current CUDA device, owned by
@@ -132,6 +133,47 @@ norm_status ln_fwd_planned(const void* x, const void* gamma, const void* beta, v
 norm_status rms_fwd_planned(const void* x, const void* w, void* y, int64_t M, int64_t N,
                             float eps, norm_dtype dtype, cudaStream_t stream,
                             const norm_plan* plan);
+
+/*
+ * Fused residual add + LayerNorm ([Ch7] §7.9-7.10, the add + norm of a
+ * transformer's residual stream; [T3] §⑤):
+ *   h_ri = x_ri + residual_ri, rounded to `dtype` (exactly what a separate
+ *          add kernel would store)
+ *   y, mean, rstd = ln_fwd of h
+ * Reads x and residual once and writes h and y. residual and h are [M, N]
+ * with the layout of x. h may be x or residual itself, and so may y (the
+ * usual in-place residual update); h and y must be different buffers
+ * (NORM_ERR_ARG otherwise). Any other overlap is undefined.
+ */
+norm_status ln_fwd_add(const void* x, const void* residual, const void* gamma,
+                       const void* beta, void* h, void* y, float* mean, float* rstd,
+                       int64_t M, int64_t N, float eps, norm_dtype dtype,
+                       cudaStream_t stream);
+
+/* Fused residual add + RMSNorm: h as for ln_fwd_add, y = rms_fwd of h. */
+norm_status rms_fwd_add(const void* x, const void* residual, const void* w, void* h,
+                        void* y, int64_t M, int64_t N, float eps, norm_dtype dtype,
+                        cudaStream_t stream);
+
+/* The plan ln_fwd_add / rms_fwd_add would choose: as norm_make_plan, with
+ * CTAs of at most 512 threads (the fused kernels keep two rows' worth of
+ * loads in flight and need the registers). `aligned16` covers all six
+ * pointers. Host only. */
+norm_status norm_make_plan_add(int64_t M, int64_t N, norm_dtype dtype, int aligned16,
+                               int num_sms, norm_plan* plan);
+
+/* The fused calls with an explicit plan, checked as for ln_fwd_planned;
+ * plans with `stages` != 0 or more than 512 threads return NORM_ERR_PLAN. */
+norm_status ln_fwd_add_planned(const void* x, const void* residual, const void* gamma,
+                               const void* beta, void* h, void* y, float* mean,
+                               float* rstd, int64_t M, int64_t N, float eps,
+                               norm_dtype dtype, cudaStream_t stream,
+                               const norm_plan* plan);
+
+norm_status rms_fwd_add_planned(const void* x, const void* residual, const void* w,
+                                void* h, void* y, int64_t M, int64_t N, float eps,
+                                norm_dtype dtype, cudaStream_t stream,
+                                const norm_plan* plan);
 
 /* Static description of a status code. */
 const char* norm_status_string(norm_status status);

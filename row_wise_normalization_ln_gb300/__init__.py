@@ -17,7 +17,7 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "ln_fwd", "rms_fwd", "make_plan", "NormPlan", "NormError", "LibraryNotBuilt", "library",
+    "ln_fwd", "rms_fwd", "ln_fwd_add", "rms_fwd_add", "make_plan", "NormPlan", "NormError", "LibraryNotBuilt", "library",
     "NORM_F32", "NORM_BF16", "NORM_MAP_GROUP", "NORM_MAP_CTA",
 ]
 
@@ -84,8 +84,14 @@ def library() -> ctypes.CDLL:
     L.rms_fwd.argtypes = [vp, vp, vp, i64, i64, f32, i32, vp]
     L.ln_fwd_planned.argtypes = L.ln_fwd.argtypes + [ctypes.POINTER(NormPlan)]
     L.rms_fwd_planned.argtypes = L.rms_fwd.argtypes + [ctypes.POINTER(NormPlan)]
+    L.ln_fwd_add.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, f32, i32, vp]
+    L.rms_fwd_add.argtypes = [vp, vp, vp, vp, vp, i64, i64, f32, i32, vp]
+    L.ln_fwd_add_planned.argtypes = L.ln_fwd_add.argtypes + [ctypes.POINTER(NormPlan)]
+    L.rms_fwd_add_planned.argtypes = L.rms_fwd_add.argtypes + [ctypes.POINTER(NormPlan)]
     L.norm_make_plan.argtypes = [i64, i64, i32, i32, i32, ctypes.POINTER(NormPlan)]
-    for f in ("ln_fwd", "rms_fwd", "ln_fwd_planned", "rms_fwd_planned", "norm_make_plan",
+    L.norm_make_plan_add.argtypes = L.norm_make_plan.argtypes
+    for f in ("ln_fwd", "rms_fwd", "ln_fwd_planned", "rms_fwd_planned", "ln_fwd_add", "rms_fwd_add",
+              "ln_fwd_add_planned", "rms_fwd_add_planned", "norm_make_plan", "norm_make_plan_add",
               "norm_last_cuda_error", "norm_abi_version"):
         getattr(L, f).restype = ctypes.c_int
     L.norm_status_string.argtypes = [ctypes.c_int]
@@ -102,10 +108,13 @@ def _dtype_code(t: torch.dtype) -> int:
     raise TypeError(f"libnorm supports float32 and bfloat16, got {t}")
 
 
-def make_plan(M: int, N: int, dtype: torch.dtype, aligned: bool = True, num_sms: int = 152) -> dict:
-    """The launch plan the library would choose (host-only, no CUDA call)."""
+def make_plan(M: int, N: int, dtype: torch.dtype, aligned: bool = True, num_sms: int = 152,
+              add: bool = False) -> dict:
+    """The launch plan the library would choose (host-only, no CUDA call);
+    ``add`` for the fused residual-add calls."""
     p = NormPlan()
-    st = library().norm_make_plan(M, N, _dtype_code(dtype), int(aligned), num_sms, ctypes.byref(p))
+    fn = library().norm_make_plan_add if add else library().norm_make_plan
+    st = fn(M, N, _dtype_code(dtype), int(aligned), num_sms, ctypes.byref(p))
     if st != NORM_OK:
         raise NormError(st, "norm_make_plan")
     return p.as_dict()
@@ -124,6 +133,35 @@ def _param(p: torch.Tensor, x: torch.Tensor, name: str) -> torch.Tensor:
     if p.numel() != x.shape[-1]:
         raise ValueError(f"{name} must have {x.shape[-1]} elements, got {p.numel()}")
     return p.reshape(-1).contiguous()
+
+
+def _out(t: Optional[torch.Tensor], x: torch.Tensor, x2: torch.Tensor, name: str) -> torch.Tensor:
+    y = t if t is not None else torch.empty_like(x2)
+    if y.shape != x.shape and y.shape != x2.shape or not y.is_contiguous() or y.dtype != x.dtype \
+            or y.device != x.device:
+        raise ValueError(f"{name} must be a contiguous tensor of x's shape, dtype and device")
+    return y
+
+
+def _residual(r: torch.Tensor, x: torch.Tensor) -> torch.Tensor:
+    if r.shape != x.shape or r.dtype != x.dtype or r.device != x.device:
+        raise ValueError("residual must have x's shape, dtype and device")
+    return _rows(r)
+
+
+def _stats(M: int, x: torch.Tensor, mean, rstd, stats: bool):
+    if not stats:
+        return None, None
+    mean = mean if mean is not None else torch.empty(M, device=x.device, dtype=torch.float32)
+    rstd = rstd if rstd is not None else torch.empty(M, device=x.device, dtype=torch.float32)
+    for t, n in ((mean, "mean"), (rstd, "rstd")):
+        if t.dtype != torch.float32 or t.numel() != M or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous fp32 tensor of {M} elements")
+    return mean, rstd
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return t.data_ptr() if t is not None else None
 
 
 def _stream_handle(stream: Optional[torch.cuda.Stream], device: torch.device) -> int:
@@ -153,21 +191,10 @@ def ln_fwd(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float 
     M, N = x2.shape
     g = _param(gamma, x, "gamma")
     b = _param(beta, x, "beta")
-    y = out if out is not None else torch.empty_like(x2)
-    if y.shape != x.shape and y.shape != x2.shape or not y.is_contiguous() or y.dtype != x.dtype:
-        raise ValueError("out must be a contiguous tensor of x's shape and dtype")
-    if stats:
-        mean = mean if mean is not None else torch.empty(M, device=x.device, dtype=torch.float32)
-        rstd = rstd if rstd is not None else torch.empty(M, device=x.device, dtype=torch.float32)
-        for t, n in ((mean, "mean"), (rstd, "rstd")):
-            if t.dtype != torch.float32 or t.numel() != M or not t.is_contiguous():
-                raise ValueError(f"{n} must be a contiguous fp32 tensor of {M} elements")
-    else:
-        mean = rstd = None
+    y = _out(out, x, x2, "out")
+    mean, rstd = _stats(M, x, mean, rstd, stats)
     L = library()
-    args = (x2.data_ptr(), g.data_ptr(), b.data_ptr(), y.data_ptr(),
-            mean.data_ptr() if mean is not None else None,
-            rstd.data_ptr() if rstd is not None else None,
+    args = (x2.data_ptr(), g.data_ptr(), b.data_ptr(), y.data_ptr(), _ptr(mean), _ptr(rstd),
             M, N, float(eps), code)
     with torch.cuda.device(x.device):
         h = _stream_handle(stream, x.device)
@@ -186,9 +213,7 @@ def rms_fwd(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6, *, out: Optiona
     x2 = _rows(x)
     M, N = x2.shape
     wv = _param(w, x, "w")
-    y = out if out is not None else torch.empty_like(x2)
-    if y.shape != x.shape and y.shape != x2.shape or not y.is_contiguous() or y.dtype != x.dtype:
-        raise ValueError("out must be a contiguous tensor of x's shape and dtype")
+    y = _out(out, x, x2, "out")
     L = library()
     args = (x2.data_ptr(), wv.data_ptr(), y.data_ptr(), M, N, float(eps), code)
     with torch.cuda.device(x.device):
@@ -197,3 +222,57 @@ def rms_fwd(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6, *, out: Optiona
     if st != NORM_OK:
         raise NormError(st, "rms_fwd")
     return y.view(x.shape)
+
+
+def ln_fwd_add(x: torch.Tensor, residual: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor,
+               eps: float = 1e-5, *, h_out: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+               mean: Optional[torch.Tensor] = None, rstd: Optional[torch.Tensor] = None, stats: bool = True,
+               stream: Optional[torch.cuda.Stream] = None, plan=None):
+    """Fused residual add + LayerNorm: ``h = x + residual`` (rounded to x's
+    dtype), ``y = LayerNorm(h)``. Returns ``(h, y, mean, rstd)``. ``h_out``
+    may be ``residual`` or ``x`` (in-place residual update) and so may
+    ``out``; the two must differ."""
+    if not x.is_cuda:
+        raise ValueError("ln_fwd_add needs a CUDA tensor")
+    code = _dtype_code(x.dtype)
+    x2 = _rows(x)
+    r2 = _residual(residual, x)
+    M, N = x2.shape
+    g = _param(gamma, x, "gamma")
+    b = _param(beta, x, "beta")
+    hh = _out(h_out, x, x2, "h_out")
+    y = _out(out, x, x2, "out")
+    mean, rstd = _stats(M, x, mean, rstd, stats)
+    L = library()
+    args = (x2.data_ptr(), r2.data_ptr(), g.data_ptr(), b.data_ptr(), hh.data_ptr(), y.data_ptr(),
+            _ptr(mean), _ptr(rstd), M, N, float(eps), code)
+    with torch.cuda.device(x.device):
+        s = _stream_handle(stream, x.device)
+        st = (L.ln_fwd_add(*args, s) if plan is None else L.ln_fwd_add_planned(*args, s, _plan_ptr(plan)))
+    if st != NORM_OK:
+        raise NormError(st, "ln_fwd_add")
+    return hh.view(x.shape), y.view(x.shape), mean, rstd
+
+
+def rms_fwd_add(x: torch.Tensor, residual: torch.Tensor, w: torch.Tensor, eps: float = 1e-6, *,
+                h_out: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None, plan=None):
+    """Fused residual add + RMSNorm: ``h = x + residual``, ``y = RMSNorm(h)``.
+    Returns ``(h, y)``; aliasing as for ``ln_fwd_add``."""
+    if not x.is_cuda:
+        raise ValueError("rms_fwd_add needs a CUDA tensor")
+    code = _dtype_code(x.dtype)
+    x2 = _rows(x)
+    r2 = _residual(residual, x)
+    M, N = x2.shape
+    wv = _param(w, x, "w")
+    hh = _out(h_out, x, x2, "h_out")
+    y = _out(out, x, x2, "out")
+    L = library()
+    args = (x2.data_ptr(), r2.data_ptr(), wv.data_ptr(), hh.data_ptr(), y.data_ptr(), M, N, float(eps), code)
+    with torch.cuda.device(x.device):
+        s = _stream_handle(stream, x.device)
+        st = (L.rms_fwd_add(*args, s) if plan is None else L.rms_fwd_add_planned(*args, s, _plan_ptr(plan)))
+    if st != NORM_OK:
+        raise NormError(st, "rms_fwd_add")
+    return hh.view(x.shape), y.view(x.shape)

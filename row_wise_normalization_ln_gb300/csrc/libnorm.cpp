@@ -61,8 +61,10 @@ int vec_for(int64_t N, norm_dtype dtype, bool all_aligned) {
 // than 256 such threads go to a cluster of up to 8 CTAs of 128 threads, each
 // walking its share in two rounds; lane groups only pay off below 64
 // accesses per row.
-norm_status make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_aligned, int num_sms, norm_plan* p) {
+norm_status make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_aligned, int num_sms, bool add,
+                      norm_plan* p) {
     std::memset(p, 0, sizeof *p);
+    const int max_threads = add ? libnorm::kFusedMaxThreads : kMaxThreads;
     const int vec = vec_for(N, dtype, all_aligned);
     const int64_t nacc = ceil_div(N, vec);
     const int64_t busy_threads = int64_t(num_sms) * 1024;  // half of the resident-thread capacity
@@ -102,7 +104,7 @@ norm_status make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_aligned, 
     // Few rows: trade registers per thread for more threads per row.
     while (per > 1 && M * cluster * threads < busy_threads) {
         const int64_t t2 = round_up(ceil_div(nacc, cluster * (per / 2)), 32);
-        if (t2 > kMaxThreads) break;
+        if (t2 > max_threads) break;
         per /= 2;
         threads = t2;
     }
@@ -117,9 +119,12 @@ norm_status make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_aligned, 
     return NORM_OK;
 }
 
-// Validate an explicit plan against the call; derive `rounds`.
-norm_status check_plan(const norm_plan& in, int64_t N, norm_dtype dtype, bool all_aligned, norm_plan* out) {
+// Validate an explicit plan against the call; derive `rounds`. The fused
+// residual add (`add`) has no ring kernel and smaller CTAs.
+norm_status check_plan(const norm_plan& in, int64_t N, norm_dtype dtype, bool all_aligned, bool add,
+                       norm_plan* out) {
     norm_plan p = in;
+    if (add && (p.stages != 0 || p.threads > libnorm::kFusedMaxThreads)) return NORM_ERR_PLAN;
     const int s = elem_size(dtype);
     if (p.mapping != NORM_MAP_GROUP && p.mapping != NORM_MAP_CTA) return NORM_ERR_PLAN;
     if (p.vec_elems != 1) {
@@ -180,24 +185,33 @@ int device_sm_count(int* dev_out) {
 
 using Launcher = cudaError_t (*)(const norm_plan&, const NormArgs&, cudaStream_t, int, int);
 
+Launcher pick_launcher(bool ln, bool add, norm_dtype dtype) {
+    const bool f32 = dtype == NORM_F32;
+    if (add)
+        return ln ? (f32 ? libnorm::launch_ln_add_f32 : libnorm::launch_ln_add_bf16)
+                  : (f32 ? libnorm::launch_rms_add_f32 : libnorm::launch_rms_add_bf16);
+    return ln ? (f32 ? libnorm::launch_ln_f32 : libnorm::launch_ln_bf16)
+              : (f32 ? libnorm::launch_rms_f32 : libnorm::launch_rms_bf16);
+}
+
+// a.res != null selects the fused residual add.
 norm_status run(bool ln, const NormArgs& a, norm_dtype dtype, bool all_aligned, cudaStream_t stream,
                 const norm_plan* user_plan) {
+    const bool add = a.res != nullptr;
     norm_plan plan;
     if (user_plan) {
-        const norm_status st = check_plan(*user_plan, a.N, dtype, all_aligned, &plan);
+        const norm_status st = check_plan(*user_plan, a.N, dtype, all_aligned, add, &plan);
         if (st != NORM_OK) return st;
     }
     int dev = 0;
     const int sms = device_sm_count(&dev);
     if (sms <= 0) return NORM_ERR_CUDA;
-    if (!user_plan) make_plan(a.M, a.N, dtype, all_aligned, sms, &plan);
+    if (!user_plan) make_plan(a.M, a.N, dtype, all_aligned, sms, add, &plan);
     NormArgs args = a;
     args.group = plan.group;
     args.rounds = plan.rounds;
     args.stages = plan.stages;
-    Launcher launch = ln ? (dtype == NORM_F32 ? libnorm::launch_ln_f32 : libnorm::launch_ln_bf16)
-                         : (dtype == NORM_F32 ? libnorm::launch_rms_f32 : libnorm::launch_rms_bf16);
-    const cudaError_t e = launch(plan, args, stream, sms, dev);
+    const cudaError_t e = pick_launcher(ln, add, dtype)(plan, args, stream, sms, dev);
     if (e != cudaSuccess) {
         g_last_cuda_error = static_cast<int>(e);
         return NORM_ERR_CUDA;
@@ -213,7 +227,7 @@ norm_status ln_impl(const void* x, const void* gamma, const void* beta, void* y,
     if (M == 0) return NORM_OK;
     if (!x || !gamma || !beta || !y) return NORM_ERR_ARG;
     const bool al = aligned16(x) && aligned16(y) && aligned16(gamma) && aligned16(beta);
-    NormArgs a{x, gamma, beta, y, mean, rstd, M, static_cast<int32_t>(N), eps, 0, 1, 0};
+    NormArgs a{x, gamma, beta, y, mean, rstd, nullptr, nullptr, M, static_cast<int32_t>(N), eps, 0, 1, 0};
     return run(true, a, dtype, al, stream, plan);
 }
 
@@ -225,7 +239,35 @@ norm_status rms_impl(const void* x, const void* w, void* y, int64_t M, int64_t N
     if (M == 0) return NORM_OK;
     if (!x || !w || !y) return NORM_ERR_ARG;
     const bool al = aligned16(x) && aligned16(y) && aligned16(w);
-    NormArgs a{x, w, nullptr, y, nullptr, nullptr, M, static_cast<int32_t>(N), eps, 0, 1, 0};
+    NormArgs a{x, w, nullptr, y, nullptr, nullptr, nullptr, nullptr, M, static_cast<int32_t>(N), eps, 0, 1, 0};
+    return run(false, a, dtype, al, stream, plan);
+}
+
+// Fused residual add: h and y are both written, so they may not be the same
+// buffer; each may be x or the residual itself.
+norm_status ln_add_impl(const void* x, const void* res, const void* gamma, const void* beta, void* h, void* y,
+                        float* mean, float* rstd, int64_t M, int64_t N, float eps, norm_dtype dtype,
+                        cudaStream_t stream, const norm_plan* plan) {
+    norm_status st = check_sizes(M, N, dtype);
+    if (st != NORM_OK) return st;
+    if (!std::isfinite(eps) || eps < 0.f) return NORM_ERR_ARG;
+    if (M == 0) return NORM_OK;
+    if (!x || !res || !gamma || !beta || !h || !y || h == y) return NORM_ERR_ARG;
+    const bool al = aligned16(x) && aligned16(res) && aligned16(h) && aligned16(y) && aligned16(gamma) &&
+                    aligned16(beta);
+    NormArgs a{x, gamma, beta, y, mean, rstd, res, h, M, static_cast<int32_t>(N), eps, 0, 1, 0};
+    return run(true, a, dtype, al, stream, plan);
+}
+
+norm_status rms_add_impl(const void* x, const void* res, const void* w, void* h, void* y, int64_t M, int64_t N,
+                         float eps, norm_dtype dtype, cudaStream_t stream, const norm_plan* plan) {
+    norm_status st = check_sizes(M, N, dtype);
+    if (st != NORM_OK) return st;
+    if (!std::isfinite(eps) || eps < 0.f) return NORM_ERR_ARG;
+    if (M == 0) return NORM_OK;
+    if (!x || !res || !w || !h || !y || h == y) return NORM_ERR_ARG;
+    const bool al = aligned16(x) && aligned16(res) && aligned16(h) && aligned16(y) && aligned16(w);
+    NormArgs a{x, w, nullptr, y, nullptr, nullptr, res, h, M, static_cast<int32_t>(N), eps, 0, 1, 0};
     return run(false, a, dtype, al, stream, plan);
 }
 
@@ -254,11 +296,41 @@ norm_status rms_fwd_planned(const void* x, const void* w, void* y, int64_t M, in
     return rms_impl(x, w, y, M, N, eps, dtype, stream, plan);
 }
 
+norm_status ln_fwd_add(const void* x, const void* residual, const void* gamma, const void* beta, void* h, void* y,
+                       float* mean, float* rstd, int64_t M, int64_t N, float eps, norm_dtype dtype,
+                       cudaStream_t stream) {
+    return ln_add_impl(x, residual, gamma, beta, h, y, mean, rstd, M, N, eps, dtype, stream, nullptr);
+}
+
+norm_status rms_fwd_add(const void* x, const void* residual, const void* w, void* h, void* y, int64_t M, int64_t N,
+                        float eps, norm_dtype dtype, cudaStream_t stream) {
+    return rms_add_impl(x, residual, w, h, y, M, N, eps, dtype, stream, nullptr);
+}
+
+norm_status ln_fwd_add_planned(const void* x, const void* residual, const void* gamma, const void* beta, void* h,
+                               void* y, float* mean, float* rstd, int64_t M, int64_t N, float eps,
+                               norm_dtype dtype, cudaStream_t stream, const norm_plan* plan) {
+    return ln_add_impl(x, residual, gamma, beta, h, y, mean, rstd, M, N, eps, dtype, stream, plan);
+}
+
+norm_status rms_fwd_add_planned(const void* x, const void* residual, const void* w, void* h, void* y, int64_t M,
+                                int64_t N, float eps, norm_dtype dtype, cudaStream_t stream,
+                                const norm_plan* plan) {
+    return rms_add_impl(x, residual, w, h, y, M, N, eps, dtype, stream, plan);
+}
+
 norm_status norm_make_plan(int64_t M, int64_t N, norm_dtype dtype, int aligned, int num_sms, norm_plan* plan) {
     const norm_status st = check_sizes(M, N, dtype);
     if (st != NORM_OK) return st;
     if (!plan || num_sms < 1) return NORM_ERR_ARG;
-    return make_plan(M, N, dtype, aligned != 0, num_sms, plan);
+    return make_plan(M, N, dtype, aligned != 0, num_sms, false, plan);
+}
+
+norm_status norm_make_plan_add(int64_t M, int64_t N, norm_dtype dtype, int aligned, int num_sms, norm_plan* plan) {
+    const norm_status st = check_sizes(M, N, dtype);
+    if (st != NORM_OK) return st;
+    if (!plan || num_sms < 1) return NORM_ERR_ARG;
+    return make_plan(M, N, dtype, aligned != 0, num_sms, true, plan);
 }
 
 const char* norm_status_string(norm_status s) {

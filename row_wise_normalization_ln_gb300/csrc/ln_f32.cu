@@ -5,7 +5,7 @@
 namespace libnorm {
 
 cudaError_t launch_ln_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev) {
-    return launch_norm<float, true>(plan, a, s, num_sms, dev);
+    return launch_norm<float, true, false>(plan, a, s, num_sms, dev);
 }
 
 }  // namespace libnorm

@@ -9,6 +9,11 @@
 
 namespace libnorm {
 
+// CTA size limit of the fused residual-add kernels: x and the residual are in
+// flight together, which needs more than the 64 registers a 1024-thread CTA
+// leaves each thread.
+constexpr int kFusedMaxThreads = 512;
+
 struct NormArgs {
     const void* x;      // [M, N]
     const void* gamma;  // [N] (LayerNorm gamma, RMSNorm w)
@@ -16,6 +21,8 @@ struct NormArgs {
     void* y;            // [M, N]
     float* mean;        // [M] or null (LayerNorm only)
     float* rstd;        // [M] or null (LayerNorm only)
+    const void* res;    // [M, N] residual (fused residual add only)
+    void* h;            // [M, N] h = x + res (fused residual add only)
     int64_t M;
     int32_t N;
     float eps;
@@ -31,5 +38,10 @@ cudaError_t launch_ln_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t
 cudaError_t launch_ln_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
 cudaError_t launch_rms_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
 cudaError_t launch_rms_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+// The same with the fused residual add (a.res, a.h set).
+cudaError_t launch_ln_add_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_ln_add_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_rms_add_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_rms_add_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
 
 }  // namespace libnorm

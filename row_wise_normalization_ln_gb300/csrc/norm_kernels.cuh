@@ -114,6 +114,11 @@ struct Ops<float, 4> {
         return make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
                           __float_as_uint(o[3]));
     }
+    // Residual add h = x + r, each element rounded once to fp32.
+    static __device__ __forceinline__ Raw add_round(const Raw& x, const Raw& r) {
+        return make_uint4(__float_as_uint(e(x, 0) + e(r, 0)), __float_as_uint(e(x, 1) + e(r, 1)),
+                          __float_as_uint(e(x, 2) + e(r, 2)), __float_as_uint(e(x, 3) + e(r, 3)));
+    }
     static __device__ __forceinline__ Raw load(const float* p) { return *reinterpret_cast<const uint4*>(p); }
     static __device__ __forceinline__ Raw load_param(const float* p) {
         return __ldg(reinterpret_cast<const uint4*>(p));
@@ -175,6 +180,18 @@ struct Ops<__nv_bfloat16, 8> {
         }
         return make_uint4(o[0], o[1], o[2], o[3]);
     }
+    // Residual add h = x + r: the exact sum of two bf16 values needs at most
+    // 18 bits of the fp32 sum's 24, so rounding that sum to bf16 rounds the
+    // exact sum once.
+    static __device__ __forceinline__ Raw add_round(const Raw& x, const Raw& r) {
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 h = __fadd2_rn(bf16x2_widen(w(x, i)), bf16x2_widen(w(r, i)));
+            o[i] = pack_bf16x2(h.x, h.y);
+        }
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    }
     static __device__ __forceinline__ Raw load(const __nv_bfloat16* p) { return *reinterpret_cast<const uint4*>(p); }
     static __device__ __forceinline__ Raw load_param(const __nv_bfloat16* p) {
         return __ldg(reinterpret_cast<const uint4*>(p));
@@ -204,6 +221,7 @@ struct ScalarOps {
         return from_float(fmaf(fmaf(e(r) - K, rs, nmr), e(g), e(b)));
     }
     static __device__ __forceinline__ Raw rms_out(Raw r, float rs, Raw wt) { return from_float((e(r) * e(wt)) * rs); }
+    static __device__ __forceinline__ Raw add_round(Raw x, Raw r) { return from_float(e(x) + e(r)); }
     static __device__ __forceinline__ Raw from_float(float v) {
         if constexpr (sizeof(T) == 4)
             return __float_as_uint(v);
@@ -233,10 +251,16 @@ struct ScalarOps {
 template <class T, int VEC>
 using OpsFor = typename std::conditional<VEC == 1, ScalarOps<T>, Ops<T, VEC>>::type;
 
-// The row's first element, the shift K of LayerNorm.
+// The row's first element, the shift K of LayerNorm; with a residual, the
+// first element of h = x + r (rounded as the stored h is).
 template <class T>
 __device__ __forceinline__ float first_elem(const T* row) {
     return ScalarOps<T>::e(ScalarOps<T>::load(row));
+}
+template <class T>
+__device__ __forceinline__ float first_elem_add(const T* xrow, const T* rrow) {
+    using SO = ScalarOps<T>;
+    return SO::e(SO::add_round(SO::load(xrow), SO::load(rrow)));
 }
 
 // ================================================================== a thread's slice
@@ -256,6 +280,19 @@ struct Slice {
 #pragma unroll
         for (int j = 0; j < V; ++j)
             if (j < nvalid) raw[j] = O::load(p + j * stride);
+    }
+    // Fused residual add: hold h = x + r (rounded to T). h is stored later,
+    // by store_h, once every thread of the row has read its inputs (h may be
+    // the x or r buffer itself).
+    __device__ __forceinline__ void load_add(const T* px, const T* pr, int stride, int nvalid) {
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            if (j < nvalid) raw[j] = O::add_round(O::load(px + j * stride), O::load(pr + j * stride));
+    }
+    __device__ __forceinline__ void store_h(T* ph, int stride, int nvalid) const {
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            if (j < nvalid) O::store(ph + j * stride, raw[j]);
     }
     // Welford state of the valid elements, two passes over the registers:
     // the sum and mean of x - K, then M2 about that mean.
@@ -380,9 +417,9 @@ __device__ __forceinline__ void row_stats(RowReduceSmem& red, float n_t, float s
 // Lanes [k*G, (k+1)*G) of the CTA own row blockIdx*rows_per_cta + k. Lane l
 // of a group holds accesses l, l+G, l+2G, ... (the G lanes of a group read G
 // consecutive accesses per instruction). The statistics meet in xor
-// butterflies over the group.
-template <class T, int VEC, int V, bool LN>
-__global__ void __launch_bounds__(1024) norm_fwd_group(const NormArgs a) {
+// butterflies over the group. ADD as for norm_fwd_cta.
+template <class T, int VEC, int V, bool LN, bool ADD>
+__global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_group(const NormArgs a) {
     using S = Slice<T, VEC, V, LN>;
     const int G = a.group;
     const int tid = threadIdx.x;
@@ -404,10 +441,14 @@ __global__ void __launch_bounds__(1024) norm_fwd_group(const NormArgs a) {
         const bool row_ok = row < a.M;
         const int nv = row_ok ? nvalid : 0;
         const T* xr = static_cast<const T*>(a.x) + row * a.N;
+        const T* rr = ADD ? static_cast<const T*>(a.res) + row * a.N : nullptr;
         S s;
-        const float K = (LN && row_ok) ? first_elem(xr) : 0.f;
+        const float K = (LN && row_ok) ? (ADD ? first_elem_add(xr, rr) : first_elem(xr)) : 0.f;
         s.set_shift(K);
-        s.load(xr + gl * VEC, stride, nv);
+        if constexpr (ADD)
+            s.load_add(xr + gl * VEC, rr + gl * VEC, stride, nv);
+        else
+            s.load(xr + gl * VEC, stride, nv);
         float mu = 0.f, rs;
         if constexpr (LN) {
             float sum = 0.f, mean = 0.f, m2 = 0.f;
@@ -424,6 +465,7 @@ __global__ void __launch_bounds__(1024) norm_fwd_group(const NormArgs a) {
             rs = rsqrtf(group_sum(s.sumsq(nv), G) * invN + a.eps);
         }
         s.emit(g, b, static_cast<T*>(a.y) + row * a.N + gl * VEC, stride, nv, mu, rs);
+        if constexpr (ADD) s.store_h(static_cast<T*>(a.h) + row * a.N + gl * VEC, stride, nv);
     }
 }
 
@@ -436,9 +478,11 @@ __global__ void __launch_bounds__(1024) norm_fwd_group(const NormArgs a) {
 // folded into the thread's state with the pairwise merge); the output pass
 // then walks the rounds backwards, reusing the registers of the last round
 // and re-reading the others. CL: launched with clusters (C > 1); without,
-// every cluster step compiles away.
-template <class T, int VEC, int V, bool LN, bool CL>
-__global__ void __launch_bounds__(1024) norm_fwd_cta(const NormArgs a) {
+// every cluster step compiles away. ADD: fused residual add; the row is
+// h = x + r (rounded to T), written to a.h in the output pass, after the
+// row's barrier, so that h may be the x or r buffer itself.
+template <class T, int VEC, int V, bool LN, bool CL, bool ADD>
+__global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(const NormArgs a) {
     using S = Slice<T, VEC, V, LN>;
     __shared__ RowReduceSmem red;
 
@@ -463,16 +507,20 @@ __global__ void __launch_bounds__(1024) norm_fwd_cta(const NormArgs a) {
 
     for (int64_t row = first_row; row < a.M; row += row_step) {
         const T* xr = static_cast<const T*>(a.x) + row * a.N;
+        const T* rr = ADD ? static_cast<const T*>(a.res) + row * a.N : nullptr;
         T* yr = static_cast<T*>(a.y) + row * a.N;
         S s;
-        const float K = LN ? first_elem(xr) : 0.f;
+        const float K = LN ? (ADD ? first_elem_add(xr, rr) : first_elem(xr)) : 0.f;
         s.set_shift(K);
         float n_t = 0.f, sum_t = 0.f, mean_t = 0.f, m2_t = 0.f, ss_t = 0.f;
         int nv = 0;
         for (int r = 0; r < rounds; ++r) {
             const int f = (r * static_cast<int>(C) + rank) * V * T_ + in_slice;
             nv = valid_runs(nacc, f, 32, V);
-            s.load(xr + f * VEC, stride, nv);
+            if constexpr (ADD)
+                s.load_add(xr + f * VEC, rr + f * VEC, stride, nv);
+            else
+                s.load(xr + f * VEC, stride, nv);
             if constexpr (LN) {
                 const float n = static_cast<float>(nv * VEC);
                 float sum = 0.f, mean = 0.f, m2 = 0.f;
@@ -502,10 +550,14 @@ __global__ void __launch_bounds__(1024) norm_fwd_cta(const NormArgs a) {
             const int f = (r * static_cast<int>(C) + rank) * V * T_ + in_slice;
             if (r != rounds - 1) {
                 nv = valid_runs(nacc, f, 32, V);
-                s.load(xr + f * VEC, stride, nv);
+                if constexpr (ADD)
+                    s.load_add(xr + f * VEC, rr + f * VEC, stride, nv);  // x, r of this round are untouched
+                else
+                    s.load(xr + f * VEC, stride, nv);
             }
             s.emit(static_cast<const T*>(a.gamma) + f * VEC, static_cast<const T*>(a.beta) + f * VEC, yr + f * VEC,
                    stride, nv, mu, rs);
+            if constexpr (ADD) s.store_h(static_cast<T*>(a.h) + row * a.N + f * VEC, stride, nv);
         }
     }
     // No CTA may exit while a peer can still read its shared memory.
@@ -610,19 +662,19 @@ __global__ void __launch_bounds__(1024) norm_fwd_pipe(const NormArgs a) {
 template <class T, bool LN>
 using KernelFn = void (*)(const NormArgs);
 
-template <class T, bool LN, int VEC, int V>
+template <class T, bool LN, bool ADD, int VEC, int V>
 KernelFn<T, LN> pick_cta(bool cl) {
-    return cl ? norm_fwd_cta<T, VEC, V, LN, true> : norm_fwd_cta<T, VEC, V, LN, false>;
+    return cl ? norm_fwd_cta<T, VEC, V, LN, true, ADD> : norm_fwd_cta<T, VEC, V, LN, false, ADD>;
 }
 
-template <class T, bool LN, int VEC>
+template <class T, bool LN, bool ADD, int VEC>
 KernelFn<T, LN> pick_kernel(int mapping, int per_thread, bool cl) {
     const bool group = mapping == NORM_MAP_GROUP;
     switch (per_thread) {
-        case 1: return group ? norm_fwd_group<T, VEC, 1, LN> : pick_cta<T, LN, VEC, 1>(cl);
-        case 2: return group ? norm_fwd_group<T, VEC, 2, LN> : pick_cta<T, LN, VEC, 2>(cl);
-        case 4: return group ? norm_fwd_group<T, VEC, 4, LN> : pick_cta<T, LN, VEC, 4>(cl);
-        case 8: return group ? norm_fwd_group<T, VEC, 8, LN> : pick_cta<T, LN, VEC, 8>(cl);
+        case 1: return group ? norm_fwd_group<T, VEC, 1, LN, ADD> : pick_cta<T, LN, ADD, VEC, 1>(cl);
+        case 2: return group ? norm_fwd_group<T, VEC, 2, LN, ADD> : pick_cta<T, LN, ADD, VEC, 2>(cl);
+        case 4: return group ? norm_fwd_group<T, VEC, 4, LN, ADD> : pick_cta<T, LN, ADD, VEC, 4>(cl);
+        case 8: return group ? norm_fwd_group<T, VEC, 8, LN, ADD> : pick_cta<T, LN, ADD, VEC, 8>(cl);
         default: return nullptr;
     }
 }
@@ -683,20 +735,25 @@ cudaError_t allow_smem(int per_thread, bool cl, int dev) {
     }
 }
 
-template <class T, bool LN>
+// ADD: the fused residual add (register kernels only; no ring).
+template <class T, bool LN, bool ADD>
 cudaError_t launch_norm(const norm_plan& p, const NormArgs& a, cudaStream_t stream, int num_sms, int dev) {
     KernelFn<T, LN> k;
     size_t smem = 0;
     const bool cl = p.mapping == NORM_MAP_CTA && p.cluster > 1;
     if (p.stages > 0) {
-        k = pick_pipe<T, LN>(p.per_thread, cl);
-        if (k == nullptr) return cudaErrorInvalidValue;
-        smem = pipe_smem_bytes(p, LN);
-        const cudaError_t e = allow_smem<T, LN>(p.per_thread, cl, dev);
-        if (e != cudaSuccess) return e;
+        if constexpr (ADD) {
+            return cudaErrorInvalidValue;
+        } else {
+            k = pick_pipe<T, LN>(p.per_thread, cl);
+            if (k == nullptr) return cudaErrorInvalidValue;
+            smem = pipe_smem_bytes(p, LN);
+            const cudaError_t e = allow_smem<T, LN>(p.per_thread, cl, dev);
+            if (e != cudaSuccess) return e;
+        }
     } else {
-        k = p.vec_elems == 1 ? pick_kernel<T, LN, 1>(p.mapping, p.per_thread, cl)
-                             : pick_kernel<T, LN, ElemVec<T>::value>(p.mapping, p.per_thread, cl);
+        k = p.vec_elems == 1 ? pick_kernel<T, LN, ADD, 1>(p.mapping, p.per_thread, cl)
+                             : pick_kernel<T, LN, ADD, ElemVec<T>::value>(p.mapping, p.per_thread, cl);
         if (k == nullptr) return cudaErrorInvalidValue;
     }
     cudaLaunchConfig_t cfg = {};

@@ -18,6 +18,9 @@ Workloads (shapes and value distributions of the source pages):
                            post's V0/V2 sizes); x ~ U(-1,1), w ~ U(0,1), eps 1e-6.
   ln_f32_2048x65536        LayerNorm fp32 long rows; x ~ N(3,1).
   ln_f32_8192x5000         LayerNorm fp32, N not a power of two; x ~ N(3,1).
+  add_*                    the fused residual add + norm on the shape and
+                           recipe of the workload it names: the residual r is
+                           drawn from the same recipe, after the parameters.
 """
 from __future__ import annotations
 
@@ -35,6 +38,7 @@ class Workload:
     N: int
     eps: float
     recipe: str    # key of the value distribution below
+    add: bool = False  # fused residual add: h = x + r, y = norm(h)
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -44,17 +48,23 @@ class Workload:
     def elem_size(self) -> int:
         return 4 if self.dtype == "f32" else 2
 
+    @property
+    def row_tensors(self) -> int:
+        """[M, N] tensors one call moves: x, y; with the fused add also r, h."""
+        return 4 if self.add else 2
+
     def algorithmic_bytes(self, M: int | None = None) -> int:
-        """HBM bytes one forward call must move: read x, write y, read the
-        per-column parameters, write 8 B of statistics per row (LayerNorm)."""
+        """HBM bytes one forward call must move: read x (and r), write y (and
+        h), read the per-column parameters, write 8 B of statistics per row
+        (LayerNorm)."""
         M = self.M if M is None else M
         s = self.elem_size
         params = 2 if self.op == "ln" else 1
         stats = 8 * M if self.op == "ln" else 0
-        return 2 * M * self.N * s + params * self.N * s + stats
+        return self.row_tensors * M * self.N * s + params * self.N * s + stats
 
     def scaled(self, M: int | None = None, N: int | None = None) -> "Workload":
-        return Workload(self.name, self.op, self.dtype, M or self.M, N or self.N, self.eps, self.recipe)
+        return Workload(self.name, self.op, self.dtype, M or self.M, N or self.N, self.eps, self.recipe, self.add)
 
 
 WORKLOADS = {
@@ -66,39 +76,48 @@ WORKLOADS = {
         Workload("rms_bf16_65536x2048", "rms", "bf16", 65536, 2048, 1e-6, "uniform_pm1"),
         Workload("ln_f32_2048x65536", "ln", "f32", 2048, 65536, 1e-5, "normal31"),
         Workload("ln_f32_8192x5000", "ln", "f32", 8192, 5000, 1e-5, "normal31"),
+        Workload("add_rms_f32_8192x4096", "rms", "f32", 8192, 4096, 1e-6, "uniform_pm1", True),
+        Workload("add_rms_bf16_65536x2048", "rms", "bf16", 65536, 2048, 1e-6, "uniform_pm1", True),
+        Workload("add_ln_bf16_4096x8192_outliers", "ln", "bf16", 4096, 8192, 1e-5, "offset_outliers", True),
+        Workload("add_ln_f32_2048x65536", "ln", "f32", 2048, 65536, 1e-5, "normal31", True),
     ]
 }
 
 BENCH_WORKLOAD = "rms_f32_8192x4096"
 
 
-def generate(w: Workload, seed: int = 0) -> dict[str, torch.Tensor]:
-    """CPU tensors for one workload: {"x", "gamma", "beta"} (LayerNorm) or
-    {"x", "w"} (RMSNorm), all in the workload's dtype, drawn in a fixed order
-    from one seeded CPU generator."""
-    g = torch.Generator().manual_seed(seed)
-    M, N = w.M, w.N
-    if w.recipe == "normal01":
-        x = torch.randn(M, N, generator=g)
-    elif w.recipe == "normal31":
-        x = torch.randn(M, N, generator=g) + 3.0
-    elif w.recipe == "uniform_pm1":
-        x = torch.rand(M, N, generator=g) * 2.0 - 1.0
-    elif w.recipe == "offset_outliers":
+def _draw(recipe: str, M: int, N: int, g: torch.Generator) -> torch.Tensor:
+    if recipe == "normal01":
+        return torch.randn(M, N, generator=g)
+    if recipe == "normal31":
+        return torch.randn(M, N, generator=g) + 3.0
+    if recipe == "uniform_pm1":
+        return torch.rand(M, N, generator=g) * 2.0 - 1.0
+    if recipe == "offset_outliers":
         offset = torch.rand(M, 1, generator=g) * 900.0 + 100.0
         x = offset + torch.randn(M, N, generator=g) * 0.01
         n_out = max(1, round(0.01 * N))
         cols = torch.randperm(N, generator=g)[:n_out]
         signs = torch.where(torch.rand(n_out, generator=g) < 0.5, -1.0, 1.0)
         x[:, cols] = signs * 300.0
-    else:
-        raise KeyError(w.recipe)
-    out = {"x": x}
+        return x
+    raise KeyError(recipe)
+
+
+def generate(w: Workload, seed: int = 0) -> dict[str, torch.Tensor]:
+    """CPU tensors for one workload: {"x", "gamma", "beta"} (LayerNorm) or
+    {"x", "w"} (RMSNorm), plus "r" for the fused add, all in the workload's
+    dtype, drawn in a fixed order from one seeded CPU generator."""
+    g = torch.Generator().manual_seed(seed)
+    M, N = w.M, w.N
+    out = {"x": _draw(w.recipe, M, N, g)}
     if w.op == "ln":
         out["gamma"] = torch.rand(N, generator=g) + 0.5
         out["beta"] = torch.rand(N, generator=g) * 0.2 - 0.1
     else:
         out["w"] = torch.rand(N, generator=g)
+    if w.add:
+        out["r"] = _draw(w.recipe, M, N, g)
     return {k: v.to(w.torch_dtype).contiguous() for k, v in out.items()}
 
 

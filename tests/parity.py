@@ -12,6 +12,10 @@ budget of y = (x - mean) * rstd * gamma + beta:
     2^-21 * ((|mean| * rstd + max|x_hat|) * max|gamma| + max|beta|)
 (eight fp32 ulps of every term that enters y, including the rounding of the
 fp32 mean itself). For RMSNorm the floor is 2^-21 * max|x| * rstd * max|w|.
+
+Fused residual add: h = x + r must match the oracle's correctly rounded sum
+bit for bit (one IEEE addition in either dtype); y and the statistics are
+then held to the bars above against the oracle's norm of that h.
 """
 from __future__ import annotations
 
@@ -117,6 +121,46 @@ def check_rms(x, w, eps, y, rows=None) -> dict:
     y_ref, r_ref = oracle.rms_fwd(xn, wn, e)
     floor = rms_floor(as_f64(xn), as_f64(wn), r_ref) if yn.dtype == np.uint16 else None
     return check_y(yn, y_ref, floor)
+
+
+def torch_of(a: np.ndarray) -> torch.Tensor:
+    """Inverse of np_of: CPU tensor from float32 or raw bf16 (uint16) bits."""
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+
+
+def check_h(x, r, h, rows=None) -> torch.Tensor:
+    """h of the fused add against the oracle's rounded sum, bit for bit;
+    returns the oracle's h (CPU tensor, the selected rows)."""
+    xn, rn_, hn = np_of(x), np_of(r), np_of(h)
+    if rows is not None:
+        xn, rn_, hn = xn[rows], rn_[rows], hn[rows]
+    h_ref = oracle.add_round(xn, rn_)
+    bits = np.uint16 if h_ref.dtype == np.uint16 else np.uint32
+    bad = hn.view(bits) != h_ref.view(bits)
+    assert not bad.any(), f"{int(bad.sum())} elements of h differ from the rounded sum"
+    return torch_of(h_ref)
+
+
+def check_ln_add(x, r, gamma, beta, eps, h, y, mean=None, rstd=None, rows=None) -> dict:
+    h_ref = check_h(x, r, h, rows)
+    if rows is not None:
+        y = np_of(y)[rows]
+        mean = np_of(mean)[rows] if mean is not None else None
+        rstd = np_of(rstd)[rows] if rstd is not None else None
+    return check_ln(h_ref, gamma, beta, eps, _t(y), _t(mean), _t(rstd))
+
+
+def check_rms_add(x, r, w, eps, h, y, rows=None) -> dict:
+    h_ref = check_h(x, r, h, rows)
+    if rows is not None:
+        y = np_of(y)[rows]
+    return check_rms(h_ref, w, eps, _t(y))
+
+
+def _t(a):
+    return torch_of(a) if isinstance(a, np.ndarray) else a
 
 
 def sample_rows(M: int, k: int = 48, seed: int = 0) -> np.ndarray:

@@ -31,6 +31,7 @@ def declared_functions():
 def test_header_declares_the_abi():
     assert set(declared_functions()) == {
         "ln_fwd", "rms_fwd", "ln_fwd_planned", "rms_fwd_planned", "norm_make_plan",
+        "ln_fwd_add", "rms_fwd_add", "ln_fwd_add_planned", "rms_fwd_add_planned", "norm_make_plan_add",
         "norm_status_string", "norm_last_cuda_error", "norm_abi_version"}
 
 
@@ -79,6 +80,56 @@ def test_zero_rows_is_a_noop(lib):
     # M == 0: OK, nothing launched, pointers may be NULL
     assert lib.ln_fwd(None, None, None, None, None, None, 0, 8, 1e-5, rn.NORM_F32, None) == rn.NORM_OK
     assert lib.rms_fwd(None, None, None, 0, 8, 1e-6, rn.NORM_BF16, None) == rn.NORM_OK
+
+
+Q = ctypes.c_void_p(0x2000)   # a second fake buffer
+
+
+@pytest.mark.parametrize("M,N", [(-1, 8), (4, 0), (4, (1 << 24) + 1), (2 ** 62, 4)])
+def test_fused_add_bad_sizes_rejected(lib, M, N):
+    assert lib.ln_fwd_add(P, P, P, P, P, Q, None, None, M, N, 1e-5, rn.NORM_F32, None) == rn.NORM_ERR_ARG
+    assert lib.rms_fwd_add(P, P, P, P, Q, M, N, 1e-6, rn.NORM_BF16, None) == rn.NORM_ERR_ARG
+
+
+def test_fused_add_bad_dtype_and_eps_rejected(lib):
+    assert lib.ln_fwd_add(P, P, P, P, P, Q, None, None, 4, 8, 1e-5, 3, None) == rn.NORM_ERR_DTYPE
+    assert lib.rms_fwd_add(P, P, P, P, Q, 4, 8, float("nan"), rn.NORM_F32, None) == rn.NORM_ERR_ARG
+
+
+def test_fused_add_null_pointers_rejected(lib):
+    for i in range(6):
+        args = [P, P, P, P, P, Q]
+        args[i] = None
+        assert lib.ln_fwd_add(*args, None, None, 4, 8, 1e-5, rn.NORM_F32, None) == rn.NORM_ERR_ARG
+    for i in range(5):
+        args = [P, P, P, P, Q]
+        args[i] = None
+        assert lib.rms_fwd_add(*args, 4, 8, 1e-6, rn.NORM_F32, None) == rn.NORM_ERR_ARG
+
+
+def test_fused_add_h_and_y_must_differ(lib):
+    # h == y: both are written, refused on the host
+    assert lib.ln_fwd_add(P, Q, P, P, Q, Q, None, None, 4, 8, 1e-5, rn.NORM_F32, None) == rn.NORM_ERR_ARG
+    assert lib.rms_fwd_add(P, Q, P, P, P, 4, 8, 1e-6, rn.NORM_BF16, None) == rn.NORM_ERR_ARG
+
+
+def test_fused_add_zero_rows_is_a_noop(lib):
+    assert lib.ln_fwd_add(None, None, None, None, None, None, None, None, 0, 8, 1e-5, rn.NORM_F32,
+                          None) == rn.NORM_OK
+    assert lib.rms_fwd_add(None, None, None, None, None, 0, 8, 1e-6, rn.NORM_BF16, None) == rn.NORM_OK
+
+
+@pytest.mark.parametrize("kw", [
+    dict(stages=3, grid=0),          # no ring kernel for the fused add
+    dict(threads=544),               # above the 512-thread cap of the fused kernels
+    dict(threads=1024, per_thread=1),
+])
+def test_fused_add_plans_rejected(lib, kw):
+    p = _plan(**kw)
+    assert lib.rms_fwd_add_planned(P, P, P, P, Q, 4, 1000, 1e-6, rn.NORM_F32, None,
+                                   ctypes.byref(p)) == rn.NORM_ERR_PLAN
+    assert lib.ln_fwd_add_planned(P, P, P, P, P, Q, None, None, 4, 1000, 1e-5, rn.NORM_F32, None,
+                                  ctypes.byref(p)) == rn.NORM_ERR_PLAN
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
@@ -173,6 +224,20 @@ def test_plans_are_consistent(lib, dtype, aligned, M):
                 assert p["grid"] % p["cluster"] == 0 and p["grid"] == M * p["cluster"]
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("M", [1, 3, 128, 8192])
+def test_fused_add_plans_are_consistent(lib, dtype, M):
+    """The fused calls plan as the plain ones, with CTAs of at most 512
+    threads and no ring; where the plain plan already fits, it is the same."""
+    for N in NS:
+        p = rn.make_plan(M, N, dtype, True, 152, add=True)
+        q = rn.make_plan(M, N, dtype, True, 152)
+        assert 32 <= p["threads"] <= 512 and p["stages"] == 0
+        assert _covers(p, N), (N, p)
+        if q["threads"] <= 512:
+            assert p == q, (N, p, q)
+
+
 def test_plans_for_the_workloads(lib):
     """The mapping each benchmark workload gets (152 SMs, aligned buffers)."""
     got = {name: rn.make_plan(w.M, w.N, w.torch_dtype, True, 152) for name, w in WORKLOADS.items()}
@@ -185,6 +250,14 @@ def test_plans_for_the_workloads(lib):
         "ln_f32_2048x65536": dict(mapping=rn.NORM_MAP_CTA, per_thread=8, threads=128, cluster=8, rounds=2),
         "ln_f32_8192x5000": dict(mapping=rn.NORM_MAP_CTA, per_thread=8, threads=160, cluster=1, rounds=1),
     }
+    got.update({name: rn.make_plan(w.M, w.N, w.torch_dtype, True, 152, add=True)
+                for name, w in WORKLOADS.items() if w.add})
+    want.update({
+        "add_rms_f32_8192x4096": want["rms_f32_8192x4096"],
+        "add_rms_bf16_65536x2048": want["rms_bf16_65536x2048"],
+        "add_ln_bf16_4096x8192_outliers": want["ln_bf16_4096x8192_outliers"],
+        "add_ln_f32_2048x65536": want["ln_f32_2048x65536"],
+    })
     for name, w in want.items():
         for k, v in w.items():
             assert got[name][k] == v, (name, k, got[name])
@@ -204,3 +277,7 @@ def test_binding_rejects_cpu_tensors():
         rn.ln_fwd(x, torch.ones(8), torch.zeros(8))
     with pytest.raises(ValueError):
         rn.rms_fwd(x, torch.ones(8))
+    with pytest.raises(ValueError):
+        rn.ln_fwd_add(x, x, torch.ones(8), torch.zeros(8))
+    with pytest.raises(ValueError):
+        rn.rms_fwd_add(x, x, torch.ones(8))

@@ -48,11 +48,12 @@ def run_rms(x, w, eps, plan=None):
 # Scaled-down rows of every workload (same N, same value recipe): whole
 # outputs compared element by element, with the plan the full-size launch
 # uses (so the benchmarked kernel variant is the one checked).
+PLAIN = [n for n, w in wl.WORKLOADS.items() if not w.add]   # the fused ones: test_fused_add_gpu.py
 SMALL_M = {"ln_f32_128x1024": 128, "rms_f32_8192x4096": 96, "ln_bf16_4096x8192_outliers": 64,
            "rms_bf16_65536x2048": 517, "ln_f32_2048x65536": 6, "ln_f32_8192x5000": 77}
 
 
-@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+@pytest.mark.parametrize("name", PLAIN)
 def test_workload_rows_with_full_size_plan(name):
     w = wl.WORKLOADS[name]
     plan = rn.make_plan(w.M, w.N, w.torch_dtype, True, torch.cuda.get_device_properties(0).multi_processor_count)
@@ -72,7 +73,7 @@ def test_workload_rows_with_full_size_plan(name):
         check_rms(inp["x"], inp["w"], w.eps, y)
 
 
-@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+@pytest.mark.parametrize("name", PLAIN)
 def test_workload_full_size_sampled(name):
     """The full-size launch (default plan, as benchmarked): sampled rows
     element by element; statistics of every row (LayerNorm)."""
