@@ -202,8 +202,11 @@ def step_fn(w, rn, params):
 def time_same_bytes_copy(w, inp, device, steps=600, per_graph=60):
     """Device time of torch's copy of one buffer into another, each as large
     as the call's [M, N] inputs (x, or x and r): the algorithmic bytes minus
-    parameters and statistics, graph-replayed over rotating sets larger than
-    L2: what a plain copy of this size achieves."""
+    parameters and statistics, over rotating sets larger than L2: what a
+    plain copy of this size achieves. Timed both as graph replays and as
+    plain launches, the faster kept: captured in a graph, torch's copy of
+    512 MB or more becomes a memcpy node that runs at about half the copy
+    bandwidth of the same copy launched directly."""
     import torch
     n = w.M * w.N * (w.row_tensors // 2)
     sets = [(torch.empty(n, dtype=w.torch_dtype, device=device), torch.empty(n, dtype=w.torch_dtype, device=device))
@@ -228,10 +231,18 @@ def time_same_bytes_copy(w, inp, device, steps=600, per_graph=60):
         g.replay()
     t1.record()
     torch.cuda.synchronize(device)
-    ms = t0.elapsed_time(t1) / (steps // per_graph * per_graph)
+    graph_ms = t0.elapsed_time(t1) / (steps // per_graph * per_graph)
+    plain = min(steps, 200)
+    t0.record()
+    for i in range(plain):
+        src, dst = sets[i % len(sets)]
+        dst.copy_(src)
+    t1.record()
+    torch.cuda.synchronize(device)
+    plain_ms = t0.elapsed_time(t1) / plain
     del g, sets
     torch.cuda.empty_cache()
-    return ms
+    return min(graph_ms, plain_ms)
 
 
 def n_sets_for(w):

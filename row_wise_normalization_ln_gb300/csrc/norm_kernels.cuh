@@ -478,9 +478,14 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_group(
 // folded into the thread's state with the pairwise merge); the output pass
 // then walks the rounds backwards, reusing the registers of the last round
 // and re-reading the others. CL: launched with clusters (C > 1); without,
-// every cluster step compiles away. ADD: fused residual add; the row is
-// h = x + r (rounded to T), written to a.h in the output pass, after the
-// row's barrier, so that h may be the x or r buffer itself.
+// every cluster step compiles away.
+// ADD: fused residual add; the row is h = x + r (rounded to T). The rounds
+// are then read in reverse, so that round 0, which holds the shift element
+// every thread of the row reads first, is the one kept in registers; its h
+// is stored in the output pass, after the row's barrier. The other rounds
+// store h as soon as it is formed and the output pass re-reads h, not x and
+// r. Every thread re-reads only its own accesses, so h (and y) may be the x
+// or r buffer itself.
 template <class T, int VEC, int V, bool LN, bool CL, bool ADD>
 __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(const NormArgs a) {
     using S = Slice<T, VEC, V, LN>;
@@ -512,20 +517,24 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
         S s;
         const float K = LN ? (ADD ? first_elem_add(xr, rr) : first_elem(xr)) : 0.f;
         s.set_shift(K);
+        T* hr = ADD ? static_cast<T*>(a.h) + row * a.N : nullptr;
         float n_t = 0.f, sum_t = 0.f, mean_t = 0.f, m2_t = 0.f, ss_t = 0.f;
         int nv = 0;
-        for (int r = 0; r < rounds; ++r) {
+        for (int i = 0; i < rounds; ++i) {
+            const int r = ADD ? rounds - 1 - i : i;
             const int f = (r * static_cast<int>(C) + rank) * V * T_ + in_slice;
             nv = valid_runs(nacc, f, 32, V);
-            if constexpr (ADD)
+            if constexpr (ADD) {
                 s.load_add(xr + f * VEC, rr + f * VEC, stride, nv);
-            else
+                if (r != 0) s.store_h(hr + f * VEC, stride, nv);
+            } else {
                 s.load(xr + f * VEC, stride, nv);
+            }
             if constexpr (LN) {
                 const float n = static_cast<float>(nv * VEC);
                 float sum = 0.f, mean = 0.f, m2 = 0.f;
                 s.welford(nv, nv > 0 ? 1.f / n : 0.f, sum, mean, m2);
-                if (r == 0) {
+                if (i == 0) {
                     n_t = n, sum_t = sum, mean_t = mean, m2_t = m2;
                 } else if (n > 0.f) {  // pairwise merge ([Ch7] §7.4.1)
                     const float nn = n_t + n;
@@ -546,18 +555,27 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
             if (a.mean) a.mean[row] = K + mu;
             if (a.rstd) a.rstd[row] = rs;
         }
-        for (int r = rounds - 1; r >= 0; --r) {
-            const int f = (r * static_cast<int>(C) + rank) * V * T_ + in_slice;
-            if (r != rounds - 1) {
-                nv = valid_runs(nacc, f, 32, V);
-                if constexpr (ADD)
-                    s.load_add(xr + f * VEC, rr + f * VEC, stride, nv);  // x, r of this round are untouched
-                else
-                    s.load(xr + f * VEC, stride, nv);
+        if constexpr (ADD) {
+            for (int r = 0; r < rounds; ++r) {
+                const int f = (r * static_cast<int>(C) + rank) * V * T_ + in_slice;
+                if (r != 0) {
+                    nv = valid_runs(nacc, f, 32, V);
+                    s.load(hr + f * VEC, stride, nv);  // only this thread wrote h there
+                }
+                s.emit(static_cast<const T*>(a.gamma) + f * VEC, static_cast<const T*>(a.beta) + f * VEC,
+                       yr + f * VEC, stride, nv, mu, rs);
+                if (r == 0) s.store_h(hr + f * VEC, stride, nv);
             }
-            s.emit(static_cast<const T*>(a.gamma) + f * VEC, static_cast<const T*>(a.beta) + f * VEC, yr + f * VEC,
-                   stride, nv, mu, rs);
-            if constexpr (ADD) s.store_h(static_cast<T*>(a.h) + row * a.N + f * VEC, stride, nv);
+        } else {
+            for (int r = rounds - 1; r >= 0; --r) {
+                const int f = (r * static_cast<int>(C) + rank) * V * T_ + in_slice;
+                if (r != rounds - 1) {
+                    nv = valid_runs(nacc, f, 32, V);
+                    s.load(xr + f * VEC, stride, nv);
+                }
+                s.emit(static_cast<const T*>(a.gamma) + f * VEC, static_cast<const T*>(a.beta) + f * VEC,
+                       yr + f * VEC, stride, nv, mu, rs);
+            }
         }
     }
     // No CTA may exit while a peer can still read its shared memory.
