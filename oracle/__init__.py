@@ -51,8 +51,11 @@ def lib():
         L.oracle_welford_update.argtypes = [ctypes.POINTER(Welford), dbl]
         L.oracle_chan_combine.argtypes = [ctypes.POINTER(Welford)] * 3
         L.oracle_add_round.argtypes = [vp, vp, i32, i64, vp]
+        L.oracle_ln_bwd.argtypes = [vp, vp, vp, i32, i64, i64, dbl, vp, vp, vp]
+        L.oracle_rms_bwd.argtypes = [vp, vp, vp, i32, i64, i64, dbl, vp, vp]
         for f in ("oracle_row_moments", "oracle_ln_fwd", "oracle_rms_fwd", "oracle_round_f32",
-                  "oracle_round_bf16", "oracle_welford_update", "oracle_chan_combine", "oracle_add_round"):
+                  "oracle_round_bf16", "oracle_welford_update", "oracle_chan_combine", "oracle_add_round",
+                  "oracle_ln_bwd", "oracle_rms_bwd"):
             getattr(L, f).restype = None
         L.oracle_abi_version.restype = ctypes.c_int
         _lib = L
@@ -152,6 +155,32 @@ def rms_fwd_add(x, r, w, eps):
     """Fused residual add + RMSNorm: returns (h, y, rstd)."""
     h = add_round(x, r)
     return (h,) + rms_fwd(h, w, eps)
+
+
+def ln_bwd(dy: np.ndarray, x: np.ndarray, gamma: np.ndarray, eps: float):
+    """LayerNorm backward of a 2-D array given the upstream gradient dy.
+    Returns (dx, dgamma, dbeta) in float64."""
+    dy, x, gamma = _c(dy), _c(x), _c(gamma)
+    M, N = x.shape
+    code = _dtype_code(x)
+    assert _dtype_code(dy) == code and _dtype_code(gamma) == code and dy.shape == x.shape and gamma.size == N
+    dx = np.empty((M, N), np.float64)
+    dg = np.empty(N, np.float64)
+    db = np.empty(N, np.float64)
+    lib().oracle_ln_bwd(_ptr(dy), _ptr(x), _ptr(gamma), code, M, N, float(eps), _ptr(dx), _ptr(dg), _ptr(db))
+    return dx, dg, db
+
+
+def rms_bwd(dy: np.ndarray, x: np.ndarray, w: np.ndarray, eps: float):
+    """RMSNorm backward of a 2-D array. Returns (dx, dw) in float64."""
+    dy, x, w = _c(dy), _c(x), _c(w)
+    M, N = x.shape
+    code = _dtype_code(x)
+    assert _dtype_code(dy) == code and _dtype_code(w) == code and dy.shape == x.shape and w.size == N
+    dx = np.empty((M, N), np.float64)
+    dw = np.empty(N, np.float64)
+    lib().oracle_rms_bwd(_ptr(dy), _ptr(x), _ptr(w), code, M, N, float(eps), _ptr(dx), _ptr(dw))
+    return dx, dw
 
 
 def welford_update(s: Welford, x: float) -> Welford:

@@ -1,6 +1,6 @@
 /*
  * oracle.c - plain, slow, single-threaded fp64 CPU reference for the
- * row-wise LayerNorm and RMSNorm forward pass.
+ * row-wise LayerNorm and RMSNorm forward and backward passes.
  *
  * TEST INFRASTRUCTURE ONLY. Only the tests, the smoke check and the CPU
  * baseline leg of the benchmark may load this library. The product path
@@ -231,4 +231,81 @@ void oracle_add_round(const void *x, const void *r, int dtype, int64_t n, void *
     }
 }
 
-int oracle_abi_version(void) { return 2; }
+/*
+ * LayerNorm backward over an [M, N] row-major matrix ([Ch7] §7.7), given the
+ * upstream gradient dy of the same shape. Per row, with mu, var by the
+ * two-pass definition and rstd = 1/sqrt(var + eps):
+ *   xhat_i = (x_i - mu) * rstd,  g_i = dy_i * gamma_i,
+ *   gbar = sum_j g_j / N,  gxbar = sum_j g_j xhat_j / N,
+ *   dx_i = rstd * (g_i - gbar - xhat_i * gxbar)
+ * (gamma multiplies dy inside the bracket, element by element), and over
+ * rows dgamma_i = sum_n dy_i xhat_i, dbeta_i = sum_n dy_i. dy, x and gamma
+ * share `dtype`; every output is double.
+ */
+void oracle_ln_bwd(const void *dy, const void *x, const void *gamma, int dtype,
+                   int64_t M, int64_t N, double eps,
+                   double *dx, double *dgamma, double *dbeta)
+{
+    const int64_t es = orc_elem_size(dtype);
+    for (int64_t i = 0; i < N; ++i)
+        dgamma[i] = dbeta[i] = 0.0;
+    for (int64_t r = 0; r < M; ++r) {
+        const void *xr = (const char *)x + r * N * es;
+        const void *dyr = (const char *)dy + r * N * es;
+        double mu, var;
+        oracle_row_moments(xr, dtype, N, &mu, &var);
+        const double rs = 1.0 / sqrt(var + eps);
+        double sg = 0.0, sgx = 0.0;
+        for (int64_t i = 0; i < N; ++i) {
+            const double xh = (orc_load(xr, dtype, i) - mu) * rs;
+            const double g = orc_load(dyr, dtype, i) * orc_load(gamma, dtype, i);
+            sg += g;
+            sgx += g * xh;
+        }
+        const double gbar = sg / (double)N, gxbar = sgx / (double)N;
+        for (int64_t i = 0; i < N; ++i) {
+            const double xh = (orc_load(xr, dtype, i) - mu) * rs;
+            const double d = orc_load(dyr, dtype, i);
+            const double g = d * orc_load(gamma, dtype, i);
+            dx[r * N + i] = rs * (g - gbar - xh * gxbar);
+            dgamma[i] += d * xh;
+            dbeta[i] += d;
+        }
+    }
+}
+
+/*
+ * RMSNorm backward ([Ch7] §7.7, last paragraph: one row sum, of dy*w*x).
+ * With rstd = 1/sqrt(sum x^2 / N + eps) and y_i = x_i * rstd * w_i:
+ *   S = sum_j dy_j w_j x_j,
+ *   dx_i = rstd * w_i * dy_i - x_i * rstd^3 * S / N,
+ *   dw_i = sum_n dy_i x_i rstd.
+ * (d rstd / d x_j = -rstd^3 x_j / N.)
+ */
+void oracle_rms_bwd(const void *dy, const void *x, const void *w, int dtype,
+                    int64_t M, int64_t N, double eps, double *dx, double *dw)
+{
+    const int64_t es = orc_elem_size(dtype);
+    for (int64_t i = 0; i < N; ++i)
+        dw[i] = 0.0;
+    for (int64_t r = 0; r < M; ++r) {
+        const void *xr = (const char *)x + r * N * es;
+        const void *dyr = (const char *)dy + r * N * es;
+        double ss = 0.0, s = 0.0;
+        for (int64_t i = 0; i < N; ++i) {
+            const double xi = orc_load(xr, dtype, i);
+            ss += xi * xi;
+            s += orc_load(dyr, dtype, i) * orc_load(w, dtype, i) * xi;
+        }
+        const double rs = 1.0 / sqrt(ss / (double)N + eps);
+        const double c = rs * rs * rs * s / (double)N;
+        for (int64_t i = 0; i < N; ++i) {
+            const double xi = orc_load(xr, dtype, i);
+            const double d = orc_load(dyr, dtype, i);
+            dx[r * N + i] = rs * orc_load(w, dtype, i) * d - xi * c;
+            dw[i] += d * xi * rs;
+        }
+    }
+}
+
+int oracle_abi_version(void) { return 3; }

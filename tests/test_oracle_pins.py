@@ -387,3 +387,168 @@ def test_fused_add_is_norm_of_the_sum():
     assert np.array_equal(y, y2) and np.array_equal(mean, mean2) and np.array_equal(rstd, rstd2)
     h, y, rstd = oracle.rms_fwd_add(x, r, g, 1e-6)
     assert np.array_equal(y, oracle.rms_fwd(x + r, g, 1e-6)[0])
+
+
+# ---------------------------------------------------------------- backward
+
+def _loss_ln(x, g, b, dy, eps):
+    """L = sum dy * y with y the (pinned) forward oracle: its gradient is
+    what the backward oracle must return."""
+    return float((oracle.ln_fwd(x, g, b, eps)[0] * dy).sum())
+
+
+def _loss_rms(x, w, dy, eps):
+    return float((oracle.rms_fwd(x, w, eps)[0] * dy).sum())
+
+
+def _fd(f, a, h):
+    """Central differences of f with respect to every entry of `a`."""
+    out = np.empty(a.shape)
+    for idx in np.ndindex(a.shape):
+        ap, am = a.copy(), a.copy()
+        ap[idx] += h
+        am[idx] -= h
+        out[idx] = (f(ap) - f(am)) / (2 * h)
+    return out
+
+
+@pytest.mark.parametrize("M,N,eps", [(1, 1, 1e-5), (2, 2, 1e-5), (3, 5, 1e-5), (2, 8, 0.3), (4, 17, 1e-5)])
+def test_ln_bwd_is_the_gradient_of_the_forward(M, N, eps):
+    """'第 7 章' §7.7 formulas against finite differences of the forward
+    definition (step 1e-5: truncation ~1e-10, rounding ~1e-11)."""
+    rng = np.random.default_rng(M * 100 + N)
+    x = rng.normal(1.0, 2.0, (M, N))
+    g = rng.uniform(0.5, 1.5, N)
+    b = rng.uniform(-0.5, 0.5, N)
+    dy = rng.normal(0, 1, (M, N))
+    dx, dg, db = oracle.ln_bwd(dy, x, g, eps)
+    h = 1e-5
+    assert np.allclose(dx, _fd(lambda a: _loss_ln(a, g, b, dy, eps), x, h), rtol=1e-6, atol=1e-7)
+    assert np.allclose(dg, _fd(lambda a: _loss_ln(x, a, b, dy, eps), g, h), rtol=1e-6, atol=1e-7)
+    assert np.allclose(db, _fd(lambda a: _loss_ln(x, g, a, dy, eps), b, h), rtol=1e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("M,N,eps", [(1, 1, 1e-6), (2, 3, 1e-6), (3, 8, 0.5), (4, 19, 1e-6)])
+def test_rms_bwd_is_the_gradient_of_the_forward(M, N, eps):
+    rng = np.random.default_rng(M * 10 + N)
+    x = rng.normal(0.5, 1.5, (M, N))
+    w = rng.uniform(0.2, 1.2, N)
+    dy = rng.normal(0, 1, (M, N))
+    dx, dw = oracle.rms_bwd(dy, x, w, eps)
+    h = 1e-5
+    assert np.allclose(dx, _fd(lambda a: _loss_rms(a, w, dy, eps), x, h), rtol=1e-6, atol=1e-7)
+    assert np.allclose(dw, _fd(lambda a: _loss_rms(x, a, dy, eps), w, h), rtol=1e-6, atol=1e-7)
+
+
+def test_gamma_outside_the_bracket_is_caught():
+    """§7.7 warns that gamma multiplies dy inside the bracket; the formula
+    with gamma pulled out (the common mistake) fails the finite-difference
+    check that the oracle passes: a negative control of that pin."""
+    rng = np.random.default_rng(3)
+    x = rng.normal(0, 1, (2, 9))
+    g = rng.uniform(0.2, 2.0, 9)
+    b = np.zeros(9)
+    dy = rng.normal(0, 1, (2, 9))
+    fd = _fd(lambda a: _loss_ln(a, g, b, dy, 1e-5), x, 1e-5)
+    mu = x.mean(1, keepdims=True)
+    rs = 1 / np.sqrt(((x - mu) ** 2).mean(1, keepdims=True) + 1e-5)
+    xh = (x - mu) * rs
+    wrong = rs * g * (dy - dy.mean(1, keepdims=True) - xh * (dy * xh).mean(1, keepdims=True))
+    assert np.abs(wrong - fd).max() > 1e-2
+    assert np.allclose(oracle.ln_bwd(dy, x, g, 1e-5)[0], fd, rtol=1e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+def test_ln_bwd_matches_torch_autograd(dtype):
+    """Library routine: torch's fp64 layer_norm backward (autograd)."""
+    rng = np.random.default_rng(21)
+    M, N = 7, 333
+    x = rng.normal(3, 2, (M, N)).astype(dtype)
+    g = rng.uniform(0.5, 1.5, N).astype(dtype)
+    b = rng.uniform(-0.1, 0.1, N).astype(dtype)
+    dy = rng.normal(0, 1, (M, N)).astype(dtype)
+    xt = torch.tensor(x, dtype=torch.float64, requires_grad=True)
+    gt = torch.tensor(g, dtype=torch.float64, requires_grad=True)
+    bt = torch.tensor(b, dtype=torch.float64, requires_grad=True)
+    y = torch.nn.functional.layer_norm(xt, (N,), gt, bt, 1e-5)
+    y.backward(torch.tensor(dy, dtype=torch.float64))
+    dx, dg, db = oracle.ln_bwd(dy, x, g, 1e-5)
+    assert np.allclose(dx, xt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    assert np.allclose(dg, gt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    assert np.allclose(db, bt.grad.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_rms_bwd_matches_torch_autograd():
+    rng = np.random.default_rng(22)
+    M, N = 6, 250
+    x = rng.normal(0, 1, (M, N))
+    w = rng.uniform(0, 1, N)
+    dy = rng.normal(0, 1, (M, N))
+    xt = torch.tensor(x, requires_grad=True)
+    wt = torch.tensor(w, requires_grad=True)
+    ms = (xt * xt).mean(-1, keepdim=True)
+    y = xt * torch.rsqrt(ms + 1e-6) * wt   # written out: RMSNorm by its definition, differentiated by autograd
+    y.backward(torch.tensor(dy))
+    dx, dw = oracle.rms_bwd(dy, x, w, 1e-6)
+    assert np.allclose(dx, xt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    assert np.allclose(dw, wt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    if hasattr(torch.nn.functional, "rms_norm"):
+        xt.grad = None
+        wt.grad = None
+        torch.nn.functional.rms_norm(xt, (N,), wt, 1e-6).backward(torch.tensor(dy))
+        assert np.allclose(dx, xt.grad.numpy(), rtol=1e-10, atol=1e-12)
+        assert np.allclose(dw, wt.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_bwd_invariants():
+    """LayerNorm: sum_i dx_i = 0 for any dy and gamma (xhat sums to zero),
+    and with eps = 0 also sum_i dx_i xhat_i = 0 (y does not change when x is
+    scaled about its mean). RMSNorm with eps = 0: sum_i dx_i x_i = 0 (y does
+    not change when x is scaled)."""
+    rng = np.random.default_rng(23)
+    M, N = 5, 1000
+    x = rng.normal(2, 3, (M, N))
+    g = rng.uniform(0.5, 1.5, N)
+    dy = rng.normal(0, 1, (M, N))
+    dx, _, _ = oracle.ln_bwd(dy, x, g, 1e-5)
+    scale = np.abs(dx).sum(1)
+    assert np.all(np.abs(dx.sum(1)) <= 1e-13 * scale)
+    dx0, _, _ = oracle.ln_bwd(dy, x, g, 0.0)
+    xh = (x - x.mean(1, keepdims=True)) / x.std(1, keepdims=True)
+    assert np.all(np.abs((dx0 * xh).sum(1)) <= 1e-12 * np.abs(dx0 * xh).sum(1))
+    dxr, _ = oracle.rms_bwd(dy, x, g, 0.0)
+    assert np.all(np.abs((dxr * x).sum(1)) <= 1e-12 * np.abs(dxr * x).sum(1))
+
+
+def test_bwd_special_cases():
+    """Constant dy with gamma = 1: g is constant, so dx = 0; dbeta_i = M c;
+    dgamma_i = c * sum_n xhat_ni. dy = 0: every gradient is zero."""
+    rng = np.random.default_rng(24)
+    M, N, c = 4, 64, 0.75
+    x = rng.normal(0, 1, (M, N))
+    dy = np.full((M, N), c)
+    dx, dg, db = oracle.ln_bwd(dy, x, np.ones(N), 1e-5)
+    assert np.abs(dx).max() <= 1e-13
+    assert np.allclose(db, M * c, rtol=0, atol=1e-13)
+    mu = x.mean(1, keepdims=True)
+    xh = (x - mu) / np.sqrt(((x - mu) ** 2).mean(1, keepdims=True) + 1e-5)
+    assert np.allclose(dg, c * xh.sum(0), rtol=1e-12, atol=1e-13)
+    z = np.zeros((M, N))
+    for v in oracle.ln_bwd(z, x, rng.uniform(0, 1, N), 1e-5) + oracle.rms_bwd(z, x, rng.uniform(0, 1, N), 1e-6):
+        assert not v.any()
+
+
+def test_bwd_bf16_inputs_widen_exactly():
+    """bf16 inputs give the gradient of their exact fp32 values."""
+    rng = np.random.default_rng(25)
+    x = rng.normal(0, 1, (3, 40)).astype(np.float32)
+    g = rng.uniform(0.5, 1.5, 40).astype(np.float32)
+    dy = rng.normal(0, 1, (3, 40)).astype(np.float32)
+    bf = lambda a: (a.view(np.uint32) >> 16).astype(np.uint16)
+    back = lambda u: (u.astype(np.uint32) << 16).view(np.float32)
+    for got, want in zip(oracle.ln_bwd(bf(dy), bf(x), bf(g), 1e-5),
+                         oracle.ln_bwd(back(bf(dy)), back(bf(x)), back(bf(g)), 1e-5)):
+        assert np.array_equal(got, want)
+    for got, want in zip(oracle.rms_bwd(bf(dy), bf(x), bf(g), 1e-6),
+                         oracle.rms_bwd(back(bf(dy)), back(bf(x)), back(bf(g)), 1e-6)):
+        assert np.array_equal(got, want)
