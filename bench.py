@@ -91,7 +91,23 @@ def kernel_name(w, plan) -> str:
     kind = "group" if plan["mapping"] == 0 else "cta"
     t = "float" if w.dtype == "f32" else "__nv_bfloat16"
     op = ("ADD+" if w.add else "") + ("LN" if w.op == "ln" else "RMS")
+    if w.bwd:
+        return f"norm_bwd_cta<{t},{plan['vec_elems']},{plan['per_thread']},{op}>"
     return f"norm_fwd_{kind}<{t},{plan['vec_elems']},{plan['per_thread']},{op}>"
+
+
+def op_name(w) -> str:
+    return ("add+" if w.add else "") + w.op + ("_bwd" if w.bwd else "")
+
+
+def metric_name(w) -> str:
+    return f"LN/RMSNorm {'bwd' if w.bwd else 'fwd'} achieved HBM GB/s"
+
+
+def plan_for(rn, w, num_sms):
+    if w.bwd:
+        return rn.make_bwd_plan(w.M, w.N, w.torch_dtype, w.op == "ln", True, num_sms)
+    return rn.make_plan(w.M, w.N, w.torch_dtype, True, num_sms, add=w.add)
 
 
 class ClockSampler:
@@ -161,6 +177,8 @@ class ClockSampler:
 
 def make_sets(w, inp, n_sets, device):
     import torch
+    if w.bwd:
+        return make_bwd_sets(w, inp, n_sets, device)
     sets = []
     for _ in range(n_sets):
         s = {"x": inp["x"].to(device), "y": torch.empty(w.M, w.N, dtype=w.torch_dtype, device=device)}
@@ -175,8 +193,42 @@ def make_sets(w, inp, n_sets, device):
     return sets, params
 
 
+def make_bwd_sets(w, inp, n_sets, device):
+    """Backward sets: dy, x, dx per set (LayerNorm: the statistics of x from
+    ln_fwd, computed once here, outside the timed region); the column
+    gradients and the workspace are shared by the sets (calls are
+    serialised on one stream)."""
+    import torch
+    import row_wise_normalization_ln_gb300 as rn
+    params = {k: v.to(device) for k, v in inp.items() if k not in ("x", "dy")}
+    sets = []
+    for _ in range(n_sets):
+        s = {"x": inp["x"].to(device), "dy": inp["dy"].to(device), "dx": torch.empty(w.M, w.N, dtype=w.torch_dtype,
+                                                                                     device=device)}
+        if w.op == "ln":
+            _, s["mean"], s["rstd"] = rn.ln_fwd(s["x"], params["gamma"], params["beta"], w.eps, out=s["dx"])
+        sets.append(s)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    plan = rn.make_bwd_plan(w.M, w.N, w.torch_dtype, w.op == "ln", True, sms)
+    nb = rn.bwd_workspace_bytes(plan, w.N, w.op == "ln")
+    params["ws"] = torch.empty(max(nb, 16) // 4, dtype=torch.float32, device=device)
+    params["dg"] = torch.empty(w.N, dtype=torch.float32, device=device)
+    params["db"] = torch.empty(w.N, dtype=torch.float32, device=device)
+    return sets, params
+
+
 def step_fn(w, rn, params):
-    if w.add and w.op == "ln":
+    if w.bwd and w.op == "ln":
+        g, ws, dg, db = params["gamma"], params["ws"], params["dg"], params["db"]
+
+        def f(s):
+            rn.ln_bwd(s["dy"], s["x"], g, s["mean"], s["rstd"], dx=s["dx"], dgamma=dg, dbeta=db, workspace=ws)
+    elif w.bwd:
+        wt, ws, dg = params["w"], params["ws"], params["dg"]
+
+        def f(s):
+            rn.rms_bwd(s["dy"], s["x"], wt, w.eps, dx=s["dx"], dw=dg, workspace=ws)
+    elif w.add and w.op == "ln":
         g, b = params["gamma"], params["beta"]
 
         def f(s):
@@ -201,14 +253,15 @@ def step_fn(w, rn, params):
 
 def time_same_bytes_copy(w, inp, device, steps=600, per_graph=60):
     """Device time of torch's copy of one buffer into another, each as large
-    as the call's [M, N] inputs (x, or x and r): the algorithmic bytes minus
+    as half the call's [M, N] traffic (x; x and r for the fused add; 1.5 [M, N]
+    for the backward, which moves dy, x and dx): the algorithmic bytes minus
     parameters and statistics, over rotating sets larger than L2: what a
     plain copy of this size achieves. Timed both as graph replays and as
     plain launches, the faster kept: captured in a graph, torch's copy of
     512 MB or more becomes a memcpy node that runs at about half the copy
     bandwidth of the same copy launched directly."""
     import torch
-    n = w.M * w.N * (w.row_tensors // 2)
+    n = w.M * w.N * w.row_tensors // 2
     sets = [(torch.empty(n, dtype=w.torch_dtype, device=device), torch.empty(n, dtype=w.torch_dtype, device=device))
             for _ in range(n_sets_for(w))]
     for src, _ in sets:
@@ -312,10 +365,64 @@ class _Null:
         return False
 
 
+def time_e2e_bwd(w, rn, inp, device, steps):
+    """Backward end to end: H2D of dy, x, the parameter (and, for LayerNorm,
+    the statistics, which ln_fwd computed once beforehand), the call, D2H of
+    dx and the column gradients."""
+    import torch
+    ln = w.op == "ln"
+    hin = {k: inp[k].pin_memory() for k in ("dy", "x", "gamma" if ln else "w")}
+    din = {k: torch.empty_like(v, device=device) for k, v in hin.items()}
+    if ln:
+        xd = inp["x"].to(device)
+        _, m, r = rn.ln_fwd(xd, inp["gamma"].to(device), inp["beta"].to(device), w.eps)
+        hin["mean"], hin["rstd"] = m.cpu().pin_memory(), r.cpu().pin_memory()
+        din["mean"], din["rstd"] = torch.empty_like(m), torch.empty_like(r)
+        del xd
+    dx = torch.empty_like(din["x"])
+    hdx = torch.empty_like(hin["x"]).pin_memory()
+    dg = torch.empty(w.N, dtype=torch.float32, device=device)
+    db = torch.empty(w.N, dtype=torch.float32, device=device)
+    hdg = torch.empty(w.N, dtype=torch.float32).pin_memory()
+    hdb = torch.empty(w.N, dtype=torch.float32).pin_memory()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    plan = rn.make_bwd_plan(w.M, w.N, w.torch_dtype, ln, True, sms)
+    ws = torch.empty(max(rn.bwd_workspace_bytes(plan, w.N, ln), 16) // 4, dtype=torch.float32, device=device)
+    h2d = sum(v.numel() * v.element_size() for v in hin.values())
+    d2h = hdx.numel() * hdx.element_size() + (8 if ln else 4) * w.N
+
+    def one():
+        for k in hin:
+            din[k].copy_(hin[k], non_blocking=True)
+        if ln:
+            rn.ln_bwd(din["dy"], din["x"], din["gamma"], din["mean"], din["rstd"], dx=dx, dgamma=dg, dbeta=db,
+                      workspace=ws)
+            hdb.copy_(db, non_blocking=True)
+        else:
+            rn.rms_bwd(din["dy"], din["x"], din["w"], w.eps, dx=dx, dw=dg, workspace=ws)
+        hdg.copy_(dg, non_blocking=True)
+        hdx.copy_(dx, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize(device)
+    stream = torch.cuda.current_stream(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        one()
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    return t0.elapsed_time(t1) / steps, h2d, d2h
+
+
 def time_e2e(w, rn, inp, device, steps):
     """Host buffers in, host buffers out: H2D of x (and r) and the
     parameters, the call, D2H of y (and h, and the statistics), every step,
     on one stream."""
+    if w.bwd:
+        return time_e2e_bwd(w, rn, inp, device, steps)
     import torch
     hin = {k: v.pin_memory() for k, v in inp.items()}
     din = {k: torch.empty_like(v, device=device) for k, v in hin.items()}
@@ -379,6 +486,11 @@ def oracle_rows(w, inp, rows: int):
 
     x = npx(inp["x"][:rows])
     e = oracle.eps_as_f32(w.eps)
+    if w.bwd:
+        dy = npx(inp["dy"][:rows])
+        if w.op == "ln":
+            return lambda: oracle.ln_bwd(dy, x, npx(inp["gamma"]), e)
+        return lambda: oracle.rms_bwd(dy, x, npx(inp["w"]), e)
     if w.add:
         r = npx(inp["r"][:rows])
         if w.op == "ln":
@@ -456,10 +568,10 @@ def run_reference(args, w):
     el = time.perf_counter() - t0
     gbs = w.algorithmic_bytes(rows) * args.steps / el / 1e9
     line = {
-        "impl": "reference", "metric": "LN/RMSNorm fwd achieved HBM GB/s", "value": round(gbs, 4), "unit": "GB/s",
+        "impl": "reference", "metric": metric_name(w), "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "op": ("add+" if w.add else "") + w.op,
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "op": op_name(w),
                    "io_dtype": w.dtype, "eps": w.eps, "sample_rows_per_step": rows},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{rows} of {w.M} rows per step, fp64, 1 thread"},
@@ -520,8 +632,7 @@ def main():
                            # achieved GB/s over the same-size copy's GB/s
                            "frac_of_same_size_copy": round(
                                gbs / ((wk.row_tensors * wk.M * wk.N * wk.elem_size) / (copy_us / 1e6) / 1e9), 4),
-                           "rows_per_s": round(wk.M / (us / 1e6)), "plan": rn.make_plan(
-                               wk.M, wk.N, wk.torch_dtype, True, props.multi_processor_count, add=wk.add)}
+                           "rows_per_s": round(wk.M / (us / 1e6)), "plan": plan_for(rn, wk, props.multi_processor_count)}
             del wi
 
     if world > 1:
@@ -534,11 +645,11 @@ def main():
 
     cpu = cpu_baseline(w, inp, args.cpu_seconds)
     line = {
-        "metric": "LN/RMSNorm fwd achieved HBM GB/s", "value": round(value, 2), "unit": "GB/s",
+        "metric": metric_name(w), "value": round(value, 2), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "us_per_call": round(kern_ms * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": w.name, "op": ("add+" if w.add else "") + w.op, "M": w.M, "N": w.N,
+        "config": {"workload": w.name, "op": op_name(w), "M": w.M, "N": w.N,
                    "io_dtype": w.dtype, "eps": w.eps,
                    "algorithmic_bytes_per_call": bytes_per_call,
                    "l2": f"{n_sets_for(w)} rotating input/output sets of "
@@ -547,8 +658,7 @@ def main():
                    "parallelism": f"replicas x{world} (rows independent)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": traffic,
-                     "kernel": kernel_name(w, rn.make_plan(w.M, w.N, w.torch_dtype, True, props.multi_processor_count,
-                                                           add=w.add)),
+                     "kernel": kernel_name(w, plan_for(rn, w, props.multi_processor_count)),
                      "kernel_hash": kernel_source_hash()},
         "e2e": {"value": round(bytes_per_call / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},

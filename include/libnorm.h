@@ -4,7 +4,8 @@
  * Sources of the operations (page title, section):
  *   [Ch7]  "第 7 章 LayerNorm 与 RMSNorm" (CUDA 算子工程): §7.1 LayerNorm
  *          definition, §7.4 Welford, §7.4.1 parallel merge, §7.5 RMSNorm,
- *          §7.6 fused kernel structure (per-row statistics, mean/rstd saved).
+ *          §7.6 fused kernel structure (per-row statistics, mean/rstd saved),
+ *          §7.7 backward formulas.
  *   [RMS2] "CUDA算子优化(2)：RMSNorm": §1 formula, §2 [B*T, C] layout.
  *   [T3]   "T3 讲解：LayerNorm / RMSNorm 的 forward": §② masking, biased
  *          variance, fp32 statistics; §④ host reshape to [M, N]; §⑤ fusion
@@ -13,7 +14,7 @@
  * Conventions shared by every entry point:
  *   - All pointers are DEVICE pointers on the current CUDA device, owned by
  *     the caller. The library allocates nothing and keeps no state between
- *     calls; work is enqueued asynchronously on `stream` (NULL = the legacy
+ *     calls (the backward's scratch is a caller-provided workspace); work is enqueued asynchronously on `stream` (NULL = the legacy
  *     default stream). The caller keeps buffers alive until the stream has
  *     finished the call.
  *   - x and y are [M, N] row-major and contiguous (row stride N elements).
@@ -36,6 +37,7 @@
 #ifndef LIBNORM_H
 #define LIBNORM_H
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -174,6 +176,74 @@ norm_status rms_fwd_add_planned(const void* x, const void* residual, const void*
                                 void* h, void* y, int64_t M, int64_t N, float eps,
                                 norm_dtype dtype, cudaStream_t stream,
                                 const norm_plan* plan);
+
+/*
+ * LayerNorm backward ([Ch7] §7.7; [T3] §⑥: the forward's fp32 mean and rstd
+ * are reused, so the backward makes no statistics pass of its own):
+ *   xhat_ri = (x_ri - mean_r) * rstd_r,   g_ri = dy_ri * gamma_i
+ *   dx_ri   = rstd_r * (g_ri - sum_j g_rj / N - xhat_ri * sum_j g_rj xhat_rj / N)
+ *   dgamma_i = sum_r dy_ri * xhat_ri,     dbeta_i = sum_r dy_ri
+ * dy, x, dx: [M, N] of `dtype`; gamma: [N] of `dtype`; mean, rstd: fp32 [M]
+ * as written by ln_fwd; dgamma, dbeta: fp32 [N] (always written; zero when
+ * M == 0). dx may be dy or x itself; any other overlap is undefined.
+ * `workspace` (device memory owned by the caller, 16-byte aligned, at least
+ * norm_bwd_workspace_bytes() for the plan norm_bwd_make_plan chooses on this
+ * device; may be NULL when that is 0) holds the partial column sums; calls
+ * sharing a workspace must not overlap on the GPU. The column sums are added
+ * in a fixed order: results are deterministic for a given plan.
+ * Limit: a row must fit one register pass of a cluster of 8 CTAs of 512
+ * threads: N <= 65536 (fp32, bf16 LayerNorm) or 131072 (bf16 RMSNorm) with
+ * 16-byte vectors, N <= 32768 with element accesses; longer rows return
+ * NORM_ERR_ARG.
+ */
+norm_status ln_bwd(const void* dy, const void* x, const void* gamma, const float* mean,
+                   const float* rstd, void* dx, float* dgamma, float* dbeta, void* workspace,
+                   size_t workspace_bytes, int64_t M, int64_t N, norm_dtype dtype,
+                   cudaStream_t stream);
+
+/*
+ * RMSNorm backward ([Ch7] §7.7, last paragraph: one row sum). rstd is
+ * recomputed from x with `eps` (rms_fwd saves no statistics; x is in
+ * registers, so this costs no memory traffic):
+ *   rstd_r = 1 / sqrt(sum_j x_rj^2 / N + eps)
+ *   dx_ri  = rstd_r * w_i * dy_ri - x_ri * rstd_r^3 * sum_j dy_rj w_j x_rj / N
+ *   dw_i   = sum_r dy_ri * x_ri * rstd_r            (fp32 [N])
+ * Layout, workspace, aliasing and limits as for ln_bwd.
+ */
+norm_status rms_bwd(const void* dy, const void* x, const void* w, void* dx, float* dw,
+                    void* workspace, size_t workspace_bytes, int64_t M, int64_t N, float eps,
+                    norm_dtype dtype, cudaStream_t stream);
+
+/*
+ * The backward plan for M rows of N elements (`layer_norm` != 0 for ln_bwd)
+ * on a device with `num_sms` SMs; host only. In a backward plan `cluster`
+ * CTAs cover a row in one pass (rounds = 1) and `group` is the launched
+ * cluster size: equal to `cluster` when a row spans several CTAs, otherwise
+ * the number of CTAs (each on its own rows) whose column sums are added in
+ * distributed shared memory before one partial row goes to the workspace.
+ * At most `grid` CTAs walk the rows in a grid-stride loop: the launch takes
+ * no more than can be resident on the device at once (0 when M == 0).
+ * Returns NORM_ERR_ARG for rows beyond the backward's limit.
+ */
+norm_status norm_bwd_make_plan(int64_t M, int64_t N, norm_dtype dtype, int layer_norm,
+                               int aligned16, int num_sms, norm_plan* plan);
+
+/* Workspace bytes a backward plan needs: (grid / group) partial rows of N
+ * fp32 values, two arrays for LayerNorm, one for RMSNorm. Host only. */
+norm_status norm_bwd_workspace_bytes(const norm_plan* plan, int64_t N, int layer_norm,
+                                     size_t* bytes);
+
+/* The backward with an explicit plan (checked on the host as above;
+ * NORM_ERR_PLAN if it does not fit the call). */
+norm_status ln_bwd_planned(const void* dy, const void* x, const void* gamma, const float* mean,
+                           const float* rstd, void* dx, float* dgamma, float* dbeta,
+                           void* workspace, size_t workspace_bytes, int64_t M, int64_t N,
+                           norm_dtype dtype, cudaStream_t stream, const norm_plan* plan);
+
+norm_status rms_bwd_planned(const void* dy, const void* x, const void* w, void* dx, float* dw,
+                            void* workspace, size_t workspace_bytes, int64_t M, int64_t N,
+                            float eps, norm_dtype dtype, cudaStream_t stream,
+                            const norm_plan* plan);
 
 /* Static description of a status code. */
 const char* norm_status_string(norm_status status);

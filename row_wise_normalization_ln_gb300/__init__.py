@@ -17,7 +17,7 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "ln_fwd", "rms_fwd", "ln_fwd_add", "rms_fwd_add", "make_plan", "NormPlan", "NormError", "LibraryNotBuilt", "library",
+    "ln_fwd", "rms_fwd", "ln_fwd_add", "rms_fwd_add", "ln_bwd", "rms_bwd", "make_plan", "make_bwd_plan", "NormPlan", "NormError", "LibraryNotBuilt", "library",
     "NORM_F32", "NORM_BF16", "NORM_MAP_GROUP", "NORM_MAP_CTA",
 ]
 
@@ -90,8 +90,17 @@ def library() -> ctypes.CDLL:
     L.rms_fwd_add_planned.argtypes = L.rms_fwd_add.argtypes + [ctypes.POINTER(NormPlan)]
     L.norm_make_plan.argtypes = [i64, i64, i32, i32, i32, ctypes.POINTER(NormPlan)]
     L.norm_make_plan_add.argtypes = L.norm_make_plan.argtypes
+    sz = ctypes.c_size_t
+    L.ln_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i64, i64, i32, vp]
+    L.rms_bwd.argtypes = [vp, vp, vp, vp, vp, vp, sz, i64, i64, f32, i32, vp]
+    L.ln_bwd_planned.argtypes = L.ln_bwd.argtypes + [ctypes.POINTER(NormPlan)]
+    L.rms_bwd_planned.argtypes = L.rms_bwd.argtypes + [ctypes.POINTER(NormPlan)]
+    L.norm_bwd_make_plan.argtypes = [i64, i64, i32, i32, i32, i32, ctypes.POINTER(NormPlan)]
+    L.norm_bwd_workspace_bytes.argtypes = [ctypes.POINTER(NormPlan), i64, i32, ctypes.POINTER(sz)]
     for f in ("ln_fwd", "rms_fwd", "ln_fwd_planned", "rms_fwd_planned", "ln_fwd_add", "rms_fwd_add",
               "ln_fwd_add_planned", "rms_fwd_add_planned", "norm_make_plan", "norm_make_plan_add",
+              "ln_bwd", "rms_bwd", "ln_bwd_planned", "rms_bwd_planned", "norm_bwd_make_plan",
+              "norm_bwd_workspace_bytes",
               "norm_last_cuda_error", "norm_abi_version"):
         getattr(L, f).restype = ctypes.c_int
     L.norm_status_string.argtypes = [ctypes.c_int]
@@ -118,6 +127,26 @@ def make_plan(M: int, N: int, dtype: torch.dtype, aligned: bool = True, num_sms:
     if st != NORM_OK:
         raise NormError(st, "norm_make_plan")
     return p.as_dict()
+
+
+def make_bwd_plan(M: int, N: int, dtype: torch.dtype, layer_norm: bool, aligned: bool = True,
+                  num_sms: int = 152) -> dict:
+    """The backward plan ln_bwd / rms_bwd would choose (host-only)."""
+    p = NormPlan()
+    st = library().norm_bwd_make_plan(M, N, _dtype_code(dtype), int(layer_norm), int(aligned), num_sms,
+                                      ctypes.byref(p))
+    if st != NORM_OK:
+        raise NormError(st, "norm_bwd_make_plan")
+    return p.as_dict()
+
+
+def bwd_workspace_bytes(plan, N: int, layer_norm: bool) -> int:
+    n = ctypes.c_size_t()
+    p = plan if isinstance(plan, NormPlan) else NormPlan.from_dict(plan)
+    st = library().norm_bwd_workspace_bytes(ctypes.byref(p), N, int(layer_norm), ctypes.byref(n))
+    if st != NORM_OK:
+        raise NormError(st, "norm_bwd_workspace_bytes")
+    return n.value
 
 
 def _rows(x: torch.Tensor) -> torch.Tensor:
@@ -276,3 +305,76 @@ def rms_fwd_add(x: torch.Tensor, residual: torch.Tensor, w: torch.Tensor, eps: f
     if st != NORM_OK:
         raise NormError(st, "rms_fwd_add")
     return hh.view(x.shape), y.view(x.shape)
+
+
+def _aligned16(*ts) -> bool:
+    return all(t.data_ptr() % 16 == 0 for t in ts)
+
+
+def _bwd_common(dy, x, w, layer_norm, dx, workspace, plan):
+    if not x.is_cuda:
+        raise ValueError("the backward needs CUDA tensors")
+    code = _dtype_code(x.dtype)
+    if dy.shape != x.shape or dy.dtype != x.dtype or dy.device != x.device:
+        raise ValueError("dy must have x's shape, dtype and device")
+    x2, dy2 = _rows(x), _rows(dy)
+    M, N = x2.shape
+    wv = _param(w, x, "gamma" if layer_norm else "w")
+    dxt = _out(dx, x, x2, "dx")
+    if plan is None:
+        sms = torch.cuda.get_device_properties(x.device).multi_processor_count
+        pl = make_bwd_plan(M, N, x.dtype, layer_norm, _aligned16(x2, dy2, wv, dxt), sms)
+    else:
+        pl = dict(plan)
+    need = bwd_workspace_bytes(pl, N, layer_norm)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16) // 4 + 4, dtype=torch.float32, device=x.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    return code, x2, dy2, M, N, wv, dxt, workspace, nbytes
+
+
+def ln_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean: torch.Tensor, rstd: torch.Tensor, *,
+           dx: Optional[torch.Tensor] = None, dgamma: Optional[torch.Tensor] = None,
+           dbeta: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+           stream: Optional[torch.cuda.Stream] = None, plan=None):
+    """LayerNorm backward: returns ``(dx, dgamma, dbeta)``; dgamma and dbeta
+    are fp32 ``[N]``. ``mean``/``rstd`` are ln_fwd's fp32 statistics.
+    ``workspace`` (a CUDA tensor, any dtype) is allocated when not given."""
+    code, x2, dy2, M, N, g, dxt, ws, nbytes = _bwd_common(dy, x, gamma, True, dx, workspace, plan)
+    for t, n in ((mean, "mean"), (rstd, "rstd")):
+        if t.dtype != torch.float32 or t.numel() != M or not t.is_contiguous() or t.device != x.device:
+            raise ValueError(f"{n} must be a contiguous fp32 CUDA tensor of {M} elements")
+    dg = dgamma if dgamma is not None else torch.empty(N, dtype=torch.float32, device=x.device)
+    db = dbeta if dbeta is not None else torch.empty(N, dtype=torch.float32, device=x.device)
+    for t, n in ((dg, "dgamma"), (db, "dbeta")):
+        if t.dtype != torch.float32 or t.numel() != N or not t.is_contiguous() or t.device != x.device:
+            raise ValueError(f"{n} must be a contiguous fp32 CUDA tensor of {N} elements")
+    L = library()
+    args = (dy2.data_ptr(), x2.data_ptr(), g.data_ptr(), mean.data_ptr(), rstd.data_ptr(), dxt.data_ptr(),
+            dg.data_ptr(), db.data_ptr(), ws.data_ptr(), nbytes, M, N, code)
+    with torch.cuda.device(x.device):
+        s = _stream_handle(stream, x.device)
+        st = L.ln_bwd(*args, s) if plan is None else L.ln_bwd_planned(*args, s, _plan_ptr(plan))
+    if st != NORM_OK:
+        raise NormError(st, "ln_bwd")
+    return dxt.view(x.shape), dg, db
+
+
+def rms_bwd(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6, *,
+            dx: Optional[torch.Tensor] = None, dw: Optional[torch.Tensor] = None,
+            workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None, plan=None):
+    """RMSNorm backward: returns ``(dx, dw)``, dw fp32 ``[N]``; rstd is
+    recomputed from x with ``eps`` (the forward's)."""
+    code, x2, dy2, M, N, wv, dxt, ws, nbytes = _bwd_common(dy, x, w, False, dx, workspace, plan)
+    dwt = dw if dw is not None else torch.empty(N, dtype=torch.float32, device=x.device)
+    if dwt.dtype != torch.float32 or dwt.numel() != N or not dwt.is_contiguous() or dwt.device != x.device:
+        raise ValueError(f"dw must be a contiguous fp32 CUDA tensor of {N} elements")
+    L = library()
+    args = (dy2.data_ptr(), x2.data_ptr(), wv.data_ptr(), dxt.data_ptr(), dwt.data_ptr(), ws.data_ptr(), nbytes,
+            M, N, float(eps), code)
+    with torch.cuda.device(x.device):
+        s = _stream_handle(stream, x.device)
+        st = L.rms_bwd(*args, s) if plan is None else L.rms_bwd_planned(*args, s, _plan_ptr(plan))
+    if st != NORM_OK:
+        raise NormError(st, "rms_bwd")
+    return dxt.view(x.shape), dwt

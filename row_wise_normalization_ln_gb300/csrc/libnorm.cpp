@@ -158,6 +158,96 @@ norm_status check_plan(const norm_plan& in, int64_t N, norm_dtype dtype, bool al
     return NORM_OK;
 }
 
+// ------------------------------------------------------------ backward plans
+// A backward plan covers a row in one register round: `cluster` CTAs of
+// `threads` threads with `per_thread` accesses each. `group` is the launched
+// cluster size: equal to `cluster` when a row spans several CTAs; otherwise
+// the number of CTAs (each on its own rows) whose column accumulators are
+// added through distributed shared memory before one partial row is
+// written. `grid` is an upper bound on the CTAs launched (the launch takes
+// no more than fit on the device at once); the workspace holds grid / group
+// partial rows.
+constexpr int kBwdMaxThreads = libnorm::kBwdMaxThreads;
+
+int bwd_vmax(bool ln, norm_dtype dtype, int vec) {
+    return vec == 1 ? 8 : (ln && elem_size(dtype) == 2) ? 2 : 4;
+}
+
+norm_status bwd_make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_aligned, int num_sms, bool ln,
+                          norm_plan* p) {
+    std::memset(p, 0, sizeof *p);
+    const int vec = vec_for(N, dtype, all_aligned);
+    const int64_t nacc = ceil_div(N, vec);
+    int per = bwd_vmax(ln, dtype, vec);
+    int64_t cluster = 1;
+    int64_t threads = round_up(ceil_div(nacc, per), 32);
+    while (threads > kBwdMaxThreads && cluster < kMaxCluster) {
+        cluster *= 2;
+        threads = round_up(ceil_div(nacc, cluster * per), 32);
+    }
+    if (threads > kBwdMaxThreads) return NORM_ERR_ARG;  // the row does not fit one round of a cluster
+    // Rows of 512 to 1024 accesses: 512 threads of half the registers each
+    // (measured faster than 256 threads of full ones).
+    while (cluster == 1 && per > 1 && threads <= 256 && nacc >= 512) {
+        per /= 2;
+        threads = round_up(ceil_div(nacc, per), 32);
+    }
+    while (per > 1 && threads < 64) {
+        per /= 2;
+        threads = round_up(ceil_div(nacc, cluster * per), 32);
+    }
+    p->mapping = NORM_MAP_CTA;
+    p->vec_elems = vec;
+    p->per_thread = per;
+    p->threads = static_cast<int32_t>(threads);
+    p->cluster = static_cast<int32_t>(cluster);
+    p->rounds = 1;
+    // Persistent grid of at most 1024 threads and 6 CTAs per SM in whole
+    // clusters (the launch takes fewer if fewer fit at once). CTAs that each take their own
+    // rows add their column sums in clusters of 2 (of 8 for small CTAs, many
+    // of which share an SM): the partial rows halve, and such clusters are
+    // easy to place.
+    const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>(6, 1024 / threads));
+    if (cluster > 1) {
+        const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(M, num_sms * per_sm / cluster));
+        p->group = static_cast<int32_t>(cluster);
+        p->grid = M > 0 ? clusters * cluster : 0;
+    } else {
+        const int64_t ctas = std::min<int64_t>(M, num_sms * per_sm);
+        const int64_t want = threads <= 128 ? kMaxCluster : 2;
+        const int64_t q = std::min<int64_t>(want, pow2_ceil(std::max<int64_t>(ctas, 1)));
+        p->group = static_cast<int32_t>(q);
+        p->grid = M > 0 ? round_up(ctas, q) : 0;
+    }
+    return NORM_OK;
+}
+
+norm_status bwd_check_plan(const norm_plan& in, int64_t M, int64_t N, norm_dtype dtype, bool all_aligned, bool ln,
+                           norm_plan* out) {
+    norm_plan p = in;
+    const int s = elem_size(dtype);
+    if (p.mapping != NORM_MAP_CTA || p.stages != 0) return NORM_ERR_PLAN;
+    if (p.vec_elems != 1) {
+        if (p.vec_elems != 16 / s || !all_aligned || (N * s) % 16 != 0) return NORM_ERR_PLAN;
+    }
+    if (!is_pow2(p.per_thread) || p.per_thread > bwd_vmax(ln, dtype, p.vec_elems)) return NORM_ERR_PLAN;
+    if (p.threads < 32 || p.threads > kBwdMaxThreads || p.threads % 32 != 0) return NORM_ERR_PLAN;
+    if (!is_pow2(p.cluster) || p.cluster > kMaxCluster) return NORM_ERR_PLAN;
+    if (!is_pow2(p.group) || p.group > kMaxCluster) return NORM_ERR_PLAN;
+    if (p.cluster > 1 && p.group != p.cluster) return NORM_ERR_PLAN;
+    const int64_t nacc = ceil_div(N, p.vec_elems);
+    if (int64_t(p.cluster) * p.threads * p.per_thread < nacc) return NORM_ERR_PLAN;  // one round only
+    if (M > 0 && (p.grid < p.group || p.grid > kMaxGrid || p.grid % p.group != 0)) return NORM_ERR_PLAN;
+    p.rounds = 1;
+    if (M == 0) p.grid = 0;
+    *out = p;
+    return NORM_OK;
+}
+
+size_t bwd_workspace(const norm_plan& p, int64_t N, bool ln) {
+    return static_cast<size_t>(libnorm::bwd_partials(p)) * (ln ? 2 : 1) * static_cast<size_t>(N) * sizeof(float);
+}
+
 // SM count of the current device (cached per device); `dev` receives the
 // device ordinal.
 int device_sm_count(int* dev_out) {
@@ -271,9 +361,97 @@ norm_status rms_add_impl(const void* x, const void* res, const void* w, void* h,
     return run(false, a, dtype, al, stream, plan);
 }
 
+// Backward: dx = d(loss)/dx for y = norm(x); column gradients in fp32.
+norm_status bwd_impl(bool ln, const void* dy, const void* x, const void* gamma, const float* mean, const float* rstd,
+                     void* dx, float* dgamma, float* dbeta, void* ws, size_t ws_bytes, int64_t M, int64_t N,
+                     float eps, norm_dtype dtype, cudaStream_t stream, const norm_plan* user_plan) {
+    norm_status st = check_sizes(M, N, dtype);
+    if (st != NORM_OK) return st;
+    if (!std::isfinite(eps) || eps < 0.f) return NORM_ERR_ARG;
+    if (!dgamma || (ln && !dbeta)) return NORM_ERR_ARG;
+    if (M > 0 && (!dy || !x || !gamma || !dx || (ln && (!mean || !rstd)))) return NORM_ERR_ARG;
+    const bool al = aligned16(dy) && aligned16(x) && aligned16(gamma) && aligned16(dx);
+    {
+        norm_plan probe;  // rows beyond the backward's limit fail here, before any CUDA call
+        st = bwd_make_plan(M, N, dtype, al, 1, ln, &probe);
+        if (st != NORM_OK) return st;
+    }
+    auto ws_ok = [&](const norm_plan& pl) {
+        const size_t need = bwd_workspace(pl, N, ln);
+        return need == 0 || (ws && ws_bytes >= need && (reinterpret_cast<uintptr_t>(ws) & 15u) == 0);
+    };
+    norm_plan plan;
+    if (user_plan) {
+        st = bwd_check_plan(*user_plan, M, N, dtype, al, ln, &plan);
+        if (st != NORM_OK) return st;
+        if (!ws_ok(plan)) return NORM_ERR_ARG;
+    }
+    int dev = 0;
+    const int sms = device_sm_count(&dev);
+    if (sms <= 0) return NORM_ERR_CUDA;
+    if (!user_plan) {
+        st = bwd_make_plan(M, N, dtype, al, sms, ln, &plan);
+        if (st != NORM_OK) return st;
+        if (!ws_ok(plan)) return NORM_ERR_ARG;
+    }
+    libnorm::BwdArgs a{dy, x, gamma, mean, rstd, dx, static_cast<float*>(ws), dgamma, dbeta, M,
+                       static_cast<int32_t>(N), eps, plan.cluster};
+    const bool f32 = dtype == NORM_F32;
+    const cudaError_t e = ln ? (f32 ? libnorm::launch_ln_bwd_f32(plan, a, stream, dev, sms)
+                                    : libnorm::launch_ln_bwd_bf16(plan, a, stream, dev, sms))
+                             : (f32 ? libnorm::launch_rms_bwd_f32(plan, a, stream, dev, sms)
+                                    : libnorm::launch_rms_bwd_bf16(plan, a, stream, dev, sms));
+    if (e != cudaSuccess) {
+        g_last_cuda_error = static_cast<int>(e);
+        return NORM_ERR_CUDA;
+    }
+    return NORM_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+norm_status ln_bwd(const void* dy, const void* x, const void* gamma, const float* mean, const float* rstd, void* dx,
+                   float* dgamma, float* dbeta, void* workspace, size_t workspace_bytes, int64_t M, int64_t N,
+                   norm_dtype dtype, cudaStream_t stream) {
+    return bwd_impl(true, dy, x, gamma, mean, rstd, dx, dgamma, dbeta, workspace, workspace_bytes, M, N, 0.f, dtype,
+                    stream, nullptr);
+}
+
+norm_status rms_bwd(const void* dy, const void* x, const void* w, void* dx, float* dw, void* workspace,
+                    size_t workspace_bytes, int64_t M, int64_t N, float eps, norm_dtype dtype, cudaStream_t stream) {
+    return bwd_impl(false, dy, x, w, nullptr, nullptr, dx, dw, nullptr, workspace, workspace_bytes, M, N, eps, dtype,
+                    stream, nullptr);
+}
+
+norm_status ln_bwd_planned(const void* dy, const void* x, const void* gamma, const float* mean, const float* rstd,
+                           void* dx, float* dgamma, float* dbeta, void* workspace, size_t workspace_bytes, int64_t M,
+                           int64_t N, norm_dtype dtype, cudaStream_t stream, const norm_plan* plan) {
+    return bwd_impl(true, dy, x, gamma, mean, rstd, dx, dgamma, dbeta, workspace, workspace_bytes, M, N, 0.f, dtype,
+                    stream, plan);
+}
+
+norm_status rms_bwd_planned(const void* dy, const void* x, const void* w, void* dx, float* dw, void* workspace,
+                            size_t workspace_bytes, int64_t M, int64_t N, float eps, norm_dtype dtype,
+                            cudaStream_t stream, const norm_plan* plan) {
+    return bwd_impl(false, dy, x, w, nullptr, nullptr, dx, dw, nullptr, workspace, workspace_bytes, M, N, eps, dtype,
+                    stream, plan);
+}
+
+norm_status norm_bwd_make_plan(int64_t M, int64_t N, norm_dtype dtype, int layer_norm, int aligned, int num_sms,
+                               norm_plan* plan) {
+    const norm_status st = check_sizes(M, N, dtype);
+    if (st != NORM_OK) return st;
+    if (!plan || num_sms < 1) return NORM_ERR_ARG;
+    return bwd_make_plan(M, N, dtype, aligned != 0, num_sms, layer_norm != 0, plan);
+}
+
+norm_status norm_bwd_workspace_bytes(const norm_plan* plan, int64_t N, int layer_norm, size_t* bytes) {
+    if (!plan || !bytes || N < 1 || N > kMaxN || plan->group < 1 || plan->grid < 0) return NORM_ERR_ARG;
+    *bytes = bwd_workspace(*plan, N, layer_norm != 0);
+    return NORM_OK;
+}
 
 norm_status ln_fwd(const void* x, const void* gamma, const void* beta, void* y, float* mean, float* rstd,
                    int64_t M, int64_t N, float eps, norm_dtype dtype, cudaStream_t stream) {

@@ -1,0 +1,10 @@
+// LayerNorm backward kernels, f32 rows.
+#include "norm_bwd.cuh"
+
+namespace libnorm {
+
+cudaError_t launch_ln_bwd_f32(const norm_plan& plan, const BwdArgs& a, cudaStream_t s, int dev, int num_sms) {
+    return launch_norm_bwd<float, true>(plan, a, s, dev, num_sms);
+}
+
+}  // namespace libnorm

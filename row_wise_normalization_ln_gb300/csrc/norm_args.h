@@ -31,6 +31,38 @@ struct NormArgs {
     int32_t stages;     // pipelined CTA mapping: shared-memory ring stages
 };
 
+// Backward pass. A CTA (row_cluster == 1) or a cluster of row_cluster CTAs
+// owns one row at a time; each thread accumulates the column gradients of
+// its own columns over the rows it visits. Those accumulators leave through
+// `ws` as partial rows [partials][narr][N] (narr = 2 for LayerNorm: dgamma,
+// dbeta; 1 for RMSNorm: dw), which a second kernel sums in a fixed order.
+struct BwdArgs {
+    const void* dy;       // [M, N]
+    const void* x;        // [M, N]
+    const void* gamma;    // [N] (LayerNorm gamma, RMSNorm w)
+    const float* mean;    // [M] (LayerNorm)
+    const float* rstd;    // [M] (LayerNorm)
+    void* dx;             // [M, N]
+    float* ws;            // [partials][narr][N]
+    float* dgamma;        // [N] (LayerNorm dgamma, RMSNorm dw)
+    float* dbeta;         // [N] (LayerNorm)
+    int64_t M;
+    int32_t N;
+    float eps;            // RMSNorm (rstd is recomputed from x)
+    int32_t row_cluster;  // CTAs per row
+};
+
+constexpr int kBwdMaxThreads = 512;
+
+// Partial rows of the column gradients a backward plan produces (one per
+// cluster, or per CTA without clusters).
+inline int64_t bwd_partials(const norm_plan& p) { return p.group > 0 ? p.grid / p.group : 0; }
+
+cudaError_t launch_ln_bwd_f32(const norm_plan& plan, const BwdArgs& a, cudaStream_t s, int dev, int num_sms);
+cudaError_t launch_ln_bwd_bf16(const norm_plan& plan, const BwdArgs& a, cudaStream_t s, int dev, int num_sms);
+cudaError_t launch_rms_bwd_f32(const norm_plan& plan, const BwdArgs& a, cudaStream_t s, int dev, int num_sms);
+cudaError_t launch_rms_bwd_bf16(const norm_plan& plan, const BwdArgs& a, cudaStream_t s, int dev, int num_sms);
+
 // Launch the kernel variant `plan` names on the current device `dev` (with
 // `num_sms` SMs). The plan has been validated; a pipelined plan with grid 0
 // gets a persistent grid sized by occupancy.

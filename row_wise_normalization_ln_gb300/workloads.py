@@ -21,6 +21,9 @@ Workloads (shapes and value distributions of the source pages):
   add_*                    the fused residual add + norm on the shape and
                            recipe of the workload it names: the residual r is
                            drawn from the same recipe, after the parameters.
+  bwd_*                    the backward on the shape and recipe of the
+                           workload it names: the upstream gradient
+                           dy ~ N(0,1) is drawn after the parameters.
 """
 from __future__ import annotations
 
@@ -39,6 +42,7 @@ class Workload:
     eps: float
     recipe: str    # key of the value distribution below
     add: bool = False  # fused residual add: h = x + r, y = norm(h)
+    bwd: bool = False  # backward: dx (and the column gradients) from dy, x
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -50,21 +54,29 @@ class Workload:
 
     @property
     def row_tensors(self) -> int:
-        """[M, N] tensors one call moves: x, y; with the fused add also r, h."""
-        return 4 if self.add else 2
+        """[M, N] tensors one call moves: x, y; with the fused add also r, h;
+        backward: dy, x, dx."""
+        return 4 if self.add else 3 if self.bwd else 2
 
     def algorithmic_bytes(self, M: int | None = None) -> int:
-        """HBM bytes one forward call must move: read x (and r), write y (and
-        h), read the per-column parameters, write 8 B of statistics per row
-        (LayerNorm)."""
+        """HBM bytes one call must move. Forward: read x (and r), write y
+        (and h), read the per-column parameters, write 8 B of statistics per
+        row (LayerNorm). Backward: read dy and x, write dx, read gamma (w)
+        and, for LayerNorm, the 8 B of statistics per row; write the fp32
+        column gradients (dgamma and dbeta, or dw)."""
         M = self.M if M is None else M
         s = self.elem_size
+        if self.bwd:
+            stats = 8 * M if self.op == "ln" else 0
+            cols = (2 if self.op == "ln" else 1) * 4 * self.N
+            return 3 * M * self.N * s + self.N * s + stats + cols
         params = 2 if self.op == "ln" else 1
         stats = 8 * M if self.op == "ln" else 0
         return self.row_tensors * M * self.N * s + params * self.N * s + stats
 
     def scaled(self, M: int | None = None, N: int | None = None) -> "Workload":
-        return Workload(self.name, self.op, self.dtype, M or self.M, N or self.N, self.eps, self.recipe, self.add)
+        return Workload(self.name, self.op, self.dtype, M or self.M, N or self.N, self.eps, self.recipe, self.add,
+                        self.bwd)
 
 
 WORKLOADS = {
@@ -80,6 +92,11 @@ WORKLOADS = {
         Workload("add_rms_bf16_65536x2048", "rms", "bf16", 65536, 2048, 1e-6, "uniform_pm1", True),
         Workload("add_ln_bf16_4096x8192_outliers", "ln", "bf16", 4096, 8192, 1e-5, "offset_outliers", True),
         Workload("add_ln_f32_2048x65536", "ln", "f32", 2048, 65536, 1e-5, "normal31", True),
+        Workload("bwd_rms_f32_8192x4096", "rms", "f32", 8192, 4096, 1e-6, "uniform_pm1", bwd=True),
+        Workload("bwd_ln_bf16_4096x8192_outliers", "ln", "bf16", 4096, 8192, 1e-5, "offset_outliers", bwd=True),
+        Workload("bwd_rms_bf16_65536x2048", "rms", "bf16", 65536, 2048, 1e-6, "uniform_pm1", bwd=True),
+        Workload("bwd_ln_f32_8192x5000", "ln", "f32", 8192, 5000, 1e-5, "normal31", bwd=True),
+        Workload("bwd_ln_f32_2048x65536", "ln", "f32", 2048, 65536, 1e-5, "normal31", bwd=True),
     ]
 }
 
@@ -106,8 +123,9 @@ def _draw(recipe: str, M: int, N: int, g: torch.Generator) -> torch.Tensor:
 
 def generate(w: Workload, seed: int = 0) -> dict[str, torch.Tensor]:
     """CPU tensors for one workload: {"x", "gamma", "beta"} (LayerNorm) or
-    {"x", "w"} (RMSNorm), plus "r" for the fused add, all in the workload's
-    dtype, drawn in a fixed order from one seeded CPU generator."""
+    {"x", "w"} (RMSNorm), plus "r" for the fused add and "dy" for the
+    backward, all in the workload's dtype, drawn in a fixed order from one
+    seeded CPU generator."""
     g = torch.Generator().manual_seed(seed)
     M, N = w.M, w.N
     out = {"x": _draw(w.recipe, M, N, g)}
@@ -118,6 +136,8 @@ def generate(w: Workload, seed: int = 0) -> dict[str, torch.Tensor]:
         out["w"] = torch.rand(N, generator=g)
     if w.add:
         out["r"] = _draw(w.recipe, M, N, g)
+    if w.bwd:
+        out["dy"] = torch.randn(M, N, generator=g)
     return {k: v.to(w.torch_dtype).contiguous() for k, v in out.items()}
 
 

@@ -167,3 +167,96 @@ def sample_rows(M: int, k: int = 48, seed: int = 0) -> np.ndarray:
     rng = np.random.default_rng(seed)
     pick = set(rng.choice(M, size=min(k, M), replace=False).tolist()) | {0, M - 1}
     return np.array(sorted(pick))
+
+
+# ---------------------------------------------------------------- backward
+#
+# dx (per row, u = 2^-24). The kernel forms the two row sums in fp32 with
+# at most 64 sequential additions on any path (per-thread runs of <= 32
+# elements, then <= 12 tree levels), so each sum is off by <= 64u of the sum
+# of its absolute terms; xhat is formed from the fp32 mean and rstd, off by
+# <= 2u (|xhat| + |mean| rstd). Propagating through
+# dx = rstd (g - gbar - xhat * gxbar), with G = max|g|, X = max|xhat| +
+# |mean| rstd, bounds the error by about u rstd G (67 + 68 X^2); the tests
+# allow twice that: 2^-17 rstd G (1 + X^2).
+# RMSNorm: dx = r w dy - x r^3 S / N with r from a sum of squares (<= 36u
+# relative after rsqrt) and S off by <= 64u sum|g x|: <= 36u r G + 166u
+# max|x| r^3 mean|g x|; allowed 2^-17 r G + 2^-15 max|x| r^3 mean|g x|.
+# bf16 dx: one bf16 ulp of the rounded oracle value, or the fp32 bound.
+# Column gradients: a sum over rows in fp32 along a chain of at most
+# rows-per-CTA + 8 + partial-rows <= 2M + 8 additions: allowed
+# 2^-24 (2M + 64) sum|terms| (+ the xhat error of each term for dgamma, and
+# the rstd error for dw).
+
+def _dx_check(dx_gpu: np.ndarray, dx_ref: np.ndarray, tol_rows: np.ndarray) -> dict:
+    if dx_gpu.dtype == np.float32:
+        err = np.abs(dx_gpu.astype(np.float64) - dx_ref)
+        assert np.all(np.isfinite(dx_gpu)), "non-finite dx"
+        ratio = err / tol_rows[:, None]
+        assert (ratio <= 1).all(), f"dx off by {float(ratio.max()):.2f} x the bound"
+        return {"dx_worst_of_bound": float(ratio.max()) if ratio.size else 0.0}
+    ref_b = as_f64(oracle.round_bf16(dx_ref))
+    diff = np.abs(as_f64(dx_gpu) - ref_b)
+    ulp = ulp_bf16(ref_b)
+    bad = diff > np.maximum(ulp, tol_rows[:, None])
+    assert not bad.any(), f"{int(bad.sum())} bf16 dx off by more than 1 ulp and the fp32 bound"
+    return {"dx_exact": int((diff == 0).sum()), "dx_n": int(diff.size)}
+
+
+def _col_check(got: np.ndarray, ref: np.ndarray, tol: np.ndarray, name: str) -> float:
+    err = np.abs(got.astype(np.float64) - ref)
+    ratio = err / np.where(tol > 0, tol, 1e-300)
+    assert (err <= tol).all(), f"{name} off by {float(ratio.max()):.2f} x the bound"
+    return float(ratio.max()) if ratio.size else 0.0
+
+
+def check_ln_bwd(dy, x, gamma, eps, dx, dgamma, dbeta, rows=None) -> dict:
+    """dy, x, gamma: CPU tensors given to the kernel (with the forward's
+    statistics for `eps`); dx, dgamma, dbeta: its outputs. The column
+    gradients are checked over all rows; `rows` restricts the dx check."""
+    dyn, xn, gn = np_of(dy), np_of(x), np_of(gamma)
+    M, N = xn.shape
+    e = oracle.eps_as_f32(eps)
+    dx_ref, dg_ref, db_ref = oracle.ln_bwd(dyn, xn, gn, e)
+    _, mean, rstd = oracle.ln_fwd(xn, gn, gn, e)
+    x64, dy64, g64 = as_f64(xn), as_f64(dyn), as_f64(gn)
+    xh = (x64 - mean[:, None]) * rstd[:, None]
+    X = np.abs(xh).max(axis=1) + np.abs(mean) * rstd
+    G = np.abs(dy64 * g64[None, :]).max(axis=1)
+    tol_rows = 2.0 ** -17 * rstd * G * (1 + X * X)
+    dxn = np_of(dx)
+    if rows is not None:
+        dxn, dx_ref, tol_rows = dxn[rows], dx_ref[rows], tol_rows[rows]
+    res = _dx_check(dxn, dx_ref, tol_rows)
+    u = 2.0 ** -24
+    tol_g = u * ((2 * M + 64) * np.abs(dy64 * xh).sum(axis=0) + 4 * (np.abs(dy64) * X[:, None]).sum(axis=0))
+    tol_b = u * (2 * M + 64) * np.abs(dy64).sum(axis=0)
+    res["dgamma_worst_of_bound"] = _col_check(np_of(dgamma), dg_ref, tol_g, "dgamma")
+    res["dbeta_worst_of_bound"] = _col_check(np_of(dbeta), db_ref, tol_b, "dbeta")
+    return res
+
+
+def ln_stats_f32(x, gamma, eps):
+    """The oracle's mean and rstd of each row, rounded to fp32 (CPU tensors),
+    as inputs for the backward."""
+    _, mean, rstd = oracle.ln_fwd(np_of(x), np_of(gamma), np_of(gamma), oracle.eps_as_f32(eps))
+    return torch.from_numpy(oracle.round_f32(mean)), torch.from_numpy(oracle.round_f32(rstd))
+
+
+def check_rms_bwd(dy, x, w, eps, dx, dw, rows=None) -> dict:
+    dyn, xn, wn = np_of(dy), np_of(x), np_of(w)
+    M, N = xn.shape
+    e = oracle.eps_as_f32(eps)
+    dx_ref, dw_ref = oracle.rms_bwd(dyn, xn, wn, e)
+    _, r = oracle.rms_fwd(xn, wn, e)
+    x64, dy64, w64 = as_f64(xn), as_f64(dyn), as_f64(wn)
+    g = dy64 * w64[None, :]
+    G = np.abs(g).max(axis=1)
+    tol_rows = 2.0 ** -17 * r * G + 2.0 ** -15 * np.abs(x64).max(axis=1) * r ** 3 * np.abs(g * x64).mean(axis=1)
+    dxn = np_of(dx)
+    if rows is not None:
+        dxn, dx_ref, tol_rows = dxn[rows], dx_ref[rows], tol_rows[rows]
+    res = _dx_check(dxn, dx_ref, tol_rows)
+    tol_w = 2.0 ** -24 * (2 * M + 128) * np.abs(dy64 * x64 * r[:, None]).sum(axis=0)
+    res["dw_worst_of_bound"] = _col_check(np_of(dw), dw_ref, tol_w, "dw")
+    return res

@@ -32,6 +32,7 @@ def test_header_declares_the_abi():
     assert set(declared_functions()) == {
         "ln_fwd", "rms_fwd", "ln_fwd_planned", "rms_fwd_planned", "norm_make_plan",
         "ln_fwd_add", "rms_fwd_add", "ln_fwd_add_planned", "rms_fwd_add_planned", "norm_make_plan_add",
+        "ln_bwd", "rms_bwd", "ln_bwd_planned", "rms_bwd_planned", "norm_bwd_make_plan", "norm_bwd_workspace_bytes",
         "norm_status_string", "norm_last_cuda_error", "norm_abi_version"}
 
 
@@ -281,3 +282,113 @@ def test_binding_rejects_cpu_tensors():
         rn.ln_fwd_add(x, x, torch.ones(8), torch.zeros(8))
     with pytest.raises(ValueError):
         rn.rms_fwd_add(x, x, torch.ones(8))
+
+
+
+# ---------------------------------------------------------------- backward
+
+W = ctypes.c_void_p(0x100000)   # a fake 16-byte aligned workspace
+
+
+def _bwd_plan(**kw):
+    base = dict(mapping=rn.NORM_MAP_CTA, vec_elems=4, per_thread=4, group=8, threads=256, cluster=1, grid=16)
+    base.update(kw)
+    return rn.NormPlan.from_dict(base)
+
+
+def _ln_bwd(lib, M, N, dtype=rn.NORM_F32, ws=W, nbytes=1 << 30, plan=None, ptrs=None):
+    p = ptrs or [P] * 8
+    if plan is None:
+        return lib.ln_bwd(*p, ws, nbytes, M, N, dtype, None)
+    return lib.ln_bwd_planned(*p, ws, nbytes, M, N, dtype, None, ctypes.byref(plan))
+
+
+@pytest.mark.parametrize("M,N", [(-1, 8), (4, 0), (2 ** 62, 4)])
+def test_bwd_bad_sizes_rejected(lib, M, N):
+    assert _ln_bwd(lib, M, N) == rn.NORM_ERR_ARG
+    assert lib.rms_bwd(P, P, P, P, P, W, 1 << 30, M, N, 1e-6, rn.NORM_F32, None) == rn.NORM_ERR_ARG
+
+
+def test_bwd_rows_beyond_the_limit_rejected(lib):
+    """One register pass of an 8-CTA cluster: 65536 fp32 (LayerNorm and
+    RMSNorm), 65536 bf16 LayerNorm, 131072 bf16 RMSNorm, 32768 with element
+    accesses; refused on the host before any CUDA call."""
+    assert _ln_bwd(lib, 4, 65540) == rn.NORM_ERR_ARG
+    assert _ln_bwd(lib, 4, 65544, rn.NORM_BF16) == rn.NORM_ERR_ARG
+    assert lib.rms_bwd(P, P, P, P, P, W, 1 << 30, 4, 131080, 1e-6, rn.NORM_BF16, None) == rn.NORM_ERR_ARG
+    assert lib.rms_bwd(P, P, P, P, P, W, 1 << 30, 4, 32769, 1e-6, rn.NORM_F32, None) == rn.NORM_ERR_ARG
+    q = ctypes.c_void_p(0x1004)   # unaligned: element accesses
+    assert _ln_bwd(lib, 4, 32772, ptrs=[q] + [P] * 7) == rn.NORM_ERR_ARG
+    for N, dt, ln in ((65536, torch.float32, True), (65536, torch.bfloat16, True), (131072, torch.bfloat16, False),
+                      (65536, torch.float32, False)):
+        p = rn.make_bwd_plan(8, N, dt, ln, True, 152)
+        assert p["cluster"] == 8 and p["threads"] <= 512
+
+
+def test_bwd_null_pointers_rejected(lib):
+    for i in range(8):
+        ptrs = [P] * 8
+        ptrs[i] = None
+        assert _ln_bwd(lib, 4, 64, ptrs=ptrs) == rn.NORM_ERR_ARG
+    for i in range(5):
+        ptrs = [P] * 5
+        ptrs[i] = None
+        assert lib.rms_bwd(*ptrs, W, 1 << 30, 4, 64, 1e-6, rn.NORM_F32, None) == rn.NORM_ERR_ARG
+
+
+def test_bwd_workspace_checked_on_the_host(lib):
+    p = _bwd_plan()
+    need = rn.bwd_workspace_bytes(p, 1024, True)
+    assert need == (16 // 8) * 2 * 1024 * 4
+    assert rn.bwd_workspace_bytes(p, 1024, False) == need // 2
+    assert _ln_bwd(lib, 40, 1024, nbytes=need - 1, plan=p) == rn.NORM_ERR_ARG      # too small
+    assert _ln_bwd(lib, 40, 1024, ws=None, plan=p) == rn.NORM_ERR_ARG              # missing
+    assert _ln_bwd(lib, 40, 1024, ws=ctypes.c_void_p(0x100004), plan=p) == rn.NORM_ERR_ARG  # misaligned
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on the fake pointers")
+def test_bwd_valid_plan_passes_the_host_checks(lib):
+    p = _bwd_plan()
+    need = rn.bwd_workspace_bytes(p, 1024, True)
+    assert _ln_bwd(lib, 40, 1024, nbytes=need, plan=p) == rn.NORM_ERR_CUDA
+
+
+@pytest.mark.parametrize("kw", [
+    dict(mapping=rn.NORM_MAP_GROUP), dict(stages=2),
+    dict(vec_elems=8), dict(per_thread=8), dict(per_thread=3),
+    dict(threads=1024), dict(threads=48),
+    dict(cluster=3), dict(cluster=16), dict(group=16), dict(group=3),
+    dict(cluster=2, group=8),                   # a row cluster is the launched cluster
+    dict(grid=12),                              # not a multiple of the cluster
+    dict(threads=32, per_thread=1),             # 32*1*4 < 1024: does not cover the row in one pass
+])
+def test_bwd_bad_plans_rejected(lib, kw):
+    assert _ln_bwd(lib, 40, 1024, plan=_bwd_plan(**kw)) == rn.NORM_ERR_PLAN
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("ln", [True, False])
+@pytest.mark.parametrize("M", [0, 1, 3, 9, 4096, 65536])
+def test_bwd_plans_are_consistent(lib, dtype, ln, M):
+    s = 4 if dtype == torch.float32 else 2
+    limit = 65536 if (s == 4 or ln) else 131072
+    for N in NS + [limit]:
+        if N > limit:
+            continue
+        vec = 16 // s if (N * s) % 16 == 0 else 1
+        if vec == 1 and N > 32768:
+            with pytest.raises(rn.NormError):
+                rn.make_bwd_plan(M, N, dtype, ln, True, 152)
+            continue
+        p = rn.make_bwd_plan(M, N, dtype, ln, True, 152)
+        assert p["vec_elems"] == vec and p["rounds"] == 1 and p["stages"] == 0
+        assert p["cluster"] * p["threads"] * p["per_thread"] * vec >= N
+        assert p["threads"] % 32 == 0 and 32 <= p["threads"] <= 512
+        assert p["cluster"] in (1, 2, 4, 8) and p["group"] in (1, 2, 4, 8)
+        if p["cluster"] > 1:
+            assert p["group"] == p["cluster"]
+        if M == 0:
+            assert p["grid"] == 0 and rn.bwd_workspace_bytes(p, N, ln) == 0
+        else:
+            assert p["grid"] % p["group"] == 0 and p["grid"] >= p["group"]
+            assert rn.bwd_workspace_bytes(p, N, ln) == p["grid"] // p["group"] * (2 if ln else 1) * N * 4
