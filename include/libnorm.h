@@ -245,6 +245,32 @@ norm_status rms_bwd_planned(const void* dy, const void* x, const void* w, void* 
                             float eps, norm_dtype dtype, cudaStream_t stream,
                             const norm_plan* plan);
 
+/*
+ * ln_bwd for callers that cannot allocate device memory: the same result as
+ * ln_bwd, with no workspace argument. (The source pages have no counterpart;
+ * this is an interface convenience.) Such callers include inference and
+ * training runtimes that plan all device memory up front and forbid any
+ * allocation afterwards, code that cannot reach the framework's allocator,
+ * and latency-critical loops that cannot afford the device-wide
+ * synchronisation cudaFree may cause. The call allocates nothing: the
+ * backward's partial column sums go to one static device array of 4 MiB,
+ * which every GPU that loads this library holds until the process exits.
+ * The plan's grid is capped so that its partial rows (2 * N floats each)
+ * fit; a row whose single partial row would not fit (N > 524288, beyond the
+ * backward's own limits anyway) returns NORM_ERR_ARG, as do the sizes
+ * ln_bwd refuses.
+ * The first call on each device looks up that array's device address (with
+ * the device current) and the SM count; make that first call before any
+ * stream capture. Nothing in the array needs to start at zero: each call
+ * writes every partial row before reading it. All calls on a device share
+ * the array, so calls that overlap on the GPU (on different streams, or
+ * from different threads) race and corrupt each other's column gradients:
+ * serialise them.
+ */
+norm_status ln_bwd_noalloc(const void* dy, const void* x, const void* gamma, const float* mean,
+                           const float* rstd, void* dx, float* dgamma, float* dbeta, int64_t M,
+                           int64_t N, norm_dtype dtype, cudaStream_t stream);
+
 /* Static description of a status code. */
 const char* norm_status_string(norm_status status);
 

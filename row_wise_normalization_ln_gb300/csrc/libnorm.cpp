@@ -410,6 +410,8 @@ norm_status bwd_impl(bool ln, const void* dy, const void* x, const void* gamma, 
 
 }  // namespace
 
+void libnorm::note_cuda_error(int e) { g_last_cuda_error = e; }
+
 extern "C" {
 
 norm_status ln_bwd(const void* dy, const void* x, const void* gamma, const float* mean, const float* rstd, void* dx,

@@ -54,6 +54,9 @@ struct BwdArgs {
 
 constexpr int kBwdMaxThreads = 512;
 
+// Record a CUDA error for norm_last_cuda_error() on the calling thread.
+void note_cuda_error(int e);
+
 // Partial rows of the column gradients a backward plan produces (one per
 // cluster, or per CTA without clusters).
 inline int64_t bwd_partials(const norm_plan& p) { return p.group > 0 ? p.grid / p.group : 0; }

@@ -33,6 +33,7 @@ def test_header_declares_the_abi():
         "ln_fwd", "rms_fwd", "ln_fwd_planned", "rms_fwd_planned", "norm_make_plan",
         "ln_fwd_add", "rms_fwd_add", "ln_fwd_add_planned", "rms_fwd_add_planned", "norm_make_plan_add",
         "ln_bwd", "rms_bwd", "ln_bwd_planned", "rms_bwd_planned", "norm_bwd_make_plan", "norm_bwd_workspace_bytes",
+        "ln_bwd_noalloc",
         "norm_status_string", "norm_last_cuda_error", "norm_abi_version"}
 
 
