@@ -3,8 +3,8 @@
 TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
 and the CPU-baseline leg of ``bench.py``. The product path never imports it.
 
-Inputs are numpy arrays: ``float32``, ``float64``, or ``uint16`` holding raw
-bf16 bit patterns. Every function returns float64 results unless it is a
+Inputs are numpy arrays: ``float32``, ``float64``, ``float16``, or
+``uint16`` holding raw bf16 bit patterns. Every function returns float64 results unless it is a
 rounding helper.
 """
 from __future__ import annotations
@@ -19,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-F32, BF16, F64 = 0, 1, 2
+F32, BF16, F64, F16 = 0, 1, 2, 3
 
 _lib = None
 
@@ -48,6 +48,7 @@ def lib():
         L.oracle_rms_fwd.argtypes = [vp, vp, i32, i64, i64, dbl, vp, vp]
         L.oracle_round_f32.argtypes = [vp, vp, i64]
         L.oracle_round_bf16.argtypes = [vp, vp, i64]
+        L.oracle_round_f16.argtypes = [vp, vp, i64]
         L.oracle_welford_update.argtypes = [ctypes.POINTER(Welford), dbl]
         L.oracle_chan_combine.argtypes = [ctypes.POINTER(Welford)] * 3
         L.oracle_add_round.argtypes = [vp, vp, i32, i64, vp]
@@ -55,7 +56,7 @@ def lib():
         L.oracle_rms_bwd.argtypes = [vp, vp, vp, i32, i64, i64, dbl, vp, vp]
         for f in ("oracle_row_moments", "oracle_ln_fwd", "oracle_rms_fwd", "oracle_round_f32",
                   "oracle_round_bf16", "oracle_welford_update", "oracle_chan_combine", "oracle_add_round",
-                  "oracle_ln_bwd", "oracle_rms_bwd"):
+                  "oracle_ln_bwd", "oracle_rms_bwd", "oracle_round_f16"):
             getattr(L, f).restype = None
         L.oracle_abi_version.restype = ctypes.c_int
         _lib = L
@@ -69,7 +70,9 @@ def _dtype_code(a: np.ndarray) -> int:
         return BF16
     if a.dtype == np.float64:
         return F64
-    raise TypeError(f"oracle inputs must be float32, float64 or uint16 (bf16 bits), got {a.dtype}")
+    if a.dtype == np.float16:
+        return F16
+    raise TypeError(f"oracle inputs must be float32, float64, float16 or uint16 (bf16 bits), got {a.dtype}")
 
 
 def _c(a: np.ndarray) -> np.ndarray:
@@ -133,6 +136,14 @@ def round_bf16(v: np.ndarray) -> np.ndarray:
     out = np.empty(v.shape, np.uint16)
     lib().oracle_round_bf16(_ptr(v), _ptr(out), v.size)
     return out
+
+
+def round_f16(v: np.ndarray) -> np.ndarray:
+    """Round fp64 values to IEEE fp16, nearest-even; returns float16."""
+    v = _c(np.asarray(v, np.float64))
+    out = np.empty(v.shape, np.uint16)
+    lib().oracle_round_f16(_ptr(v), _ptr(out), v.size)
+    return out.view(np.float16)
 
 
 def add_round(x: np.ndarray, r: np.ndarray) -> np.ndarray:

@@ -16,7 +16,8 @@
  * in double precision: no blocking, no fusion, no reordering.
  *
  * Element types of the inputs: 0 = fp32, 1 = bf16 (raw 16-bit patterns),
- * 2 = fp64. Every input is widened exactly to double before any arithmetic.
+ * 2 = fp64, 3 = fp16 (raw 16-bit patterns). Every input is widened exactly
+ * to double before any arithmetic.
  *
  * Parity pins: each routine is pinned in tests/test_oracle_pins.py against
  * the pages' worked examples, closed forms, exact rational arithmetic on tiny
@@ -26,10 +27,27 @@
 #include <stdint.h>
 #include <string.h>
 
-enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F64 = 2 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F64 = 2, ORC_F16 = 3 };
+
+/* IEEE binary16 bit pattern to double, from the format's definition:
+ * sign, 5 exponent bits (bias 15), 10 fraction bits; exponent 0 holds
+ * subnormals (fraction * 2^-24), exponent 31 infinities and NaNs. Exact. */
+static double orc_f16_value(uint16_t h)
+{
+    const int sign = h >> 15, ex = (h >> 10) & 31, fr = h & 1023;
+    double v;
+    if (ex == 0)
+        v = ldexp((double)fr, -24);
+    else if (ex == 31)
+        v = fr ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + fr), ex - 25);
+    return sign ? -v : v;
+}
 
 /* Widen element i of a row to double. bf16 is the upper half of an fp32
- * bit pattern, so the widening is exact for all three types. */
+ * bit pattern; every fp16 value is a double: the widening is exact for all
+ * four types. */
 static double orc_load(const void *p, int dtype, int64_t i)
 {
     if (dtype == ORC_F32)
@@ -40,12 +58,14 @@ static double orc_load(const void *p, int dtype, int64_t i)
         memcpy(&f, &bits, sizeof f);
         return (double)f;
     }
+    if (dtype == ORC_F16)
+        return orc_f16_value(((const uint16_t *)p)[i]);
     return ((const double *)p)[i];
 }
 
 static int64_t orc_elem_size(int dtype)
 {
-    return dtype == ORC_F32 ? 4 : dtype == ORC_BF16 ? 2 : 8;
+    return dtype == ORC_F32 ? 4 : (dtype == ORC_BF16 || dtype == ORC_F16) ? 2 : 8;
 }
 
 /*
@@ -169,6 +189,44 @@ void oracle_round_bf16(const double *v, uint16_t *out, int64_t n)
         out[i] = orc_bf16(v[i]);
 }
 
+/* Round one double to IEEE binary16, nearest with ties to even, returned as
+ * the bit pattern: 11 significant bits, normal binades 2^-14 .. 2^15, below
+ * them the fixed subnormal spacing 2^-24. As for bf16, the value is scaled
+ * onto an integer grid of one ulp of its binade, rounded with rint() and
+ * scaled back; a result of 2^16 or more (65520 and up before rounding) is
+ * infinity. The pattern is then assembled field by field. */
+static uint16_t orc_f16(double v)
+{
+    if (isnan(v))
+        return 0x7E00;
+    const uint16_t sign = signbit(v) ? 0x8000 : 0;
+    const double a = fabs(v);
+    if (isinf(a))
+        return sign | 0x7C00;
+    if (a == 0.0)
+        return sign;
+    int e;
+    (void)frexp(a, &e);
+    int ex = e - 1;                 /* floor(log2 a) */
+    if (ex < -14)
+        ex = -14;
+    const double r = ldexp(rint(ldexp(a, 10 - ex)), ex - 10);
+    if (r >= 65536.0)
+        return sign | 0x7C00;
+    if (r < ldexp(1.0, -14))        /* subnormal (or zero): fraction = r / 2^-24 */
+        return sign | (uint16_t)ldexp(r, 24);
+    (void)frexp(r, &e);
+    const int be = e - 1 + 15;      /* biased exponent of the rounded value */
+    const uint16_t frac = (uint16_t)(ldexp(r, 10 - (e - 1)) - 1024.0);
+    return sign | (uint16_t)(be << 10) | frac;
+}
+
+void oracle_round_f16(const double *v, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_f16(v[i]);
+}
+
 /*
  * Welford's running state and Chan's merge, in double precision. They are
  * not used by the reference outputs above (which follow the definition);
@@ -213,9 +271,9 @@ void oracle_chan_combine(const orc_welford *a, const orc_welford *b,
  * Fused residual add ([Ch7] §7.9-7.10, the fused add + norm of the residual
  * stream; [T3] §⑤): h = x + residual, rounded to the row type, as an
  * unfused add that stores h would leave it. The sum is formed in double
- * (exact for two bf16 values; for fp32 values exact or carrying more than
- * 2*24+2 bits, so rounding it once more to the row type gives the correctly
- * rounded sum) and rounded to the row type. The norm of the
+ * (exact for two bf16 or fp16 values; for fp32 values exact or carrying more
+ * than 2*24+2 bits, so rounding it once more to the row type gives the
+ * correctly rounded sum) and rounded to the row type. The norm of the
  * fused op is then the norm of h (oracle_ln_fwd / oracle_rms_fwd on h).
  */
 void oracle_add_round(const void *x, const void *r, int dtype, int64_t n, void *h)
@@ -226,6 +284,8 @@ void oracle_add_round(const void *x, const void *r, int dtype, int64_t n, void *
             ((float *)h)[i] = (float)v;
         else if (dtype == ORC_BF16)
             ((uint16_t *)h)[i] = orc_bf16(v);
+        else if (dtype == ORC_F16)
+            ((uint16_t *)h)[i] = orc_f16(v);
         else
             ((double *)h)[i] = v;
     }
@@ -308,4 +368,4 @@ void oracle_rms_bwd(const void *dy, const void *x, const void *w, int dtype,
     }
 }
 
-int oracle_abi_version(void) { return 3; }
+int oracle_abi_version(void) { return 4; }

@@ -552,3 +552,50 @@ def test_bwd_bf16_inputs_widen_exactly():
     for got, want in zip(oracle.rms_bwd(bf(dy), bf(x), bf(g), 1e-6),
                          oracle.rms_bwd(back(bf(dy)), back(bf(x)), back(bf(g)), 1e-6)):
         assert np.array_equal(got, want)
+
+
+# ---------------------------------------------------------------- fp16
+
+def test_f16_widening_matches_numpy():
+    """fp16 patterns (every 7th of the 65536) widen to numpy's value (an
+    independent decoder), NaNs to NaN."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    h = bits.view(np.float16)
+    got = np.array([oracle.row_moments(h[i:i + 1])[0] for i in range(0, 65536, 7)])
+    want = h[::7].astype(np.float64)
+    both_nan = np.isnan(got) & np.isnan(want)
+    assert np.array_equal(got[~both_nan], want[~both_nan])
+
+
+def test_round_f16_matches_numpy():
+    """Library routine: numpy's float64 -> float16 conversion rounds to
+    nearest even; over random magnitudes spanning subnormals to overflow,
+    ties, and every fp16 value and midpoint."""
+    rng = np.random.default_rng(16)
+    v = rng.normal(0, 1, 200000) * np.exp2(rng.integers(-30, 18, 200000))
+    allh = np.arange(65536, dtype=np.uint32).astype(np.uint16).view(np.float16)
+    fin = allh[np.isfinite(allh)].astype(np.float64)
+    fin = np.unique(fin)
+    mids = (fin[:-1] + fin[1:]) / 2           # exact ties (fp64 holds them)
+    for arr in (v, fin, mids, np.array([65504.0, 65519.99, 65520.0, 1e9, -65520.0, 2.0 ** -25, 2.0 ** -26,
+                                        3 * 2.0 ** -26, 0.0, -0.0])):
+        got = oracle.round_f16(arr)
+        with np.errstate(over="ignore"):
+            want = arr.astype(np.float16)
+        assert np.array_equal(got.view(np.uint16), want.view(np.uint16))
+
+
+def test_f16_oracle_paths_equal_widened_inputs():
+    """fp16 inputs give exactly the results of their widened values."""
+    rng = np.random.default_rng(17)
+    x = rng.normal(3, 2, (4, 300)).astype(np.float16)
+    r = rng.normal(0, 1, (4, 300)).astype(np.float16)
+    g = rng.uniform(0.5, 1.5, 300).astype(np.float16)
+    b = rng.uniform(-0.1, 0.1, 300).astype(np.float16)
+    w = lambda a: a.astype(np.float64)
+    for got, want in zip(oracle.ln_fwd(x, g, b, 1e-5), oracle.ln_fwd(w(x), w(g), w(b), 1e-5)):
+        assert np.array_equal(got, want)
+    for got, want in zip(oracle.ln_bwd(r, x, g, 1e-5), oracle.ln_bwd(w(r), w(x), w(g), 1e-5)):
+        assert np.array_equal(got, want)
+    h = oracle.add_round(x, r)
+    assert h.dtype == np.float16 and np.array_equal(h, (x.astype(np.float32) + r.astype(np.float32)).astype(np.float16))
