@@ -20,8 +20,9 @@
  *   - x and y are [M, N] row-major and contiguous (row stride N elements).
  *     gamma, beta and w are [N]. x, y, gamma, beta and w all have the element
  *     type `dtype`; mean and rstd are always fp32 [M] ([T3] §⑥).
- *   - Statistics and all arithmetic are fp32; bf16 inputs are widened
- *     exactly and bf16 outputs are rounded to nearest-even.
+ *   - Statistics and all arithmetic are fp32; bf16 and fp16 inputs are
+ *     widened exactly and bf16 and fp16 outputs are rounded to nearest-even
+ *     (fp16 outputs beyond its range become infinities).
  *   - y may equal x exactly (in place). Any other overlap between outputs and
  *     inputs, or between outputs, is undefined.
  *   - Pointers need no particular alignment. When x, y and the parameter
@@ -45,7 +46,7 @@
 extern "C" {
 #endif
 
-typedef enum { NORM_F32 = 0, NORM_BF16 = 1 } norm_dtype;
+typedef enum { NORM_F32 = 0, NORM_BF16 = 1, NORM_F16 = 2 } norm_dtype;
 
 typedef enum {
     NORM_OK = 0,

@@ -18,12 +18,12 @@ import torch
 
 __all__ = [
     "ln_fwd", "rms_fwd", "ln_fwd_add", "rms_fwd_add", "ln_bwd", "rms_bwd", "make_plan", "make_bwd_plan", "NormPlan", "NormError", "LibraryNotBuilt", "library",
-    "NORM_F32", "NORM_BF16", "NORM_MAP_GROUP", "NORM_MAP_CTA",
+    "NORM_F32", "NORM_BF16", "NORM_F16", "NORM_MAP_GROUP", "NORM_MAP_CTA",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnorm.so")
 
-NORM_F32, NORM_BF16 = 0, 1
+NORM_F32, NORM_BF16, NORM_F16 = 0, 1, 2
 NORM_OK, NORM_ERR_ARG, NORM_ERR_DTYPE, NORM_ERR_CUDA, NORM_ERR_PLAN = 0, -1, -2, -3, -4
 NORM_MAP_GROUP, NORM_MAP_CTA = 0, 1
 
@@ -114,7 +114,9 @@ def _dtype_code(t: torch.dtype) -> int:
         return NORM_F32
     if t == torch.bfloat16:
         return NORM_BF16
-    raise TypeError(f"libnorm supports float32 and bfloat16, got {t}")
+    if t == torch.float16:
+        return NORM_F16
+    raise TypeError(f"libnorm supports float32, bfloat16 and float16, got {t}")
 
 
 def make_plan(M: int, N: int, dtype: torch.dtype, aligned: bool = True, num_sms: int = 152,

@@ -29,8 +29,8 @@ constexpr int kMaxStages = 4;
 
 thread_local int g_last_cuda_error = 0;
 
-bool dtype_ok(norm_dtype d) { return d == NORM_F32 || d == NORM_BF16; }
-int elem_size(norm_dtype d) { return d == NORM_BF16 ? 2 : 4; }
+bool dtype_ok(norm_dtype d) { return d == NORM_F32 || d == NORM_BF16 || d == NORM_F16; }
+int elem_size(norm_dtype d) { return d == NORM_F32 ? 4 : 2; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
@@ -276,12 +276,13 @@ int device_sm_count(int* dev_out) {
 using Launcher = cudaError_t (*)(const norm_plan&, const NormArgs&, cudaStream_t, int, int);
 
 Launcher pick_launcher(bool ln, bool add, norm_dtype dtype) {
-    const bool f32 = dtype == NORM_F32;
-    if (add)
-        return ln ? (f32 ? libnorm::launch_ln_add_f32 : libnorm::launch_ln_add_bf16)
-                  : (f32 ? libnorm::launch_rms_add_f32 : libnorm::launch_rms_add_bf16);
-    return ln ? (f32 ? libnorm::launch_ln_f32 : libnorm::launch_ln_bf16)
-              : (f32 ? libnorm::launch_rms_f32 : libnorm::launch_rms_bf16);
+    using namespace libnorm;
+    // [add][ln][dtype]
+    static const Launcher table[2][2][3] = {
+        {{launch_rms_f32, launch_rms_bf16, launch_rms_f16}, {launch_ln_f32, launch_ln_bf16, launch_ln_f16}},
+        {{launch_rms_add_f32, launch_rms_add_bf16, launch_rms_add_f16},
+         {launch_ln_add_f32, launch_ln_add_bf16, launch_ln_add_f16}}};
+    return table[add][ln][dtype];
 }
 
 // a.res != null selects the fused residual add.
@@ -396,11 +397,11 @@ norm_status bwd_impl(bool ln, const void* dy, const void* x, const void* gamma, 
     }
     libnorm::BwdArgs a{dy, x, gamma, mean, rstd, dx, static_cast<float*>(ws), dgamma, dbeta, M,
                        static_cast<int32_t>(N), eps, plan.cluster};
-    const bool f32 = dtype == NORM_F32;
-    const cudaError_t e = ln ? (f32 ? libnorm::launch_ln_bwd_f32(plan, a, stream, dev, sms)
-                                    : libnorm::launch_ln_bwd_bf16(plan, a, stream, dev, sms))
-                             : (f32 ? libnorm::launch_rms_bwd_f32(plan, a, stream, dev, sms)
-                                    : libnorm::launch_rms_bwd_bf16(plan, a, stream, dev, sms));
+    using BwdLauncher = cudaError_t (*)(const norm_plan&, const libnorm::BwdArgs&, cudaStream_t, int, int);
+    static const BwdLauncher table[2][3] = {
+        {libnorm::launch_rms_bwd_f32, libnorm::launch_rms_bwd_bf16, libnorm::launch_rms_bwd_f16},
+        {libnorm::launch_ln_bwd_f32, libnorm::launch_ln_bwd_bf16, libnorm::launch_ln_bwd_f16}};
+    const cudaError_t e = table[ln][dtype](plan, a, stream, dev, sms);
     if (e != cudaSuccess) {
         g_last_cuda_error = static_cast<int>(e);
         return NORM_ERR_CUDA;

@@ -65,6 +65,8 @@ cudaError_t launch_ln_bwd_f32(const norm_plan& plan, const BwdArgs& a, cudaStrea
 cudaError_t launch_ln_bwd_bf16(const norm_plan& plan, const BwdArgs& a, cudaStream_t s, int dev, int num_sms);
 cudaError_t launch_rms_bwd_f32(const norm_plan& plan, const BwdArgs& a, cudaStream_t s, int dev, int num_sms);
 cudaError_t launch_rms_bwd_bf16(const norm_plan& plan, const BwdArgs& a, cudaStream_t s, int dev, int num_sms);
+cudaError_t launch_ln_bwd_f16(const norm_plan& plan, const BwdArgs& a, cudaStream_t s, int dev, int num_sms);
+cudaError_t launch_rms_bwd_f16(const norm_plan& plan, const BwdArgs& a, cudaStream_t s, int dev, int num_sms);
 
 // Launch the kernel variant `plan` names on the current device `dev` (with
 // `num_sms` SMs). The plan has been validated; a pipelined plan with grid 0
@@ -73,10 +75,14 @@ cudaError_t launch_ln_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t
 cudaError_t launch_ln_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
 cudaError_t launch_rms_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
 cudaError_t launch_rms_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_ln_f16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_rms_f16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
 // The same with the fused residual add (a.res, a.h set).
 cudaError_t launch_ln_add_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
 cudaError_t launch_ln_add_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
 cudaError_t launch_rms_add_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
 cudaError_t launch_rms_add_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_ln_add_f16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_rms_add_f16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
 
 }  // namespace libnorm

@@ -50,18 +50,21 @@ struct BwdElem<float, 4> {
     }
 };
 
-template <>
-struct BwdElem<__nv_bfloat16, 8> {
+template <class T, class P>
+struct BwdElem16 {
     using Raw = uint4;
     static __device__ __forceinline__ float get(const Raw& r, int i) {
-        const uint32_t w = Ops<__nv_bfloat16, 8>::w(r, i >> 1);
-        return (i & 1) ? bf16_hi(w) : bf16_lo(w);
+        const float2 f = P::widen(Ops16<T, P>::w(r, i >> 1));
+        return (i & 1) ? f.y : f.x;
     }
     static __device__ __forceinline__ Raw pack(const float* v) {
-        return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                          pack_bf16x2(v[6], v[7]));
+        return make_uint4(P::pack(v[0], v[1]), P::pack(v[2], v[3]), P::pack(v[4], v[5]), P::pack(v[6], v[7]));
     }
 };
+template <>
+struct BwdElem<__nv_bfloat16, 8> : BwdElem16<__nv_bfloat16, Bf16Pair> {};
+template <>
+struct BwdElem<__half, 8> : BwdElem16<__half, F16Pair> {};
 
 template <class T>
 struct BwdElem<T, 1> {

@@ -50,9 +50,10 @@ struct ElemVec {
 };
 
 // ================================================================== element math
-// One access is a 16-byte vector (4 fp32 or 8 bf16) held as a uint4, or a
-// single element (VEC = 1) held in the low bits of a uint32. bf16 values are
-// widened exactly (a bf16 pattern is the top half of an fp32 pattern).
+// One access is a 16-byte vector (4 fp32, or 8 bf16 or fp16) held as a
+// uint4, or a single element (VEC = 1) held in the low bits of a uint32.
+// 16-bit values are widened exactly (a bf16 pattern is the top half of an
+// fp32 pattern; every fp16 value is an fp32 value).
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -68,6 +69,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // instructions (measured faster there).
 __device__ __forceinline__ float2 f2_splat(float v) { return make_float2(v, v); }
 __device__ __forceinline__ float2 bf16x2_widen(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
+
+// A pair of 16-bit values in one 32-bit word: exact widening to an fp32
+// pair, and nearest-even rounding of an fp32 pair back.
+struct Bf16Pair {
+    static __device__ __forceinline__ float2 widen(uint32_t w) { return bf16x2_widen(w); }
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi) { return pack_bf16x2(lo, hi); }
+};
+struct F16Pair {
+    static __device__ __forceinline__ float2 widen(uint32_t w) {
+        return __half22float2(*reinterpret_cast<const __half2*>(&w));  // every fp16 value is an fp32 value
+    }
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+        const __half2 h = __floats2half2_rn(lo, hi);  // round to nearest-even
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+};
 
 // Per-access operations, specialised on element type and width.
 template <class T, int VEC>
@@ -126,16 +143,17 @@ struct Ops<float, 4> {
     static __device__ __forceinline__ void store(float* p, const Raw& v) { *reinterpret_cast<uint4*>(p) = v; }
 };
 
-template <>
-struct Ops<__nv_bfloat16, 8> {
+// Eight 16-bit elements (bf16 or fp16) per access, worked on as fp32 pairs.
+template <class T, class P>
+struct Ops16 {
     using Raw = uint4;
     static __device__ __forceinline__ uint32_t w(const Raw& r, int i) {
         return i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w;
     }
     static __device__ __forceinline__ float shifted_sum(const Raw& r, float K) {
         const float2 nk = f2_splat(-K);
-        const float2 a = __fadd2_rn(__fadd2_rn(bf16x2_widen(r.x), nk), __fadd2_rn(bf16x2_widen(r.y), nk));
-        const float2 b = __fadd2_rn(__fadd2_rn(bf16x2_widen(r.z), nk), __fadd2_rn(bf16x2_widen(r.w), nk));
+        const float2 a = __fadd2_rn(__fadd2_rn(P::widen(r.x), nk), __fadd2_rn(P::widen(r.y), nk));
+        const float2 b = __fadd2_rn(__fadd2_rn(P::widen(r.z), nk), __fadd2_rn(P::widen(r.w), nk));
         const float2 s = __fadd2_rn(a, b);
         return s.x + s.y;
     }
@@ -144,7 +162,7 @@ struct Ops<__nv_bfloat16, 8> {
         float2 q = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float2 d = __fadd2_rn(__fadd2_rn(bf16x2_widen(w(r, i)), nk), nm);
+            const float2 d = __fadd2_rn(__fadd2_rn(P::widen(w(r, i)), nk), nm);
             q = __ffma2_rn(d, d, q);
         }
         return acc + (q.x + q.y);
@@ -153,7 +171,7 @@ struct Ops<__nv_bfloat16, 8> {
         float2 q = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float2 x = bf16x2_widen(w(r, i));
+            const float2 x = P::widen(w(r, i));
             q = __ffma2_rn(x, x, q);
         }
         return acc + (q.x + q.y);
@@ -164,9 +182,9 @@ struct Ops<__nv_bfloat16, 8> {
         uint32_t o[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float2 y = __ffma2_rn(__ffma2_rn(__fadd2_rn(bf16x2_widen(w(r, i)), nk), rs2, nm2),
-                                        bf16x2_widen(w(g, i)), bf16x2_widen(w(b, i)));
-            o[i] = pack_bf16x2(y.x, y.y);
+            const float2 y = __ffma2_rn(__ffma2_rn(__fadd2_rn(P::widen(w(r, i)), nk), rs2, nm2),
+                                        P::widen(w(g, i)), P::widen(w(b, i)));
+            o[i] = P::pack(y.x, y.y);
         }
         return make_uint4(o[0], o[1], o[2], o[3]);
     }
@@ -175,31 +193,36 @@ struct Ops<__nv_bfloat16, 8> {
         uint32_t o[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float2 y = __fmul2_rn(__fmul2_rn(bf16x2_widen(w(r, i)), bf16x2_widen(w(wt, i))), rs2);
-            o[i] = pack_bf16x2(y.x, y.y);
+            const float2 y = __fmul2_rn(__fmul2_rn(P::widen(w(r, i)), P::widen(w(wt, i))), rs2);
+            o[i] = P::pack(y.x, y.y);
         }
         return make_uint4(o[0], o[1], o[2], o[3]);
     }
-    // Residual add h = x + r: the exact sum of two bf16 values needs at most
-    // 18 bits of the fp32 sum's 24, so rounding that sum to bf16 rounds the
-    // exact sum once.
+    // Residual add h = x + r: fp32 carries at least 2p + 2 bits for both
+    // 16-bit formats (p = 8 for bf16, 11 for fp16), so rounding the fp32 sum
+    // to T rounds the exact sum once.
     static __device__ __forceinline__ Raw add_round(const Raw& x, const Raw& r) {
         uint32_t o[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float2 h = __fadd2_rn(bf16x2_widen(w(x, i)), bf16x2_widen(w(r, i)));
-            o[i] = pack_bf16x2(h.x, h.y);
+            const float2 h = __fadd2_rn(P::widen(w(x, i)), P::widen(w(r, i)));
+            o[i] = P::pack(h.x, h.y);
         }
         return make_uint4(o[0], o[1], o[2], o[3]);
     }
-    static __device__ __forceinline__ Raw load(const __nv_bfloat16* p) { return *reinterpret_cast<const uint4*>(p); }
-    static __device__ __forceinline__ Raw load_param(const __nv_bfloat16* p) {
+    static __device__ __forceinline__ Raw load(const T* p) { return *reinterpret_cast<const uint4*>(p); }
+    static __device__ __forceinline__ Raw load_param(const T* p) {
         return __ldg(reinterpret_cast<const uint4*>(p));
     }
-    static __device__ __forceinline__ void store(__nv_bfloat16* p, const Raw& v) {
+    static __device__ __forceinline__ void store(T* p, const Raw& v) {
         *reinterpret_cast<uint4*>(p) = v;
     }
 };
+
+template <>
+struct Ops<__nv_bfloat16, 8> : Ops16<__nv_bfloat16, Bf16Pair> {};
+template <>
+struct Ops<__half, 8> : Ops16<__half, F16Pair> {};
 
 // Single elements (rows that are not whole 16-byte aligned vectors).
 template <class T>
@@ -208,6 +231,8 @@ struct ScalarOps {
     static __device__ __forceinline__ float e(Raw r) {
         if constexpr (sizeof(T) == 4)
             return __uint_as_float(r);
+        else if constexpr (std::is_same<T, __half>::value)
+            return __half2float(__ushort_as_half(static_cast<unsigned short>(r)));
         else
             return __uint_as_float(r << 16);
     }
@@ -225,6 +250,8 @@ struct ScalarOps {
     static __device__ __forceinline__ Raw from_float(float v) {
         if constexpr (sizeof(T) == 4)
             return __float_as_uint(v);
+        else if constexpr (std::is_same<T, __half>::value)
+            return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v)));
         else
             return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
     }

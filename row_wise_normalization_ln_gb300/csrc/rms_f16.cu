@@ -1,0 +1,11 @@
+// RMSNorm forward kernels, fp16 rows: every (mapping, access width,
+// accesses per thread) variant the planner can name.
+#include "norm_kernels.cuh"
+
+namespace libnorm {
+
+cudaError_t launch_rms_f16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev) {
+    return launch_norm<__half, false, false>(plan, a, s, num_sms, dev);
+}
+
+}  // namespace libnorm

@@ -18,6 +18,7 @@ Workloads (shapes and value distributions of the source pages):
                            post's V0/V2 sizes); x ~ U(-1,1), w ~ U(0,1), eps 1e-6.
   ln_f32_2048x65536        LayerNorm fp32 long rows; x ~ N(3,1).
   ln_f32_8192x5000         LayerNorm fp32, N not a power of two; x ~ N(3,1).
+  ln_f16_4096x8192         LayerNorm fp16 rows, the T3 drill's N; x ~ N(3,1).
   add_*                    the fused residual add + norm on the shape and
                            recipe of the workload it names: the residual r is
                            drawn from the same recipe, after the parameters.
@@ -36,7 +37,7 @@ import torch
 class Workload:
     name: str
     op: str        # "ln" or "rms"
-    dtype: str     # "f32" or "bf16"
+    dtype: str     # "f32", "bf16" or "f16"
     M: int
     N: int
     eps: float
@@ -46,7 +47,7 @@ class Workload:
 
     @property
     def torch_dtype(self) -> torch.dtype:
-        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+        return {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[self.dtype]
 
     @property
     def elem_size(self) -> int:
@@ -88,6 +89,7 @@ WORKLOADS = {
         Workload("rms_bf16_65536x2048", "rms", "bf16", 65536, 2048, 1e-6, "uniform_pm1"),
         Workload("ln_f32_2048x65536", "ln", "f32", 2048, 65536, 1e-5, "normal31"),
         Workload("ln_f32_8192x5000", "ln", "f32", 8192, 5000, 1e-5, "normal31"),
+        Workload("ln_f16_4096x8192", "ln", "f16", 4096, 8192, 1e-5, "normal31"),
         Workload("add_rms_f32_8192x4096", "rms", "f32", 8192, 4096, 1e-6, "uniform_pm1", True),
         Workload("add_rms_bf16_65536x2048", "rms", "bf16", 65536, 2048, 1e-6, "uniform_pm1", True),
         Workload("add_ln_bf16_4096x8192_outliers", "ln", "bf16", 4096, 8192, 1e-5, "offset_outliers", True),

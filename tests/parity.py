@@ -5,8 +5,8 @@ fp32 outputs: max |y - y_ref| <= 1e-4; rstd relative error <= 1e-5; mean
 within 1e-5 of the row's scale, max(|mean_ref|, sigma_ref) (a purely relative
 bound is ill-posed for means near zero).
 
-bf16 outputs: y within one bf16 ulp of the oracle's value rounded to bf16.
-Near y = 0 a bf16 ulp is smaller than the fp32 error of any fp32
+bf16 and fp16 outputs: y within one ulp of the oracle's value rounded to
+that type. Near y = 0 an ulp is smaller than the fp32 error of any fp32
 evaluation, so each row also gets an absolute floor from the fp32 error
 budget of y = (x - mean) * rstd * gamma + beta:
     2^-21 * ((|mean| * rstd + max|x_hat|) * max|gamma| + max|beta|)
@@ -49,6 +49,23 @@ def ulp_bf16(v: np.ndarray) -> np.ndarray:
     return np.exp2(e - 7)
 
 
+def ulp_f16(v: np.ndarray) -> np.ndarray:
+    a = np.abs(v)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.where(a > 0, np.maximum(e, -14), -14)
+    return np.exp2(e - 10)
+
+
+def round16(y_ref: np.ndarray, like: np.ndarray):
+    """The oracle's values rounded to the 16-bit type of `like` (raw bf16
+    bits or float16), widened back, with that type's ulp."""
+    if like.dtype == np.float16:
+        r = oracle.round_f16(y_ref).astype(np.float64)
+        return r, ulp_f16(r)
+    r = as_f64(oracle.round_bf16(y_ref))
+    return r, ulp_bf16(r)
+
+
 def check_y(y_gpu: np.ndarray, y_ref: np.ndarray, floor_rows: np.ndarray | None = None) -> dict:
     """Compare one block of rows; returns error statistics, asserts the bar."""
     if y_gpu.dtype == np.float32:
@@ -57,14 +74,13 @@ def check_y(y_gpu: np.ndarray, y_ref: np.ndarray, floor_rows: np.ndarray | None 
         assert np.all(np.isfinite(y_gpu)), "non-finite output"
         assert worst <= FP32_Y_ABS, f"max |dy| = {worst:.3e} > {FP32_Y_ABS}"
         return {"max_abs": worst}
-    ref_b = as_f64(oracle.round_bf16(y_ref))
+    ref_b, ulp = round16(y_ref, y_gpu)
     got = as_f64(y_gpu)
     diff = np.abs(got - ref_b)
-    ulp = ulp_bf16(ref_b)
     tol = ulp if floor_rows is None else np.maximum(ulp, floor_rows[:, None])
     bad = diff > tol
     assert not bad.any(), (
-        f"{int(bad.sum())} bf16 outputs off by more than 1 ulp (worst {float((diff / ulp).max()):.2f} ulp)")
+        f"{int(bad.sum())} 16-bit outputs off by more than 1 ulp (worst {float((diff / ulp).max()):.2f} ulp)")
     return {"exact": int((diff == 0).sum()), "one_ulp": int(((diff > 0) & (diff <= ulp)).sum()),
             "floor_only": int(((diff > ulp) & ~bad).sum()), "n": int(diff.size)}
 
@@ -107,7 +123,7 @@ def check_ln(x, gamma, beta, eps, y, mean=None, rstd=None, rows=None) -> dict:
         rn_ = rn_[rows] if rn_ is not None else None
     e = oracle.eps_as_f32(eps)
     y_ref, m_ref, r_ref = oracle.ln_fwd(xn, gn, bn, e)
-    floor = ln_floor(as_f64(xn), as_f64(gn), as_f64(bn), m_ref, r_ref) if yn.dtype == np.uint16 else None
+    floor = ln_floor(as_f64(xn), as_f64(gn), as_f64(bn), m_ref, r_ref) if yn.dtype != np.float32 else None
     res = check_y(yn, y_ref, floor)
     res.update(check_stats(mn, rn_, m_ref, r_ref, e))
     return res
@@ -119,14 +135,17 @@ def check_rms(x, w, eps, y, rows=None) -> dict:
         xn, yn = xn[rows], yn[rows]
     e = oracle.eps_as_f32(eps)
     y_ref, r_ref = oracle.rms_fwd(xn, wn, e)
-    floor = rms_floor(as_f64(xn), as_f64(wn), r_ref) if yn.dtype == np.uint16 else None
+    floor = rms_floor(as_f64(xn), as_f64(wn), r_ref) if yn.dtype != np.float32 else None
     return check_y(yn, y_ref, floor)
 
 
 def torch_of(a: np.ndarray) -> torch.Tensor:
-    """Inverse of np_of: CPU tensor from float32 or raw bf16 (uint16) bits."""
+    """Inverse of np_of: CPU tensor from float32, float16 or raw bf16
+    (uint16) bits."""
     if a.dtype == np.uint16:
         return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16)
+    if a.dtype == np.float16:
+        return torch.from_numpy(a.copy())
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
 
 
@@ -137,7 +156,7 @@ def check_h(x, r, h, rows=None) -> torch.Tensor:
     if rows is not None:
         xn, rn_, hn = xn[rows], rn_[rows], hn[rows]
     h_ref = oracle.add_round(xn, rn_)
-    bits = np.uint16 if h_ref.dtype == np.uint16 else np.uint32
+    bits = np.uint16 if h_ref.dtype.itemsize == 2 else np.uint32
     bad = hn.view(bits) != h_ref.view(bits)
     assert not bad.any(), f"{int(bad.sum())} elements of h differ from the rounded sum"
     return torch_of(h_ref)
@@ -195,11 +214,10 @@ def _dx_check(dx_gpu: np.ndarray, dx_ref: np.ndarray, tol_rows: np.ndarray) -> d
         ratio = err / tol_rows[:, None]
         assert (ratio <= 1).all(), f"dx off by {float(ratio.max()):.2f} x the bound"
         return {"dx_worst_of_bound": float(ratio.max()) if ratio.size else 0.0}
-    ref_b = as_f64(oracle.round_bf16(dx_ref))
+    ref_b, ulp = round16(dx_ref, dx_gpu)
     diff = np.abs(as_f64(dx_gpu) - ref_b)
-    ulp = ulp_bf16(ref_b)
     bad = diff > np.maximum(ulp, tol_rows[:, None])
-    assert not bad.any(), f"{int(bad.sum())} bf16 dx off by more than 1 ulp and the fp32 bound"
+    assert not bad.any(), f"{int(bad.sum())} 16-bit dx off by more than 1 ulp and the fp32 bound"
     return {"dx_exact": int((diff == 0).sum()), "dx_n": int(diff.size)}
 
 

@@ -201,7 +201,7 @@ NS = [1, 2, 3, 4, 5, 7, 8, 9, 31, 32, 33, 64, 100, 255, 256, 257, 1000, 1023, 10
       4096, 4999, 5000, 8192, 16384, 32768, 65535, 65536, 100000, 262144, 262145, 1 << 20, (1 << 24)]
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("aligned", [True, False])
 @pytest.mark.parametrize("M", [1, 3, 128, 8192, 65536])
 def test_plans_are_consistent(lib, dtype, aligned, M):
@@ -251,6 +251,7 @@ def test_plans_for_the_workloads(lib):
         "rms_bf16_65536x2048": dict(mapping=rn.NORM_MAP_CTA, per_thread=4, threads=64, cluster=1, rounds=1),
         "ln_f32_2048x65536": dict(mapping=rn.NORM_MAP_CTA, per_thread=8, threads=128, cluster=8, rounds=2),
         "ln_f32_8192x5000": dict(mapping=rn.NORM_MAP_CTA, per_thread=8, threads=160, cluster=1, rounds=1),
+        "ln_f16_4096x8192": dict(mapping=rn.NORM_MAP_CTA, per_thread=8, threads=128, cluster=1, rounds=1),
     }
     got.update({name: rn.make_plan(w.M, w.N, w.torch_dtype, True, 152, add=True)
                 for name, w in WORKLOADS.items() if w.add})
