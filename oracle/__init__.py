@@ -49,6 +49,9 @@ def lib():
         L.oracle_round_f32.argtypes = [vp, vp, i64]
         L.oracle_round_bf16.argtypes = [vp, vp, i64]
         L.oracle_round_f16.argtypes = [vp, vp, i64]
+        L.oracle_quant_e4m3.argtypes = [vp, i64, dbl, vp]
+        L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_value.restype = dbl
         L.oracle_welford_update.argtypes = [ctypes.POINTER(Welford), dbl]
         L.oracle_chan_combine.argtypes = [ctypes.POINTER(Welford)] * 3
         L.oracle_add_round.argtypes = [vp, vp, i32, i64, vp]
@@ -56,7 +59,7 @@ def lib():
         L.oracle_rms_bwd.argtypes = [vp, vp, vp, i32, i64, i64, dbl, vp, vp]
         for f in ("oracle_row_moments", "oracle_ln_fwd", "oracle_rms_fwd", "oracle_round_f32",
                   "oracle_round_bf16", "oracle_welford_update", "oracle_chan_combine", "oracle_add_round",
-                  "oracle_ln_bwd", "oracle_rms_bwd", "oracle_round_f16"):
+                  "oracle_ln_bwd", "oracle_rms_bwd", "oracle_round_f16", "oracle_quant_e4m3"):
             getattr(L, f).restype = None
         L.oracle_abi_version.restype = ctypes.c_int
         _lib = L
@@ -144,6 +147,20 @@ def round_f16(v: np.ndarray) -> np.ndarray:
     out = np.empty(v.shape, np.uint16)
     lib().oracle_round_f16(_ptr(v), _ptr(out), v.size)
     return out.view(np.float16)
+
+
+def quant_e4m3(y: np.ndarray, scale: float) -> np.ndarray:
+    """E4M3 codes (uint8) of y / scale: nearest-even, saturating at 448."""
+    y = _c(np.asarray(y, np.float64))
+    q = np.empty(y.shape, np.uint8)
+    lib().oracle_quant_e4m3(_ptr(y), y.size, float(scale), _ptr(q))
+    return q
+
+
+def e4m3_values(q: np.ndarray) -> np.ndarray:
+    """Values of E4M3 codes (float64; NaN for 0x7F/0xFF)."""
+    table = np.array([lib().oracle_e4m3_value(c) for c in range(256)])
+    return table[np.asarray(q, np.uint8)]
 
 
 def add_round(x: np.ndarray, r: np.ndarray) -> np.ndarray:

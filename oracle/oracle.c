@@ -368,4 +368,61 @@ void oracle_rms_bwd(const void *dy, const void *x, const void *w, int dtype,
     }
 }
 
-int oracle_abi_version(void) { return 4; }
+/*
+ * FP8 output for the next GEMM ([Ch7] §7.9: the norm writes the quantised
+ * input of the following GEMM, as vLLM's static-scale fused kernels do).
+ * Format: OCP FP8 E4M3 ("fn": finite only): sign, 4 exponent bits (bias 7),
+ * 3 fraction bits; normal values 2^-6 .. 448, subnormals fraction * 2^-9,
+ * the pattern 0x7F / 0xFF is NaN, and there is no infinity. Quantisation
+ * with a per-tensor static scale: q = E4M3(y / scale), nearest with ties to
+ * even, saturating: values of magnitude 448 or more give +-448.
+ */
+static uint8_t orc_e4m3(double v)
+{
+    if (isnan(v))
+        return 0x7F;
+    const uint8_t sign = signbit(v) ? 0x80 : 0;
+    const double a = fabs(v);
+    if (a >= 448.0)
+        return sign | 0x7E;           /* 448 = 1.75 * 2^8: exponent 15, fraction 110 */
+    if (a == 0.0)
+        return sign;
+    int e;
+    (void)frexp(a, &e);
+    int ex = e - 1;                   /* floor(log2 a) */
+    if (ex < -6)
+        ex = -6;                      /* subnormals keep the spacing 2^-9 */
+    const double r = ldexp(rint(ldexp(a, 3 - ex)), ex - 3);
+    if (r >= 448.0)
+        return sign | 0x7E;
+    if (r < ldexp(1.0, -6))           /* subnormal (or zero): fraction = r / 2^-9 */
+        return sign | (uint8_t)ldexp(r, 9);
+    (void)frexp(r, &e);
+    const int be = e - 1 + 7;
+    const uint8_t frac = (uint8_t)(ldexp(r, 3 - (e - 1)) - 8.0);
+    return sign | (uint8_t)(be << 3) | frac;
+}
+
+/* q_i = E4M3(y_i / scale) for n values (the division is exact-rounded in
+ * double; see orc_e4m3 for the rounding). */
+void oracle_quant_e4m3(const double *y, int64_t n, double scale, uint8_t *q)
+{
+    for (int64_t i = 0; i < n; ++i)
+        q[i] = orc_e4m3(y[i] / scale);
+}
+
+/* Value of an E4M3 code (exact; NaN for 0x7F and 0xFF). */
+double oracle_e4m3_value(uint8_t q)
+{
+    const int sign = q >> 7, ex = (q >> 3) & 15, fr = q & 7;
+    double v;
+    if (ex == 15 && fr == 7)
+        return NAN;
+    if (ex == 0)
+        v = ldexp((double)fr, -9);
+    else
+        v = ldexp((double)(8 + fr), ex - 10);
+    return sign ? -v : v;
+}
+
+int oracle_abi_version(void) { return 5; }

@@ -599,3 +599,47 @@ def test_f16_oracle_paths_equal_widened_inputs():
         assert np.array_equal(got, want)
     h = oracle.add_round(x, r)
     assert h.dtype == np.float16 and np.array_equal(h, (x.astype(np.float32) + r.astype(np.float32)).astype(np.float16))
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) output
+
+def _torch_e4m3(v: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(v.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_decode_matches_torch():
+    """All 256 codes decode to torch's float8_e4m3fn values (an independent
+    library routine), NaN codes to NaN."""
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_values(codes)
+    theirs = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    nan = np.isnan(theirs)
+    assert np.array_equal(np.isnan(ours), nan) and nan.sum() == 2
+    assert np.array_equal(ours[~nan], theirs[~nan])
+    assert oracle.e4m3_values(np.array([0x7E]))[0] == 448.0 and oracle.e4m3_values(np.array([1]))[0] == 2.0 ** -9
+
+
+def test_e4m3_rounding_matches_torch_in_range():
+    """Nearest-even rounding against torch's cast, on random values below
+    the saturation point, every code value, and every midpoint (ties)."""
+    rng = np.random.default_rng(8)
+    v = rng.normal(0, 1, 100000) * np.exp2(rng.integers(-12, 9, 100000))
+    v = v[np.abs(v) < 448]
+    vals = np.unique(oracle.e4m3_values(np.arange(256, dtype=np.uint8)))
+    vals = vals[np.isfinite(vals)]
+    mids = (vals[:-1] + vals[1:]) / 2
+    for arr in (v, vals, mids, -mids, np.array([447.0, 447.99, 2.0 ** -10, 3 * 2.0 ** -10, 2.0 ** -11])):
+        arr = arr.astype(np.float32).astype(np.float64)   # torch casts from fp32: give both the same value
+        assert np.array_equal(oracle.quant_e4m3(arr, 1.0), _torch_e4m3(arr)), arr[:4]
+
+
+def test_e4m3_saturates_and_scales():
+    """Magnitudes from 448 up give +-448 (0x7E / 0xFE): the saturating form
+    the GEMM input takes; NaN stays NaN; the scale divides."""
+    big = np.array([448.0, 449.0, 463.9, 464.0, 500.0, 1e30, np.inf, -448.5, -np.inf])
+    q = oracle.quant_e4m3(big, 1.0)
+    assert q.tolist() == [0x7E] * 7 + [0xFE, 0xFE]
+    assert oracle.quant_e4m3(np.array([np.nan]), 1.0)[0] == 0x7F
+    y = np.array([1.0, -3.0, 0.5])
+    assert np.array_equal(oracle.quant_e4m3(y, 0.25), oracle.quant_e4m3(y * 4, 1.0))
+    assert oracle.e4m3_values(oracle.quant_e4m3(np.array([2.0]), 1 / 64.0))[0] == 128.0
