@@ -90,14 +90,14 @@ def ncu_traffic(workload: str):
 def kernel_name(w, plan) -> str:
     kind = "group" if plan["mapping"] == 0 else "cta"
     t = "float" if w.dtype == "f32" else "__nv_bfloat16"
-    op = ("ADD+" if w.add else "") + ("LN" if w.op == "ln" else "RMS")
+    op = ("ADD+" if w.add else "") + ("LN" if w.op == "ln" else "RMS") + ("+E4M3" if w.fp8 else "")
     if w.bwd:
         return f"norm_bwd_cta<{t},{plan['vec_elems']},{plan['per_thread']},{op}>"
     return f"norm_fwd_{kind}<{t},{plan['vec_elems']},{plan['per_thread']},{op}>"
 
 
 def op_name(w) -> str:
-    return ("add+" if w.add else "") + w.op + ("_bwd" if w.bwd else "")
+    return ("add+" if w.add else "") + w.op + ("_bwd" if w.bwd else "") + ("_fp8" if w.fp8 else "")
 
 
 def metric_name(w) -> str:
@@ -181,7 +181,8 @@ def make_sets(w, inp, n_sets, device):
         return make_bwd_sets(w, inp, n_sets, device)
     sets = []
     for _ in range(n_sets):
-        s = {"x": inp["x"].to(device), "y": torch.empty(w.M, w.N, dtype=w.torch_dtype, device=device)}
+        s = {"x": inp["x"].to(device),
+             "y": torch.empty(w.M, w.N, dtype=torch.uint8 if w.fp8 else w.torch_dtype, device=device)}
         if w.add:
             s["r"] = inp["r"].to(device)
             s["h"] = torch.empty(w.M, w.N, dtype=w.torch_dtype, device=device)
@@ -190,6 +191,8 @@ def make_sets(w, inp, n_sets, device):
             s["rstd"] = torch.empty(w.M, dtype=torch.float32, device=device)
         sets.append(s)
     params = {k: v.to(device) for k, v in inp.items() if k not in ("x", "r")}
+    if w.fp8:
+        params["scale"] = torch.tensor([w.qscale], dtype=torch.float32, device=device)
     return sets, params
 
 
@@ -228,6 +231,17 @@ def step_fn(w, rn, params):
 
         def f(s):
             rn.rms_bwd(s["dy"], s["x"], wt, w.eps, dx=s["dx"], dw=dg, workspace=ws)
+    elif w.fp8 and w.op == "ln":
+        g, b, sc = params["gamma"], params["beta"], params["scale"]
+
+        def f(s):
+            rn.ln_fwd_fp8(s["x"], g, b, sc, w.eps, residual=s.get("r"), h_out=s.get("h"), out=s["y"],
+                          mean=s["mean"], rstd=s["rstd"])
+    elif w.fp8:
+        wt, sc = params["w"], params["scale"]
+
+        def f(s):
+            rn.rms_fwd_fp8(s["x"], wt, sc, w.eps, residual=s.get("r"), h_out=s.get("h"), out=s["y"])
     elif w.add and w.op == "ln":
         g, b = params["gamma"], params["beta"]
 
@@ -261,8 +275,8 @@ def time_same_bytes_copy(w, inp, device, steps=600, per_graph=60):
     512 MB or more becomes a memcpy node that runs at about half the copy
     bandwidth of the same copy launched directly."""
     import torch
-    n = w.M * w.N * w.row_tensors // 2
-    sets = [(torch.empty(n, dtype=w.torch_dtype, device=device), torch.empty(n, dtype=w.torch_dtype, device=device))
+    n = w.M * w.N * w.row_bytes // 2
+    sets = [(torch.empty(n, dtype=torch.uint8, device=device), torch.empty(n, dtype=torch.uint8, device=device))
             for _ in range(n_sets_for(w))]
     for src, _ in sets:
         src.fill_(1.0)
@@ -299,7 +313,7 @@ def time_same_bytes_copy(w, inp, device, steps=600, per_graph=60):
 
 
 def n_sets_for(w):
-    per_set = w.row_tensors * w.M * w.N * w.elem_size
+    per_set = w.row_bytes * w.M * w.N
     return max(3, math.ceil(3 * L2_BYTES / per_set))
 
 
@@ -426,10 +440,12 @@ def time_e2e(w, rn, inp, device, steps):
     import torch
     hin = {k: v.pin_memory() for k, v in inp.items()}
     din = {k: torch.empty_like(v, device=device) for k, v in hin.items()}
-    dy = torch.empty_like(din["x"])
-    hy = torch.empty_like(hin["x"]).pin_memory()
-    dh = torch.empty_like(dy) if w.add else None
-    hh = torch.empty_like(hy).pin_memory() if w.add else None
+    ydt = torch.uint8 if w.fp8 else w.torch_dtype
+    dy = torch.empty(w.M, w.N, dtype=ydt, device=device)
+    hy = torch.empty(w.M, w.N, dtype=ydt).pin_memory()
+    dh = torch.empty_like(din["x"]) if w.add else None
+    hh = torch.empty_like(hin["x"]).pin_memory() if w.add else None
+    sc = torch.tensor([w.qscale], dtype=torch.float32, device=device) if w.fp8 else None
     ln = w.op == "ln"
     if ln:
         dm = torch.empty(w.M, dtype=torch.float32, device=device)
@@ -437,12 +453,17 @@ def time_e2e(w, rn, inp, device, steps):
         hm = torch.empty(w.M, dtype=torch.float32).pin_memory()
         hr = torch.empty_like(hm).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in hin.values())
-    d2h = hy.numel() * hy.element_size() * (2 if w.add else 1) + (8 * w.M if ln else 0)
+    d2h = hy.numel() * hy.element_size() + (hh.numel() * hh.element_size() if w.add else 0) + (8 * w.M if ln else 0)
 
     def one():
         for k in hin:
             din[k].copy_(hin[k], non_blocking=True)
-        if ln and w.add:
+        if w.fp8 and ln:
+            rn.ln_fwd_fp8(din["x"], din["gamma"], din["beta"], sc, w.eps, residual=din.get("r"), h_out=dh, out=dy,
+                          mean=dm, rstd=dr)
+        elif w.fp8:
+            rn.rms_fwd_fp8(din["x"], din["w"], sc, w.eps, residual=din.get("r"), h_out=dh, out=dy)
+        elif ln and w.add:
             rn.ln_fwd_add(din["x"], din["r"], din["gamma"], din["beta"], w.eps, h_out=dh, out=dy, mean=dm, rstd=dr)
         elif ln:
             rn.ln_fwd(din["x"], din["gamma"], din["beta"], w.eps, out=dy, mean=dm, rstd=dr)
@@ -475,7 +496,8 @@ def time_e2e(w, rn, inp, device, steps):
 # ------------------------------------------------------------------ CPU oracle
 
 def oracle_rows(w, inp, rows: int):
-    """One call of the fp64 oracle over the first `rows` rows."""
+    """One call of the fp64 oracle over the first `rows` rows (with an FP8
+    output: the norm, then the quantisation of its values)."""
     import numpy as np
     import oracle
 
@@ -494,11 +516,16 @@ def oracle_rows(w, inp, rows: int):
     if w.add:
         r = npx(inp["r"][:rows])
         if w.op == "ln":
-            return lambda: oracle.ln_fwd_add(x, r, npx(inp["gamma"]), npx(inp["beta"]), e)
-        return lambda: oracle.rms_fwd_add(x, r, npx(inp["w"]), e)
-    if w.op == "ln":
-        return lambda: oracle.ln_fwd(x, npx(inp["gamma"]), npx(inp["beta"]), oracle.eps_as_f32(w.eps))
-    return lambda: oracle.rms_fwd(x, npx(inp["w"]), oracle.eps_as_f32(w.eps))
+            norm = lambda: oracle.ln_fwd_add(x, r, npx(inp["gamma"]), npx(inp["beta"]), e)[1]
+        else:
+            norm = lambda: oracle.rms_fwd_add(x, r, npx(inp["w"]), e)[1]
+    elif w.op == "ln":
+        norm = lambda: oracle.ln_fwd(x, npx(inp["gamma"]), npx(inp["beta"]), e)[0]
+    else:
+        norm = lambda: oracle.rms_fwd(x, npx(inp["w"]), e)[0]
+    if w.fp8:
+        return lambda: oracle.quant_e4m3(norm(), w.qscale)
+    return norm
 
 
 def cpu_baseline(w, inp, seconds: float):
@@ -631,7 +658,7 @@ def main():
                            "same_size_copy_us": round(copy_us, 3),
                            # achieved GB/s over the same-size copy's GB/s
                            "frac_of_same_size_copy": round(
-                               gbs / ((wk.row_tensors * wk.M * wk.N * wk.elem_size) / (copy_us / 1e6) / 1e9), 4),
+                               gbs / ((wk.row_bytes * wk.M * wk.N) / (copy_us / 1e6) / 1e9), 4),
                            "rows_per_s": round(wk.M / (us / 1e6)), "plan": plan_for(rn, wk, props.multi_processor_count)}
             del wi
 
@@ -653,7 +680,7 @@ def main():
                    "io_dtype": w.dtype, "eps": w.eps,
                    "algorithmic_bytes_per_call": bytes_per_call,
                    "l2": f"{n_sets_for(w)} rotating input/output sets of "
-                         f"{w.row_tensors * w.M * w.N * w.elem_size >> 20} MiB "
+                         f"{w.row_bytes * w.M * w.N >> 20} MiB "
                          f"(> L2 between reuses)",
                    "parallelism": f"replicas x{world} (rows independent)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

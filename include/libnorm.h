@@ -5,7 +5,7 @@
  *   [Ch7]  "第 7 章 LayerNorm 与 RMSNorm" (CUDA 算子工程): §7.1 LayerNorm
  *          definition, §7.4 Welford, §7.4.1 parallel merge, §7.5 RMSNorm,
  *          §7.6 fused kernel structure (per-row statistics, mean/rstd saved),
- *          §7.7 backward formulas.
+ *          §7.7 backward formulas, §7.9 FP8 output for the next GEMM.
  *   [RMS2] "CUDA算子优化(2)：RMSNorm": §1 formula, §2 [B*T, C] layout.
  *   [T3]   "T3 讲解：LayerNorm / RMSNorm 的 forward": §② masking, biased
  *          variance, fp32 statistics; §④ host reshape to [M, N]; §⑤ fusion
@@ -271,6 +271,50 @@ norm_status rms_bwd_planned(const void* dy, const void* x, const void* w, void* 
 norm_status ln_bwd_noalloc(const void* dy, const void* x, const void* gamma, const float* mean,
                            const float* rstd, void* dx, float* dgamma, float* dbeta, int64_t M,
                            int64_t N, norm_dtype dtype, cudaStream_t stream);
+
+/*
+ * Norm with an FP8 output for the next GEMM ([Ch7] §7.9: the norm writes
+ * the GEMM's quantised input itself, as vLLM's static-scale fused kernels
+ * do, instead of writing y in high precision for a separate quantiser):
+ *   y8_ri = E4M3(y_ri / scale)
+ * with y as ln_fwd / rms_fwd compute it (in fp32), `scale` one fp32 value
+ * in device memory (a per-tensor static scale), E4M3 the OCP FP8 format
+ * (4 exponent, 3 fraction bits, finite only, largest 448) with
+ * round-to-nearest-even and saturation: magnitudes from 448 give +-448.
+ * y8 is [M, N] bytes (E4M3 codes), row stride N. mean and rstd as for
+ * ln_fwd. The scale must be finite and nonzero (not checked: it is read on
+ * the device). y8 may not overlap x.
+ */
+norm_status ln_fwd_fp8(const void* x, const void* gamma, const void* beta, const float* scale,
+                       void* y8, float* mean, float* rstd, int64_t M, int64_t N, float eps,
+                       norm_dtype dtype, cudaStream_t stream);
+
+norm_status rms_fwd_fp8(const void* x, const void* w, const float* scale, void* y8, int64_t M,
+                        int64_t N, float eps, norm_dtype dtype, cudaStream_t stream);
+
+/* The fused residual add with an FP8 output: h as for ln_fwd_add (h may be
+ * x or residual itself), y8 = E4M3(norm(h) / scale). */
+norm_status ln_fwd_add_fp8(const void* x, const void* residual, const void* gamma,
+                           const void* beta, const float* scale, void* h, void* y8, float* mean,
+                           float* rstd, int64_t M, int64_t N, float eps, norm_dtype dtype,
+                           cudaStream_t stream);
+
+norm_status rms_fwd_add_fp8(const void* x, const void* residual, const void* w,
+                            const float* scale, void* h, void* y8, int64_t M, int64_t N, float eps,
+                            norm_dtype dtype, cudaStream_t stream);
+
+/* The FP8-output calls with an explicit plan (residual == NULL: no fused
+ * add, h ignored); plans with `stages` != 0 return NORM_ERR_PLAN, and with
+ * a residual the fused add's 512-thread limit applies. */
+norm_status ln_fwd_fp8_planned(const void* x, const void* residual, const void* gamma,
+                               const void* beta, const float* scale, void* h, void* y8,
+                               float* mean, float* rstd, int64_t M, int64_t N, float eps,
+                               norm_dtype dtype, cudaStream_t stream, const norm_plan* plan);
+
+norm_status rms_fwd_fp8_planned(const void* x, const void* residual, const void* w,
+                                const float* scale, void* h, void* y8, int64_t M, int64_t N,
+                                float eps, norm_dtype dtype, cudaStream_t stream,
+                                const norm_plan* plan);
 
 /* Static description of a status code. */
 const char* norm_status_string(norm_status status);

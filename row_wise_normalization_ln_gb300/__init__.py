@@ -17,7 +17,8 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "ln_fwd", "rms_fwd", "ln_fwd_add", "rms_fwd_add", "ln_bwd", "rms_bwd", "make_plan", "make_bwd_plan", "NormPlan", "NormError", "LibraryNotBuilt", "library",
+    "ln_fwd", "rms_fwd", "ln_fwd_add", "rms_fwd_add", "ln_fwd_fp8", "rms_fwd_fp8", "ln_bwd", "rms_bwd",
+    "make_plan", "make_bwd_plan", "NormPlan", "NormError", "LibraryNotBuilt", "library",
     "NORM_F32", "NORM_BF16", "NORM_F16", "NORM_MAP_GROUP", "NORM_MAP_CTA",
 ]
 
@@ -97,10 +98,17 @@ def library() -> ctypes.CDLL:
     L.rms_bwd_planned.argtypes = L.rms_bwd.argtypes + [ctypes.POINTER(NormPlan)]
     L.norm_bwd_make_plan.argtypes = [i64, i64, i32, i32, i32, i32, ctypes.POINTER(NormPlan)]
     L.norm_bwd_workspace_bytes.argtypes = [ctypes.POINTER(NormPlan), i64, i32, ctypes.POINTER(sz)]
+    L.ln_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, f32, i32, vp]
+    L.rms_fwd_fp8.argtypes = [vp, vp, vp, vp, i64, i64, f32, i32, vp]
+    L.ln_fwd_add_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, f32, i32, vp]
+    L.rms_fwd_add_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, f32, i32, vp]
+    L.ln_fwd_fp8_planned.argtypes = L.ln_fwd_add_fp8.argtypes + [ctypes.POINTER(NormPlan)]
+    L.rms_fwd_fp8_planned.argtypes = L.rms_fwd_add_fp8.argtypes + [ctypes.POINTER(NormPlan)]
     for f in ("ln_fwd", "rms_fwd", "ln_fwd_planned", "rms_fwd_planned", "ln_fwd_add", "rms_fwd_add",
               "ln_fwd_add_planned", "rms_fwd_add_planned", "norm_make_plan", "norm_make_plan_add",
               "ln_bwd", "rms_bwd", "ln_bwd_planned", "rms_bwd_planned", "norm_bwd_make_plan",
-              "norm_bwd_workspace_bytes",
+              "norm_bwd_workspace_bytes", "ln_fwd_fp8", "rms_fwd_fp8", "ln_fwd_add_fp8", "rms_fwd_add_fp8",
+              "ln_fwd_fp8_planned", "rms_fwd_fp8_planned",
               "norm_last_cuda_error", "norm_abi_version"):
         getattr(L, f).restype = ctypes.c_int
     L.norm_status_string.argtypes = [ctypes.c_int]
@@ -380,3 +388,94 @@ def rms_bwd(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, eps: float = 1e-
     if st != NORM_OK:
         raise NormError(st, "rms_bwd")
     return dxt.view(x.shape), dwt
+
+
+def _scale_tensor(scale, device) -> torch.Tensor:
+    if isinstance(scale, torch.Tensor):
+        if scale.dtype != torch.float32 or scale.numel() != 1 or scale.device != device:
+            raise ValueError("scale must be one fp32 value on the input's device")
+        return scale.reshape(1)
+    return torch.tensor([float(scale)], dtype=torch.float32, device=device)
+
+
+def _fp8_out(out, x, x2) -> torch.Tensor:
+    y8 = out if out is not None else torch.empty(x2.shape, dtype=torch.uint8, device=x.device)
+    if y8.numel() != x2.numel() or not y8.is_contiguous() or y8.element_size() != 1 or y8.device != x.device:
+        raise ValueError("out must be a contiguous one-byte tensor of x's shape on its device")
+    return y8
+
+
+def ln_fwd_fp8(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, scale, eps: float = 1e-5, *,
+               residual: Optional[torch.Tensor] = None, h_out: Optional[torch.Tensor] = None,
+               out: Optional[torch.Tensor] = None, mean: Optional[torch.Tensor] = None,
+               rstd: Optional[torch.Tensor] = None, stats: bool = True,
+               stream: Optional[torch.cuda.Stream] = None, plan=None):
+    """LayerNorm forward with an FP8 E4M3 output, ``y8 = E4M3(y / scale)``
+    (uint8 codes; ``.view(torch.float8_e4m3fn)`` reads them as fp8).
+    ``scale``: a float or one fp32 CUDA value. Returns ``(y8, mean, rstd)``,
+    or ``(h, y8, mean, rstd)`` with ``residual`` (fused add, h = x + r)."""
+    if not x.is_cuda:
+        raise ValueError("ln_fwd_fp8 needs a CUDA tensor")
+    code = _dtype_code(x.dtype)
+    x2 = _rows(x)
+    M, N = x2.shape
+    g = _param(gamma, x, "gamma")
+    b = _param(beta, x, "beta")
+    sc = _scale_tensor(scale, x.device)
+    y8 = _fp8_out(out, x, x2)
+    r2 = _residual(residual, x) if residual is not None else None
+    hh = _out(h_out, x, x2, "h_out") if residual is not None else None
+    mean, rstd = _stats(M, x, mean, rstd, stats)
+    L = library()
+    with torch.cuda.device(x.device):
+        s = _stream_handle(stream, x.device)
+        if plan is not None:
+            st = L.ln_fwd_fp8_planned(x2.data_ptr(), _ptr(r2), g.data_ptr(), b.data_ptr(), sc.data_ptr(), _ptr(hh),
+                                      y8.data_ptr(), _ptr(mean), _ptr(rstd), M, N, float(eps), code, s,
+                                      _plan_ptr(plan))
+        elif residual is not None:
+            st = L.ln_fwd_add_fp8(x2.data_ptr(), r2.data_ptr(), g.data_ptr(), b.data_ptr(), sc.data_ptr(),
+                                  hh.data_ptr(), y8.data_ptr(), _ptr(mean), _ptr(rstd), M, N, float(eps), code, s)
+        else:
+            st = L.ln_fwd_fp8(x2.data_ptr(), g.data_ptr(), b.data_ptr(), sc.data_ptr(), y8.data_ptr(), _ptr(mean),
+                              _ptr(rstd), M, N, float(eps), code, s)
+    if st != NORM_OK:
+        raise NormError(st, "ln_fwd_fp8")
+    y8 = y8.view(x.shape)
+    if residual is not None:
+        return hh.view(x.shape), y8, mean, rstd
+    return y8, mean, rstd
+
+
+def rms_fwd_fp8(x: torch.Tensor, w: torch.Tensor, scale, eps: float = 1e-6, *,
+                residual: Optional[torch.Tensor] = None, h_out: Optional[torch.Tensor] = None,
+                out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None, plan=None):
+    """RMSNorm forward with an FP8 E4M3 output; returns ``y8``, or
+    ``(h, y8)`` with ``residual``."""
+    if not x.is_cuda:
+        raise ValueError("rms_fwd_fp8 needs a CUDA tensor")
+    code = _dtype_code(x.dtype)
+    x2 = _rows(x)
+    M, N = x2.shape
+    wv = _param(w, x, "w")
+    sc = _scale_tensor(scale, x.device)
+    y8 = _fp8_out(out, x, x2)
+    r2 = _residual(residual, x) if residual is not None else None
+    hh = _out(h_out, x, x2, "h_out") if residual is not None else None
+    L = library()
+    with torch.cuda.device(x.device):
+        s = _stream_handle(stream, x.device)
+        if plan is not None:
+            st = L.rms_fwd_fp8_planned(x2.data_ptr(), _ptr(r2), wv.data_ptr(), sc.data_ptr(), _ptr(hh),
+                                       y8.data_ptr(), M, N, float(eps), code, s, _plan_ptr(plan))
+        elif residual is not None:
+            st = L.rms_fwd_add_fp8(x2.data_ptr(), r2.data_ptr(), wv.data_ptr(), sc.data_ptr(), hh.data_ptr(),
+                                   y8.data_ptr(), M, N, float(eps), code, s)
+        else:
+            st = L.rms_fwd_fp8(x2.data_ptr(), wv.data_ptr(), sc.data_ptr(), y8.data_ptr(), M, N, float(eps), code, s)
+    if st != NORM_OK:
+        raise NormError(st, "rms_fwd_fp8")
+    y8 = y8.view(x.shape)
+    if residual is not None:
+        return hh.view(x.shape), y8
+    return y8

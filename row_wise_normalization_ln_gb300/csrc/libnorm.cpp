@@ -121,10 +121,11 @@ norm_status make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_aligned, 
 
 // Validate an explicit plan against the call; derive `rounds`. The fused
 // residual add (`add`) has no ring kernel and smaller CTAs.
-norm_status check_plan(const norm_plan& in, int64_t N, norm_dtype dtype, bool all_aligned, bool add,
+norm_status check_plan(const norm_plan& in, int64_t N, norm_dtype dtype, bool all_aligned, bool add, bool q8,
                        norm_plan* out) {
     norm_plan p = in;
     if (add && (p.stages != 0 || p.threads > libnorm::kFusedMaxThreads)) return NORM_ERR_PLAN;
+    if (q8 && p.stages != 0) return NORM_ERR_PLAN;
     const int s = elem_size(dtype);
     if (p.mapping != NORM_MAP_GROUP && p.mapping != NORM_MAP_CTA) return NORM_ERR_PLAN;
     if (p.vec_elems != 1) {
@@ -275,23 +276,29 @@ int device_sm_count(int* dev_out) {
 
 using Launcher = cudaError_t (*)(const norm_plan&, const NormArgs&, cudaStream_t, int, int);
 
-Launcher pick_launcher(bool ln, bool add, norm_dtype dtype) {
+Launcher pick_launcher(bool ln, bool add, bool q8, norm_dtype dtype) {
     using namespace libnorm;
-    // [add][ln][dtype]
-    static const Launcher table[2][2][3] = {
-        {{launch_rms_f32, launch_rms_bf16, launch_rms_f16}, {launch_ln_f32, launch_ln_bf16, launch_ln_f16}},
-        {{launch_rms_add_f32, launch_rms_add_bf16, launch_rms_add_f16},
-         {launch_ln_add_f32, launch_ln_add_bf16, launch_ln_add_f16}}};
-    return table[add][ln][dtype];
+    // [q8][add][ln][dtype]
+    static const Launcher table[2][2][2][3] = {
+        {{{launch_rms_f32, launch_rms_bf16, launch_rms_f16}, {launch_ln_f32, launch_ln_bf16, launch_ln_f16}},
+         {{launch_rms_add_f32, launch_rms_add_bf16, launch_rms_add_f16},
+          {launch_ln_add_f32, launch_ln_add_bf16, launch_ln_add_f16}}},
+        {{{launch_rms_fp8_f32, launch_rms_fp8_bf16, launch_rms_fp8_f16},
+          {launch_ln_fp8_f32, launch_ln_fp8_bf16, launch_ln_fp8_f16}},
+         {{launch_rms_add_fp8_f32, launch_rms_add_fp8_bf16, launch_rms_add_fp8_f16},
+          {launch_ln_add_fp8_f32, launch_ln_add_fp8_bf16, launch_ln_add_fp8_f16}}}};
+    return table[q8][add][ln][dtype];
 }
 
-// a.res != null selects the fused residual add.
+// a.res != null selects the fused residual add; a.qscale != null the FP8
+// output.
 norm_status run(bool ln, const NormArgs& a, norm_dtype dtype, bool all_aligned, cudaStream_t stream,
                 const norm_plan* user_plan) {
     const bool add = a.res != nullptr;
+    const bool q8 = a.qscale != nullptr;
     norm_plan plan;
     if (user_plan) {
-        const norm_status st = check_plan(*user_plan, a.N, dtype, all_aligned, add, &plan);
+        const norm_status st = check_plan(*user_plan, a.N, dtype, all_aligned, add, q8, &plan);
         if (st != NORM_OK) return st;
     }
     int dev = 0;
@@ -302,7 +309,7 @@ norm_status run(bool ln, const NormArgs& a, norm_dtype dtype, bool all_aligned, 
     args.group = plan.group;
     args.rounds = plan.rounds;
     args.stages = plan.stages;
-    const cudaError_t e = pick_launcher(ln, add, dtype)(plan, args, stream, sms, dev);
+    const cudaError_t e = pick_launcher(ln, add, q8, dtype)(plan, args, stream, sms, dev);
     if (e != cudaSuccess) {
         g_last_cuda_error = static_cast<int>(e);
         return NORM_ERR_CUDA;
@@ -318,7 +325,7 @@ norm_status ln_impl(const void* x, const void* gamma, const void* beta, void* y,
     if (M == 0) return NORM_OK;
     if (!x || !gamma || !beta || !y) return NORM_ERR_ARG;
     const bool al = aligned16(x) && aligned16(y) && aligned16(gamma) && aligned16(beta);
-    NormArgs a{x, gamma, beta, y, mean, rstd, nullptr, nullptr, M, static_cast<int32_t>(N), eps, 0, 1, 0};
+    NormArgs a{x, gamma, beta, y, mean, rstd, nullptr, nullptr, nullptr, M, static_cast<int32_t>(N), eps, 0, 1, 0};
     return run(true, a, dtype, al, stream, plan);
 }
 
@@ -330,7 +337,7 @@ norm_status rms_impl(const void* x, const void* w, void* y, int64_t M, int64_t N
     if (M == 0) return NORM_OK;
     if (!x || !w || !y) return NORM_ERR_ARG;
     const bool al = aligned16(x) && aligned16(y) && aligned16(w);
-    NormArgs a{x, w, nullptr, y, nullptr, nullptr, nullptr, nullptr, M, static_cast<int32_t>(N), eps, 0, 1, 0};
+    NormArgs a{x, w, nullptr, y, nullptr, nullptr, nullptr, nullptr, nullptr, M, static_cast<int32_t>(N), eps, 0, 1, 0};
     return run(false, a, dtype, al, stream, plan);
 }
 
@@ -346,7 +353,7 @@ norm_status ln_add_impl(const void* x, const void* res, const void* gamma, const
     if (!x || !res || !gamma || !beta || !h || !y || h == y) return NORM_ERR_ARG;
     const bool al = aligned16(x) && aligned16(res) && aligned16(h) && aligned16(y) && aligned16(gamma) &&
                     aligned16(beta);
-    NormArgs a{x, gamma, beta, y, mean, rstd, res, h, M, static_cast<int32_t>(N), eps, 0, 1, 0};
+    NormArgs a{x, gamma, beta, y, mean, rstd, res, h, nullptr, M, static_cast<int32_t>(N), eps, 0, 1, 0};
     return run(true, a, dtype, al, stream, plan);
 }
 
@@ -358,8 +365,26 @@ norm_status rms_add_impl(const void* x, const void* res, const void* w, void* h,
     if (M == 0) return NORM_OK;
     if (!x || !res || !w || !h || !y || h == y) return NORM_ERR_ARG;
     const bool al = aligned16(x) && aligned16(res) && aligned16(h) && aligned16(y) && aligned16(w);
-    NormArgs a{x, w, nullptr, y, nullptr, nullptr, res, h, M, static_cast<int32_t>(N), eps, 0, 1, 0};
+    NormArgs a{x, w, nullptr, y, nullptr, nullptr, res, h, nullptr, M, static_cast<int32_t>(N), eps, 0, 1, 0};
     return run(false, a, dtype, al, stream, plan);
+}
+
+// FP8 output: y8 holds one E4M3 byte per element; scale is one fp32 value
+// in device memory. With a residual (res != null) also h = x + res.
+norm_status fp8_impl(bool ln, const void* x, const void* res, const void* gamma, const void* beta,
+                     const float* scale, void* h, void* y8, float* mean, float* rstd, int64_t M, int64_t N,
+                     float eps, norm_dtype dtype, cudaStream_t stream, const norm_plan* plan) {
+    norm_status st = check_sizes(M, N, dtype);
+    if (st != NORM_OK) return st;
+    if (!std::isfinite(eps) || eps < 0.f) return NORM_ERR_ARG;
+    if (M == 0) return NORM_OK;
+    if (!x || !gamma || (ln && !beta) || !scale || !y8) return NORM_ERR_ARG;
+    if (res && (!h || h == y8)) return NORM_ERR_ARG;
+    bool al = aligned16(x) && aligned16(y8) && aligned16(gamma) && (!ln || aligned16(beta));
+    if (res) al = al && aligned16(res) && aligned16(h);
+    NormArgs a{x, gamma, ln ? beta : nullptr, y8, ln ? mean : nullptr, ln ? rstd : nullptr, res, res ? h : nullptr,
+               scale, M, static_cast<int32_t>(N), eps, 0, 1, 0};
+    return run(ln, a, dtype, al, stream, plan);
 }
 
 // Backward: dx = d(loss)/dx for y = norm(x); column gradients in fp32.
@@ -498,6 +523,43 @@ norm_status rms_fwd_add_planned(const void* x, const void* residual, const void*
                                 int64_t N, float eps, norm_dtype dtype, cudaStream_t stream,
                                 const norm_plan* plan) {
     return rms_add_impl(x, residual, w, h, y, M, N, eps, dtype, stream, plan);
+}
+
+norm_status ln_fwd_fp8(const void* x, const void* gamma, const void* beta, const float* scale, void* y8, float* mean,
+                       float* rstd, int64_t M, int64_t N, float eps, norm_dtype dtype, cudaStream_t stream) {
+    return fp8_impl(true, x, nullptr, gamma, beta, scale, nullptr, y8, mean, rstd, M, N, eps, dtype, stream, nullptr);
+}
+
+norm_status rms_fwd_fp8(const void* x, const void* w, const float* scale, void* y8, int64_t M, int64_t N, float eps,
+                        norm_dtype dtype, cudaStream_t stream) {
+    return fp8_impl(false, x, nullptr, w, nullptr, scale, nullptr, y8, nullptr, nullptr, M, N, eps, dtype, stream,
+                    nullptr);
+}
+
+norm_status ln_fwd_add_fp8(const void* x, const void* residual, const void* gamma, const void* beta,
+                           const float* scale, void* h, void* y8, float* mean, float* rstd, int64_t M, int64_t N,
+                           float eps, norm_dtype dtype, cudaStream_t stream) {
+    if (!residual) return NORM_ERR_ARG;
+    return fp8_impl(true, x, residual, gamma, beta, scale, h, y8, mean, rstd, M, N, eps, dtype, stream, nullptr);
+}
+
+norm_status rms_fwd_add_fp8(const void* x, const void* residual, const void* w, const float* scale, void* h,
+                            void* y8, int64_t M, int64_t N, float eps, norm_dtype dtype, cudaStream_t stream) {
+    if (!residual) return NORM_ERR_ARG;
+    return fp8_impl(false, x, residual, w, nullptr, scale, h, y8, nullptr, nullptr, M, N, eps, dtype, stream,
+                    nullptr);
+}
+
+norm_status ln_fwd_fp8_planned(const void* x, const void* residual, const void* gamma, const void* beta,
+                               const float* scale, void* h, void* y8, float* mean, float* rstd, int64_t M, int64_t N,
+                               float eps, norm_dtype dtype, cudaStream_t stream, const norm_plan* plan) {
+    return fp8_impl(true, x, residual, gamma, beta, scale, h, y8, mean, rstd, M, N, eps, dtype, stream, plan);
+}
+
+norm_status rms_fwd_fp8_planned(const void* x, const void* residual, const void* w, const float* scale, void* h,
+                                void* y8, int64_t M, int64_t N, float eps, norm_dtype dtype, cudaStream_t stream,
+                                const norm_plan* plan) {
+    return fp8_impl(false, x, residual, w, nullptr, scale, h, y8, nullptr, nullptr, M, N, eps, dtype, stream, plan);
 }
 
 norm_status norm_make_plan(int64_t M, int64_t N, norm_dtype dtype, int aligned, int num_sms, norm_plan* plan) {

@@ -23,6 +23,7 @@ struct NormArgs {
     float* rstd;        // [M] or null (LayerNorm only)
     const void* res;    // [M, N] residual (fused residual add only)
     void* h;            // [M, N] h = x + res (fused residual add only)
+    const float* qscale;  // FP8 output only: the static scale (y is then uint8 E4M3 codes)
     int64_t M;
     int32_t N;
     float eps;
@@ -77,6 +78,20 @@ cudaError_t launch_rms_f32(const norm_plan& plan, const NormArgs& a, cudaStream_
 cudaError_t launch_rms_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
 cudaError_t launch_ln_f16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
 cudaError_t launch_rms_f16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+// FP8 E4M3 output (a.qscale set; y holds one byte per element), without and
+// with the fused residual add.
+cudaError_t launch_ln_fp8_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_ln_fp8_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_ln_fp8_f16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_rms_fp8_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_rms_fp8_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_rms_fp8_f16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_ln_add_fp8_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_ln_add_fp8_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_ln_add_fp8_f16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_rms_add_fp8_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_rms_add_fp8_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
+cudaError_t launch_rms_add_fp8_f16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
 // The same with the fused residual add (a.res, a.h set).
 cudaError_t launch_ln_add_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
 cudaError_t launch_ln_add_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);

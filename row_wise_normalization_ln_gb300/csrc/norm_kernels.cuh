@@ -131,6 +131,16 @@ struct Ops<float, 4> {
         return make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
                           __float_as_uint(o[3]));
     }
+    // The same fp32 values, unrounded (for a quantised output).
+    static __device__ __forceinline__ void ln_vals(const Raw& r, float K, float rs, float nmr, const Raw& g,
+                                                   const Raw& b, float* o) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = fmaf(fmaf(e(r, i) - K, rs, nmr), e(g, i), e(b, i));
+    }
+    static __device__ __forceinline__ void rms_vals(const Raw& r, float rs, const Raw& w, float* o) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = (e(r, i) * e(w, i)) * rs;
+    }
     // Residual add h = x + r, each element rounded once to fp32.
     static __device__ __forceinline__ Raw add_round(const Raw& x, const Raw& r) {
         return make_uint4(__float_as_uint(e(x, 0) + e(r, 0)), __float_as_uint(e(x, 1) + e(r, 1)),
@@ -198,6 +208,26 @@ struct Ops16 {
         }
         return make_uint4(o[0], o[1], o[2], o[3]);
     }
+    static __device__ __forceinline__ void ln_vals(const Raw& r, float K, float rs, float nmr, const Raw& g,
+                                                   const Raw& b, float* o) {
+        const float2 nk = f2_splat(-K), rs2 = f2_splat(rs), nm2 = f2_splat(nmr);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 y = __ffma2_rn(__ffma2_rn(__fadd2_rn(P::widen(w(r, i)), nk), rs2, nm2),
+                                        P::widen(w(g, i)), P::widen(w(b, i)));
+            o[2 * i] = y.x;
+            o[2 * i + 1] = y.y;
+        }
+    }
+    static __device__ __forceinline__ void rms_vals(const Raw& r, float rs, const Raw& wt, float* o) {
+        const float2 rs2 = f2_splat(rs);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 y = __fmul2_rn(__fmul2_rn(P::widen(w(r, i)), P::widen(w(wt, i))), rs2);
+            o[2 * i] = y.x;
+            o[2 * i + 1] = y.y;
+        }
+    }
     // Residual add h = x + r: fp32 carries at least 2p + 2 bits for both
     // 16-bit formats (p = 8 for bf16, 11 for fp16), so rounding the fp32 sum
     // to T rounds the exact sum once.
@@ -246,6 +276,10 @@ struct ScalarOps {
         return from_float(fmaf(fmaf(e(r) - K, rs, nmr), e(g), e(b)));
     }
     static __device__ __forceinline__ Raw rms_out(Raw r, float rs, Raw wt) { return from_float((e(r) * e(wt)) * rs); }
+    static __device__ __forceinline__ void ln_vals(Raw r, float K, float rs, float nmr, Raw g, Raw b, float* o) {
+        o[0] = fmaf(fmaf(e(r) - K, rs, nmr), e(g), e(b));
+    }
+    static __device__ __forceinline__ void rms_vals(Raw r, float rs, Raw wt, float* o) { o[0] = (e(r) * e(wt)) * rs; }
     static __device__ __forceinline__ Raw add_round(Raw x, Raw r) { return from_float(e(x) + e(r)); }
     static __device__ __forceinline__ Raw from_float(float v) {
         if constexpr (sizeof(T) == 4)
@@ -288,6 +322,31 @@ template <class T>
 __device__ __forceinline__ float first_elem_add(const T* xrow, const T* rrow) {
     using SO = ScalarOps<T>;
     return SO::e(SO::add_round(SO::load(xrow), SO::load(rrow)));
+}
+
+// FP8 output ([Ch7] §7.9: the norm writes the next GEMM's quantised input):
+// VEC fp32 values times the inverse of the static scale, converted to OCP
+// FP8 E4M3 with the hardware's round-to-nearest-even, saturating conversion
+// (magnitudes from 448 give +-448), stored as VEC bytes.
+template <int VEC>
+__device__ __forceinline__ void store_e4m3(uint8_t* p, const float* o, float inv) {
+    if constexpr (VEC == 1) {
+        *p = static_cast<uint8_t>(__nv_cvt_float_to_fp8(o[0] * inv, __NV_SATFINITE, __NV_E4M3));
+    } else {
+        uint32_t q[VEC / 4];
+#pragma unroll
+        for (int k = 0; k < VEC / 4; ++k) {
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(o[4 * k] * inv, o[4 * k + 1] * inv),
+                                                         __NV_SATFINITE, __NV_E4M3);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(o[4 * k + 2] * inv, o[4 * k + 3] * inv),
+                                                         __NV_SATFINITE, __NV_E4M3);
+            q[k] = lo | (hi << 16);
+        }
+        if constexpr (VEC == 4)
+            *reinterpret_cast<uint32_t*>(p) = q[0];
+        else
+            *reinterpret_cast<uint2*>(p) = make_uint2(q[0], q[1]);
+    }
 }
 
 // ================================================================== a thread's slice
@@ -377,6 +436,32 @@ struct Slice {
                     O::store(y + j * stride, O::rms_out(raw[j], rs, O::load_param(g + j * stride)));
             }
     }
+    // emit with an FP8 E4M3 output: the same fp32 values, scaled by `inv`
+    // (1 / the static scale) and quantised; `y8` points at this thread's
+    // first access in bytes (one byte per element).
+    __device__ __forceinline__ void emit_q8(const T* g, const T* b, uint8_t* y8, int stride, int nvalid, float mu,
+                                            float rs, float inv) const {
+        const float nmr = -mu * rs;
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            if (j < nvalid) {
+                float o[VEC];
+                if constexpr (LN)
+                    O::ln_vals(raw[j], K, rs, nmr, O::load_param(g + j * stride), O::load_param(b + j * stride), o);
+                else
+                    O::rms_vals(raw[j], rs, O::load_param(g + j * stride), o);
+                store_e4m3<VEC>(y8 + j * stride, o, inv);
+            }
+    }
+    // Output step of either kind.
+    template <bool Q8>
+    __device__ __forceinline__ void out(const T* g, const T* b, void* y, int64_t offset, int stride, int nvalid,
+                                        float mu, float rs, float inv) const {
+        if constexpr (Q8)
+            emit_q8(g, b, static_cast<uint8_t*>(y) + offset, stride, nvalid, mu, rs, inv);
+        else
+            emit(g, b, static_cast<T*>(y) + offset, stride, nvalid, mu, rs);
+    }
 };
 
 // How many of a thread's V runs lie inside a row of `nacc` accesses when its
@@ -445,7 +530,7 @@ __device__ __forceinline__ void row_stats(RowReduceSmem& red, float n_t, float s
 // of a group holds accesses l, l+G, l+2G, ... (the G lanes of a group read G
 // consecutive accesses per instruction). The statistics meet in xor
 // butterflies over the group. ADD as for norm_fwd_cta.
-template <class T, int VEC, int V, bool LN, bool ADD>
+template <class T, int VEC, int V, bool LN, bool ADD, bool Q8>
 __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_group(const NormArgs a) {
     using S = Slice<T, VEC, V, LN>;
     const int G = a.group;
@@ -462,6 +547,7 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_group(
     const T* b = static_cast<const T*>(a.beta) + gl * VEC;
     grid_release();
     grid_wait();
+    const float inv = Q8 ? 1.f / *a.qscale : 0.f;
 
     for (int64_t rb = blockIdx.x; rb * rows_per_cta < a.M; rb += gridDim.x) {
         const int64_t row = rb * rows_per_cta + tid / G;
@@ -491,7 +577,7 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_group(
         } else {
             rs = rsqrtf(group_sum(s.sumsq(nv), G) * invN + a.eps);
         }
-        s.emit(g, b, static_cast<T*>(a.y) + row * a.N + gl * VEC, stride, nv, mu, rs);
+        s.template out<Q8>(g, b, a.y, row * a.N + gl * VEC, stride, nv, mu, rs, inv);
         if constexpr (ADD) s.store_h(static_cast<T*>(a.h) + row * a.N + gl * VEC, stride, nv);
     }
 }
@@ -513,7 +599,7 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_group(
 // store h as soon as it is formed and the output pass re-reads h, not x and
 // r. Every thread re-reads only its own accesses, so h (and y) may be the x
 // or r buffer itself.
-template <class T, int VEC, int V, bool LN, bool CL, bool ADD>
+template <class T, int VEC, int V, bool LN, bool CL, bool ADD, bool Q8>
 __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(const NormArgs a) {
     using S = Slice<T, VEC, V, LN>;
     __shared__ RowReduceSmem red;
@@ -536,11 +622,11 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
     const float invN = 1.f / static_cast<float>(a.N);
     grid_release();
     grid_wait();
+    const float inv = Q8 ? 1.f / *a.qscale : 0.f;
 
     for (int64_t row = first_row; row < a.M; row += row_step) {
         const T* xr = static_cast<const T*>(a.x) + row * a.N;
         const T* rr = ADD ? static_cast<const T*>(a.res) + row * a.N : nullptr;
-        T* yr = static_cast<T*>(a.y) + row * a.N;
         S s;
         const float K = LN ? (ADD ? first_elem_add(xr, rr) : first_elem(xr)) : 0.f;
         s.set_shift(K);
@@ -589,8 +675,8 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
                     nv = valid_runs(nacc, f, 32, V);
                     s.load(hr + f * VEC, stride, nv);  // only this thread wrote h there
                 }
-                s.emit(static_cast<const T*>(a.gamma) + f * VEC, static_cast<const T*>(a.beta) + f * VEC,
-                       yr + f * VEC, stride, nv, mu, rs);
+                s.template out<Q8>(static_cast<const T*>(a.gamma) + f * VEC, static_cast<const T*>(a.beta) + f * VEC,
+                                   a.y, row * a.N + f * VEC, stride, nv, mu, rs, inv);
                 if (r == 0) s.store_h(hr + f * VEC, stride, nv);
             }
         } else {
@@ -600,8 +686,8 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
                     nv = valid_runs(nacc, f, 32, V);
                     s.load(xr + f * VEC, stride, nv);
                 }
-                s.emit(static_cast<const T*>(a.gamma) + f * VEC, static_cast<const T*>(a.beta) + f * VEC,
-                       yr + f * VEC, stride, nv, mu, rs);
+                s.template out<Q8>(static_cast<const T*>(a.gamma) + f * VEC, static_cast<const T*>(a.beta) + f * VEC,
+                                   a.y, row * a.N + f * VEC, stride, nv, mu, rs, inv);
             }
         }
     }
@@ -707,19 +793,19 @@ __global__ void __launch_bounds__(1024) norm_fwd_pipe(const NormArgs a) {
 template <class T, bool LN>
 using KernelFn = void (*)(const NormArgs);
 
-template <class T, bool LN, bool ADD, int VEC, int V>
+template <class T, bool LN, bool ADD, bool Q8, int VEC, int V>
 KernelFn<T, LN> pick_cta(bool cl) {
-    return cl ? norm_fwd_cta<T, VEC, V, LN, true, ADD> : norm_fwd_cta<T, VEC, V, LN, false, ADD>;
+    return cl ? norm_fwd_cta<T, VEC, V, LN, true, ADD, Q8> : norm_fwd_cta<T, VEC, V, LN, false, ADD, Q8>;
 }
 
-template <class T, bool LN, bool ADD, int VEC>
+template <class T, bool LN, bool ADD, bool Q8, int VEC>
 KernelFn<T, LN> pick_kernel(int mapping, int per_thread, bool cl) {
     const bool group = mapping == NORM_MAP_GROUP;
     switch (per_thread) {
-        case 1: return group ? norm_fwd_group<T, VEC, 1, LN, ADD> : pick_cta<T, LN, ADD, VEC, 1>(cl);
-        case 2: return group ? norm_fwd_group<T, VEC, 2, LN, ADD> : pick_cta<T, LN, ADD, VEC, 2>(cl);
-        case 4: return group ? norm_fwd_group<T, VEC, 4, LN, ADD> : pick_cta<T, LN, ADD, VEC, 4>(cl);
-        case 8: return group ? norm_fwd_group<T, VEC, 8, LN, ADD> : pick_cta<T, LN, ADD, VEC, 8>(cl);
+        case 1: return group ? norm_fwd_group<T, VEC, 1, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 1>(cl);
+        case 2: return group ? norm_fwd_group<T, VEC, 2, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 2>(cl);
+        case 4: return group ? norm_fwd_group<T, VEC, 4, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 4>(cl);
+        case 8: return group ? norm_fwd_group<T, VEC, 8, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 8>(cl);
         default: return nullptr;
     }
 }
@@ -780,14 +866,15 @@ cudaError_t allow_smem(int per_thread, bool cl, int dev) {
     }
 }
 
-// ADD: the fused residual add (register kernels only; no ring).
-template <class T, bool LN, bool ADD>
+// ADD: the fused residual add; Q8: FP8 E4M3 output (register kernels only;
+// no ring).
+template <class T, bool LN, bool ADD, bool Q8 = false>
 cudaError_t launch_norm(const norm_plan& p, const NormArgs& a, cudaStream_t stream, int num_sms, int dev) {
     KernelFn<T, LN> k;
     size_t smem = 0;
     const bool cl = p.mapping == NORM_MAP_CTA && p.cluster > 1;
     if (p.stages > 0) {
-        if constexpr (ADD) {
+        if constexpr (ADD || Q8) {
             return cudaErrorInvalidValue;
         } else {
             k = pick_pipe<T, LN>(p.per_thread, cl);
@@ -797,8 +884,8 @@ cudaError_t launch_norm(const norm_plan& p, const NormArgs& a, cudaStream_t stre
             if (e != cudaSuccess) return e;
         }
     } else {
-        k = p.vec_elems == 1 ? pick_kernel<T, LN, ADD, 1>(p.mapping, p.per_thread, cl)
-                             : pick_kernel<T, LN, ADD, ElemVec<T>::value>(p.mapping, p.per_thread, cl);
+        k = p.vec_elems == 1 ? pick_kernel<T, LN, ADD, Q8, 1>(p.mapping, p.per_thread, cl)
+                             : pick_kernel<T, LN, ADD, Q8, ElemVec<T>::value>(p.mapping, p.per_thread, cl);
         if (k == nullptr) return cudaErrorInvalidValue;
     }
     cudaLaunchConfig_t cfg = {};

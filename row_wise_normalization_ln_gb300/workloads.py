@@ -22,6 +22,10 @@ Workloads (shapes and value distributions of the source pages):
   add_*                    the fused residual add + norm on the shape and
                            recipe of the workload it names: the residual r is
                            drawn from the same recipe, after the parameters.
+  fp8_*                    the forward with an FP8 E4M3 output (static scale
+                           `qscale`, chosen so the outputs span the format:
+                           |y| <= 2 for the U(-1,1) rows, <= 16 for the
+                           outlier rows) on the shape and recipe named.
   bwd_*                    the backward on the shape and recipe of the
                            workload it names: the upstream gradient
                            dy ~ N(0,1) is drawn after the parameters.
@@ -44,6 +48,7 @@ class Workload:
     recipe: str    # key of the value distribution below
     add: bool = False  # fused residual add: h = x + r, y = norm(h)
     bwd: bool = False  # backward: dx (and the column gradients) from dy, x
+    qscale: float = 0.0  # FP8 E4M3 output with this static scale (0: output in the row dtype)
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -54,10 +59,21 @@ class Workload:
         return 4 if self.dtype == "f32" else 2
 
     @property
+    def fp8(self) -> bool:
+        return self.qscale > 0
+
+    @property
     def row_tensors(self) -> int:
         """[M, N] tensors one call moves: x, y; with the fused add also r, h;
         backward: dy, x, dx."""
         return 4 if self.add else 3 if self.bwd else 2
+
+    @property
+    def row_bytes(self) -> int:
+        """HBM bytes per element of the [M, N] tensors one call moves (an
+        FP8 output is one byte per element)."""
+        s = self.elem_size
+        return self.row_tensors * s - (s - 1 if self.fp8 else 0)
 
     def algorithmic_bytes(self, M: int | None = None) -> int:
         """HBM bytes one call must move. Forward: read x (and r), write y
@@ -73,11 +89,11 @@ class Workload:
             return 3 * M * self.N * s + self.N * s + stats + cols
         params = 2 if self.op == "ln" else 1
         stats = 8 * M if self.op == "ln" else 0
-        return self.row_tensors * M * self.N * s + params * self.N * s + stats
+        return self.row_bytes * M * self.N + params * self.N * s + stats + (4 if self.fp8 else 0)
 
     def scaled(self, M: int | None = None, N: int | None = None) -> "Workload":
         return Workload(self.name, self.op, self.dtype, M or self.M, N or self.N, self.eps, self.recipe, self.add,
-                        self.bwd)
+                        self.bwd, self.qscale)
 
 
 WORKLOADS = {
@@ -94,6 +110,10 @@ WORKLOADS = {
         Workload("add_rms_bf16_65536x2048", "rms", "bf16", 65536, 2048, 1e-6, "uniform_pm1", True),
         Workload("add_ln_bf16_4096x8192_outliers", "ln", "bf16", 4096, 8192, 1e-5, "offset_outliers", True),
         Workload("add_ln_f32_2048x65536", "ln", "f32", 2048, 65536, 1e-5, "normal31", True),
+        Workload("fp8_rms_bf16_8192x4096", "rms", "bf16", 8192, 4096, 1e-6, "uniform_pm1", qscale=2 / 448),
+        Workload("fp8_ln_bf16_4096x8192_outliers", "ln", "bf16", 4096, 8192, 1e-5, "offset_outliers",
+                 qscale=16 / 448),
+        Workload("fp8_add_rms_bf16_8192x4096", "rms", "bf16", 8192, 4096, 1e-6, "uniform_pm1", True, qscale=2 / 448),
         Workload("bwd_rms_f32_8192x4096", "rms", "f32", 8192, 4096, 1e-6, "uniform_pm1", bwd=True),
         Workload("bwd_ln_bf16_4096x8192_outliers", "ln", "bf16", 4096, 8192, 1e-5, "offset_outliers", bwd=True),
         Workload("bwd_rms_bf16_65536x2048", "rms", "bf16", 65536, 2048, 1e-6, "uniform_pm1", bwd=True),

@@ -278,3 +278,65 @@ def check_rms_bwd(dy, x, w, eps, dx, dw, rows=None) -> dict:
     tol_w = 2.0 ** -24 * (2 * M + 128) * np.abs(dy64 * x64 * r[:, None]).sum(axis=0)
     res["dw_worst_of_bound"] = _col_check(np_of(dw), dw_ref, tol_w, "dw")
     return res
+
+
+# ---------------------------------------------------------------- FP8 output
+#
+# The kernel forms y in fp32 and quantises y * (1/scale); the oracle
+# quantises the exact y / scale. An integer code is decided by floating
+# point, so the codes agree except where the exact value lies within the
+# kernel's fp32 error of a rounding boundary. The bar: the decoded code is
+# within half an E4M3 ulp of v = y / scale plus that slack (the fp32 floor
+# of y above, over the scale, plus 2^-21 |v| for the inverse scale and the
+# product), and magnitudes beyond 448 + slack give exactly +-448.
+
+E4M3_MAX = 448.0
+
+
+def ulp_e4m3(v: np.ndarray) -> np.ndarray:
+    a = np.abs(v)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.where(a > 0, np.maximum(e, -6), -6)
+    return np.exp2(e - 3)
+
+
+def check_fp8(q_gpu: np.ndarray, y_ref: np.ndarray, scale: float, floor_rows: np.ndarray) -> dict:
+    v = y_ref / scale
+    d = oracle.e4m3_values(q_gpu)
+    assert not np.isnan(d).any(), "NaN code"
+    slack = floor_rows[:, None] / scale + 2.0 ** -21 * np.abs(v)
+    sat = np.abs(v) >= E4M3_MAX + slack
+    assert np.all(d[sat] == np.sign(v[sat]) * E4M3_MAX), "saturated values must give +-448"
+    err = np.abs(d - v)
+    bound = 0.5 * ulp_e4m3(np.minimum(np.abs(v), E4M3_MAX)) + slack
+    bad = ~sat & (err > bound)
+    assert not bad.any(), f"{int(bad.sum())} FP8 codes farther than half an ulp (+ slack) from y / scale"
+    q_ref = oracle.quant_e4m3(y_ref, scale)
+    return {"codes_equal": int((q_gpu == q_ref).sum()), "n": int(q_gpu.size), "saturated": int(sat.sum())}
+
+
+def check_ln_fp8(x, gamma, beta, eps, scale, y8, mean=None, rstd=None, rows=None) -> dict:
+    xn, gn, bn = np_of(x), np_of(gamma), np_of(beta)
+    qn = y8.detach().cpu().contiguous().numpy().view(np.uint8)
+    mn = np_of(mean) if mean is not None else None
+    rn_ = np_of(rstd) if rstd is not None else None
+    if rows is not None:
+        xn, qn = xn[rows], qn[rows]
+        mn = mn[rows] if mn is not None else None
+        rn_ = rn_[rows] if rn_ is not None else None
+    e = oracle.eps_as_f32(eps)
+    y_ref, m_ref, r_ref = oracle.ln_fwd(xn, gn, bn, e)
+    floor = ln_floor(as_f64(xn), as_f64(gn), as_f64(bn), m_ref, r_ref)
+    res = check_fp8(qn, y_ref, scale, floor)
+    res.update(check_stats(mn, rn_, m_ref, r_ref, e))
+    return res
+
+
+def check_rms_fp8(x, w, eps, scale, y8, rows=None) -> dict:
+    xn, wn = np_of(x), np_of(w)
+    qn = y8.detach().cpu().contiguous().numpy().view(np.uint8)
+    if rows is not None:
+        xn, qn = xn[rows], qn[rows]
+    e = oracle.eps_as_f32(eps)
+    y_ref, r_ref = oracle.rms_fwd(xn, wn, e)
+    return check_fp8(qn, y_ref, scale, rms_floor(as_f64(xn), as_f64(wn), r_ref))

@@ -34,6 +34,7 @@ def test_header_declares_the_abi():
         "ln_fwd_add", "rms_fwd_add", "ln_fwd_add_planned", "rms_fwd_add_planned", "norm_make_plan_add",
         "ln_bwd", "rms_bwd", "ln_bwd_planned", "rms_bwd_planned", "norm_bwd_make_plan", "norm_bwd_workspace_bytes",
         "ln_bwd_noalloc",
+        "ln_fwd_fp8", "rms_fwd_fp8", "ln_fwd_add_fp8", "rms_fwd_add_fp8", "ln_fwd_fp8_planned", "rms_fwd_fp8_planned",
         "norm_status_string", "norm_last_cuda_error", "norm_abi_version"}
 
 
@@ -394,3 +395,21 @@ def test_bwd_plans_are_consistent(lib, dtype, ln, M):
         else:
             assert p["grid"] % p["group"] == 0 and p["grid"] >= p["group"]
             assert rn.bwd_workspace_bytes(p, N, ln) == p["grid"] // p["group"] * (2 if ln else 1) * N * 4
+
+
+
+# ---------------------------------------------------------------- FP8 output
+
+def test_fp8_argument_checks(lib):
+    S = ctypes.c_void_p(0x3000)
+    # no scale, no output, h == y8, bad sizes
+    assert lib.rms_fwd_fp8(P, P, None, Q, 4, 64, 1e-6, rn.NORM_F32, None) == rn.NORM_ERR_ARG
+    assert lib.rms_fwd_fp8(P, P, S, None, 4, 64, 1e-6, rn.NORM_F32, None) == rn.NORM_ERR_ARG
+    assert lib.rms_fwd_add_fp8(P, P, P, S, Q, Q, 4, 64, 1e-6, rn.NORM_BF16, None) == rn.NORM_ERR_ARG
+    assert lib.ln_fwd_fp8(P, P, P, S, Q, None, None, 4, 0, 1e-5, rn.NORM_F32, None) == rn.NORM_ERR_ARG
+    assert lib.ln_fwd_fp8(P, P, None, S, Q, None, None, 4, 64, 1e-5, rn.NORM_F32, None) == rn.NORM_ERR_ARG
+    assert lib.ln_fwd_fp8(None, None, None, None, None, None, None, 0, 64, 1e-5, rn.NORM_F16, None) == rn.NORM_OK
+    # no ring plans with an FP8 output
+    p = _plan(stages=3, grid=0)
+    assert lib.rms_fwd_fp8_planned(P, None, P, S, None, Q, 4, 1000, 1e-6, rn.NORM_F32, None,
+                                   ctypes.byref(p)) == rn.NORM_ERR_PLAN
