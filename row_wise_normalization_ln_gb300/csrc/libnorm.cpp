@@ -187,12 +187,6 @@ norm_status bwd_make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_align
         threads = round_up(ceil_div(nacc, cluster * per), 32);
     }
     if (threads > kBwdMaxThreads) return NORM_ERR_ARG;  // the row does not fit one round of a cluster
-    // Rows of 512 to 1024 accesses: 512 threads of half the registers each
-    // (measured faster than 256 threads of full ones).
-    while (cluster == 1 && per > 1 && threads <= 256 && nacc >= 512) {
-        per /= 2;
-        threads = round_up(ceil_div(nacc, per), 32);
-    }
     while (per > 1 && threads < 64) {
         per /= 2;
         threads = round_up(ceil_div(nacc, cluster * per), 32);
@@ -204,10 +198,10 @@ norm_status bwd_make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_align
     p->cluster = static_cast<int32_t>(cluster);
     p->rounds = 1;
     // Persistent grid of at most 1024 threads and 6 CTAs per SM in whole
-    // clusters (the launch takes fewer if fewer fit at once). CTAs that each take their own
-    // rows add their column sums in clusters of 2 (of 8 for small CTAs, many
-    // of which share an SM): the partial rows halve, and such clusters are
-    // easy to place.
+    // clusters (the launch takes fewer if fewer fit at once). CTAs that each
+    // take their own rows add their column sums in clusters of 4 (of 8 for
+    // small CTAs, many of which share an SM): fewer partial rows, and such
+    // clusters are easy to place (measured faster than 2 or 8).
     const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>(6, 1024 / threads));
     if (cluster > 1) {
         const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(M, num_sms * per_sm / cluster));
@@ -215,7 +209,7 @@ norm_status bwd_make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_align
         p->grid = M > 0 ? clusters * cluster : 0;
     } else {
         const int64_t ctas = std::min<int64_t>(M, num_sms * per_sm);
-        const int64_t want = threads <= 128 ? kMaxCluster : 2;
+        const int64_t want = threads <= 128 ? kMaxCluster : 4;
         const int64_t q = std::min<int64_t>(want, pow2_ceil(std::max<int64_t>(ctas, 1)));
         p->group = static_cast<int32_t>(q);
         p->grid = M > 0 ? round_up(ctas, q) : 0;

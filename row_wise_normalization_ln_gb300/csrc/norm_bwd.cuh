@@ -13,8 +13,7 @@
 //
 // norm_bwd_cta: a CTA, or a cluster of CTAs, owns one row at a time (one
 // register round; x and dy are read once) and walks rows in a grid-stride
-// loop, with the next row's loads in flight while the current one is
-// reduced. A thread owns the same columns in every row it visits, so it
+// loop, with the rows two steps ahead prefetched into L2. A thread owns the same columns in every row it visits, so it
 // accumulates the column gradients of those columns in its own slots of
 // shared memory. At the end, CTAs that share columns (the CTAs of a
 // reduction cluster, each on its own rows) add their accumulators through
@@ -65,6 +64,16 @@ template <>
 struct BwdElem<__nv_bfloat16, 8> : BwdElem16<__nv_bfloat16, Bf16Pair> {};
 template <>
 struct BwdElem<__half, 8> : BwdElem16<__half, F16Pair> {};
+
+// The pair codec of a 16-bit element type.
+template <class T>
+struct PairOf {
+    using type = Bf16Pair;
+};
+template <>
+struct PairOf<__half> {
+    using type = F16Pair;
+};
 
 template <class T>
 struct BwdElem<T, 1> {
@@ -119,11 +128,13 @@ __device__ __forceinline__ float2 row_sum2(PairReduceSmem& red, int stage, float
 // CTAs of a cluster each take their own rows and meet only at the end.
 //
 // Each thread keeps gamma (w) of its columns in registers for the whole
-// kernel, and loads the next row's x and dy (and LayerNorm statistics) into
-// registers before it reduces and writes the current one, so that a row's loads are in flight
-// while the previous row is being finished. The column accumulators live in
-// dynamic shared memory, [NA][T*V*VEC] floats, each thread at the positions
-// of its own columns (so no thread reads another's until the end).
+// kernel. Rows two steps ahead are prefetched into L2 (bulk, by one thread),
+// so a row's own loads are L2 hits while HBM already serves the rows after
+// it. (Loads into registers issued a row ahead did not overlap: the row's
+// block barrier waits for them.) The column accumulators live in registers
+// (in this thread's shared-memory slots for the 16-bit variants of 4
+// accesses per thread); at the end they sit in dynamic shared memory,
+// [NA][T*V*VEC] floats, each thread at the positions of its own columns.
 template <class T, int VEC, int V, bool LN>
 __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) {
     using O = OpsFor<T, VEC>;
@@ -157,9 +168,20 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
     const int slice = T_ * V * VEC;  // floats per accumulator array
     float* my_acc = acc_s + local * VEC;
 
-    // This thread's accumulator slots start at zero.
+    // Column accumulators in registers where they fit beside the row data
+    // (all but the 16-bit variants of 4 accesses per thread); otherwise in
+    // this thread's shared-memory slots.
+    constexpr bool ACC_REG = !(VEC == 8 && V >= 4);
+    float acc[ACC_REG ? NA : 1][ACC_REG ? V : 1][ACC_REG ? VEC : 1];
 #pragma unroll
-    for (int k = 0; k < NA; ++k)
+    for (int k = 0; k < (ACC_REG ? NA : 1); ++k)
+#pragma unroll
+        for (int j = 0; j < (ACC_REG ? V : 1); ++j)
+#pragma unroll
+            for (int e = 0; e < (ACC_REG ? VEC : 1); ++e) acc[k][j][e] = 0.f;
+    // Shared-memory accumulator slots start at zero.
+#pragma unroll
+    for (int k = 0; k < (ACC_REG ? 0 : NA); ++k)
 #pragma unroll
         for (int j = 0; j < V; ++j)
 #pragma unroll
@@ -174,66 +196,108 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
     grid_release();
     grid_wait();
 
+    // 16-bit rows work on fp32 pairs with the packed instructions and keep
+    // gamma widened (gf); other rows work on scalars.
+    constexpr bool PAIRS = VEC == 8;
+    using P = typename PairOf<T>::type;
     Raw gv[V];
+    float2 gf[PAIRS ? V : 1][4];
     {
         const T* gp = static_cast<const T*>(a.gamma) + f0 * VEC;
 #pragma unroll
         for (int j = 0; j < V; ++j)
-            if (j < nv) gv[j] = O::load_param(gp + j * stride);
+            if (j < nv) {
+                gv[j] = O::load_param(gp + j * stride);
+                if constexpr (PAIRS) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) gf[j][i] = P::widen(Ops16<T, P>::w(gv[j], i));
+                }
+            }
     }
     const T* xbase = static_cast<const T*>(a.x) + f0 * VEC;
     const T* dybase = static_cast<const T*>(a.dy) + f0 * VEC;
-    Raw xv[V], dv[V];
-    float mu = 0.f, rs = 0.f;  // LayerNorm statistics of the current row
-    if (first_row < a.M) {
-#pragma unroll
-        for (int j = 0; j < V; ++j)
-            if (j < nv) {
-                xv[j] = O::load(xbase + first_row * N + j * stride);
-                dv[j] = O::load(dybase + first_row * N + j * stride);
+    // Rows ahead go to L2 by bulk prefetch: this CTA's contiguous slice of x
+    // and dy (16-byte vector rows only) and the row's statistics, issued by
+    // one thread, two rows ahead of the row being worked on.
+    const int64_t cta_first = static_cast<int64_t>(rank) * V * T_ * VEC;  // first element of the CTA's slice
+    const uint32_t slice_bytes = static_cast<uint32_t>(
+        (cta_first < N ? min(static_cast<int64_t>(V) * T_ * VEC, N - cta_first) : 0) * sizeof(T));
+    auto prefetch_row = [&](int64_t r) {
+        if (r >= a.M) return;
+        if constexpr (VEC > 1) {
+            if (slice_bytes > 0) {
+                prefetch_l2_bulk(static_cast<const T*>(a.x) + r * N + cta_first, slice_bytes);
+                prefetch_l2_bulk(static_cast<const T*>(a.dy) + r * N + cta_first, slice_bytes);
             }
-        if constexpr (LN) {
-            mu = a.mean[first_row];
-            rs = a.rstd[first_row];
         }
+        if constexpr (LN) {
+            prefetch_l2_line(a.mean + r);
+            prefetch_l2_line(a.rstd + r);
+        }
+    };
+    if (tid == 0) {
+        prefetch_row(first_row);
+        prefetch_row(first_row + row_step);
     }
 
     int it = 0;
     for (int64_t row = first_row; row < a.M; row += row_step, ++it) {
-        // The next row's loads go out before this row is reduced.
-        const int64_t next = row + row_step;
-        Raw xn[V], dn[V];
-        float mun = 0.f, rsn = 0.f;
-        if (next < a.M) {
-#pragma unroll
-            for (int j = 0; j < V; ++j)
-                if (j < nv) {
-                    xn[j] = O::load(xbase + next * N + j * stride);
-                    dn[j] = O::load(dybase + next * N + j * stride);
-                }
-            if constexpr (LN) {
-                mun = a.mean[next];
-                rsn = a.rstd[next];
-            }
-        }
-        float s0 = 0.f, s1 = 0.f;
+        if (tid == 0) prefetch_row(row + 2 * row_step);
+        Raw xv[V], dv[V];
 #pragma unroll
         for (int j = 0; j < V; ++j)
             if (j < nv) {
+                xv[j] = O::load(xbase + row * N + j * stride);
+                dv[j] = O::load(dybase + row * N + j * stride);
+            }
+        float mu = 0.f, rs = 0.f;
+        if constexpr (LN) {
+            mu = a.mean[row];
+            rs = a.rstd[row];
+        }
+        float s0 = 0.f, s1 = 0.f;
+        if constexpr (PAIRS) {
+            const float2 nmu = f2_splat(-mu), rs2 = f2_splat(rs);
+            float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float xe = E::get(xv[j], e), de = E::get(dv[j], e), ge = E::get(gv[j], e);
-                    if constexpr (LN) {
-                        const float xh = (xe - mu) * rs;
-                        const float g = de * ge;
-                        s0 += g;
-                        s1 = fmaf(g, xh, s1);
-                    } else {
-                        s0 = fmaf(xe, xe, s0);
-                        s1 = fmaf(de * ge, xe, s1);
+            for (int j = 0; j < V; ++j)
+                if (j < nv) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 x2 = P::widen(Ops16<T, P>::w(xv[j], i));
+                        const float2 d2 = P::widen(Ops16<T, P>::w(dv[j], i));
+                        if constexpr (LN) {
+                            const float2 xh = __fmul2_rn(__fadd2_rn(x2, nmu), rs2);
+                            const float2 g = __fmul2_rn(d2, gf[j][i]);
+                            a0 = __fadd2_rn(a0, g);
+                            a1 = __ffma2_rn(g, xh, a1);
+                        } else {
+                            a0 = __ffma2_rn(x2, x2, a0);
+                            a1 = __ffma2_rn(__fmul2_rn(d2, gf[j][i]), x2, a1);
+                        }
                     }
                 }
-            }
+            s0 = a0.x + a0.y;
+            s1 = a1.x + a1.y;
+        } else {
+#pragma unroll
+            for (int j = 0; j < V; ++j)
+                if (j < nv) {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        const float xe = E::get(xv[j], e), de = E::get(dv[j], e), ge = E::get(gv[j], e);
+                        if constexpr (LN) {
+                            const float xh = (xe - mu) * rs;
+                            const float g = de * ge;
+                            s0 += g;
+                            s1 = fmaf(g, xh, s1);
+                        } else {
+                            s0 = fmaf(xe, xe, s0);
+                            s1 = fmaf(de * ge, xe, s1);
+                        }
+                    }
+                }
+        }
         const float2 S = row_sum2(red, it & 1, make_float2(s0, s1), C, nwarps, wwidth);
         T* dxr = static_cast<T*>(a.dx) + row * N + f0 * VEC;
         float c0, c1;  // LayerNorm: mean(g), mean(g xhat); RMSNorm: rstd, rstd^3 mean(dy w x)
@@ -248,32 +312,88 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
         for (int j = 0; j < V; ++j)
             if (j < nv) {
                 float o[VEC], pa[VEC], pb[VEC];
+                if constexpr (PAIRS) {
+                    const float2 nmu = f2_splat(-mu), rs2 = f2_splat(rs), nc0 = f2_splat(-c0), nc1 = f2_splat(-c1),
+                                 c02 = f2_splat(c0);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float xe = E::get(xv[j], e), de = E::get(dv[j], e), ge = E::get(gv[j], e);
-                    if constexpr (LN) {
-                        const float xh = (xe - mu) * rs;
-                        o[e] = rs * ((de * ge - c0) - xh * c1);
-                        pa[e] = de * xh;
-                        pb[e] = de;
-                    } else {
-                        o[e] = fmaf(-xe, c1, c0 * (de * ge));
-                        pa[e] = (de * xe) * c0;
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 x2 = P::widen(Ops16<T, P>::w(xv[j], i));
+                        const float2 d2 = P::widen(Ops16<T, P>::w(dv[j], i));
+                        float2 ov, av, bv = d2;
+                        if constexpr (LN) {
+                            const float2 xh = __fmul2_rn(__fadd2_rn(x2, nmu), rs2);
+                            const float2 t = __fadd2_rn(__fmul2_rn(d2, gf[j][i]), nc0);
+                            ov = __fmul2_rn(rs2, __ffma2_rn(xh, nc1, t));
+                            if constexpr (ACC_REG) {
+                                const float2 ga = __ffma2_rn(d2, xh, make_float2(acc[0][j][2 * i], acc[0][j][2 * i + 1]));
+                                const float2 gb = __fadd2_rn(make_float2(acc[NA - 1][j][2 * i], acc[NA - 1][j][2 * i + 1]), d2);
+                                acc[0][j][2 * i] = ga.x;
+                                acc[0][j][2 * i + 1] = ga.y;
+                                acc[NA - 1][j][2 * i] = gb.x;
+                                acc[NA - 1][j][2 * i + 1] = gb.y;
+                            } else {
+                                av = __fmul2_rn(d2, xh);
+                            }
+                        } else {
+                            ov = __ffma2_rn(x2, nc1, __fmul2_rn(c02, __fmul2_rn(d2, gf[j][i])));
+                            if constexpr (ACC_REG) {
+                                const float2 ga = __ffma2_rn(__fmul2_rn(d2, x2), c02,
+                                                             make_float2(acc[0][j][2 * i], acc[0][j][2 * i + 1]));
+                                acc[0][j][2 * i] = ga.x;
+                                acc[0][j][2 * i + 1] = ga.y;
+                            } else {
+                                av = __fmul2_rn(__fmul2_rn(d2, x2), c02);
+                            }
+                        }
+                        o[2 * i] = ov.x;
+                        o[2 * i + 1] = ov.y;
+                        pa[2 * i] = av.x;
+                        pa[2 * i + 1] = av.y;
+                        pb[2 * i] = bv.x;
+                        pb[2 * i + 1] = bv.y;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        const float xe = E::get(xv[j], e), de = E::get(dv[j], e), ge = E::get(gv[j], e);
+                        if constexpr (LN) {
+                            const float xh = (xe - mu) * rs;
+                            o[e] = rs * ((de * ge - c0) - xh * c1);
+                            if constexpr (ACC_REG) {
+                                acc[0][j][e] = fmaf(de, xh, acc[0][j][e]);
+                                acc[NA - 1][j][e] += de;
+                            } else {
+                                pa[e] = de * xh;
+                                pb[e] = de;
+                            }
+                        } else {
+                            o[e] = fmaf(-xe, c1, c0 * (de * ge));
+                            if constexpr (ACC_REG)
+                                acc[0][j][e] = fmaf(de * xe, c0, acc[0][j][e]);
+                            else
+                                pa[e] = (de * xe) * c0;
+                        }
                     }
                 }
                 O::store(dxr + j * stride, E::pack(o));
 #pragma unroll
-                for (int k = 0; k < NA; ++k) {
+                for (int k = 0; k < (ACC_REG ? 0 : NA); ++k) {
                     float* d = my_acc + k * slice + j * 32 * VEC;
                     const float* p = k == 0 ? pa : pb;
                     if constexpr (VEC % 4 == 0) {
 #pragma unroll
                         for (int e = 0; e < VEC; e += 4) {
                             float4 v = *reinterpret_cast<float4*>(d + e);
-                            v.x += p[e];
-                            v.y += p[e + 1];
-                            v.z += p[e + 2];
-                            v.w += p[e + 3];
+                            if constexpr (PAIRS) {
+                                const float2 lo = __fadd2_rn(make_float2(v.x, v.y), make_float2(p[e], p[e + 1]));
+                                const float2 hi = __fadd2_rn(make_float2(v.z, v.w), make_float2(p[e + 2], p[e + 3]));
+                                v = make_float4(lo.x, lo.y, hi.x, hi.y);
+                            } else {
+                                v.x += p[e];
+                                v.y += p[e + 1];
+                                v.z += p[e + 2];
+                                v.w += p[e + 3];
+                            }
                             *reinterpret_cast<float4*>(d + e) = v;
                         }
                     } else {
@@ -282,13 +402,26 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
                     }
                 }
             }
+    }
+
+    if constexpr (ACC_REG) {
+        // Hand the register accumulators to this thread's shared-memory
+        // slots (column positions), where the steps below expect them.
 #pragma unroll
-        for (int j = 0; j < V; ++j) {
-            xv[j] = xn[j];
-            dv[j] = dn[j];
-        }
-        mu = mun;
-        rs = rsn;
+        for (int k = 0; k < NA; ++k)
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                float* d = my_acc + k * slice + j * 32 * VEC;
+                if constexpr (VEC % 4 == 0) {
+#pragma unroll
+                    for (int e = 0; e < VEC; e += 4)
+                        *reinterpret_cast<float4*>(d + e) =
+                            make_float4(acc[k][j][e], acc[k][j][e + 1], acc[k][j][e + 2], acc[k][j][e + 3]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) d[e] = acc[k][j][e];
+                }
+            }
     }
 
     // Partial rows of the column gradients: one per cluster.

@@ -81,6 +81,17 @@ __device__ __forceinline__ float ld_peer_f32(uint32_t addr) {
 __device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_release() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
+// ----------------------------------------------------------------- L2 prefetch
+// Hints that move data towards L2 without writing any register, so nothing
+// (no barrier, no scoreboard) waits for them: a bulk range through the copy
+// engine (16-byte aligned address, size a multiple of 16), or one line.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2_line(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ----------------------------------------------------------------- cp.async
 // Per-thread asynchronous global -> shared copies. A thread waits for its own
 // copies with cp.async.wait_group, a hardware wait (no polling loop), and
