@@ -25,9 +25,16 @@
  *     (fp16 outputs beyond its range become infinities).
  *   - y may equal x exactly (in place). Any other overlap between outputs and
  *     inputs, or between outputs, is undefined.
- *   - Pointers need no particular alignment. When x, y and the parameter
- *     vectors are 16-byte aligned and a row is a multiple of 16 bytes, the
- *     kernels use 128-bit accesses; otherwise they use element accesses.
+ *   - Pointers need no particular alignment beyond their element type.
+ *     When x, y and the parameter vectors are 16-byte aligned and a row is a
+ *     multiple of 16 bytes, the kernels use 128-bit accesses throughout.
+ *     When the row tensors (x, y; with the fused add also residual and h)
+ *     merely share their offset within 16 bytes (odd N, or tensors that
+ *     start at the same misalignment), rows of 64 or more vectors still use
+ *     128-bit accesses from each row's first aligned element, with the few
+ *     elements before and after taken one by one (gamma and beta then by
+ *     element where their vectors are not aligned). Otherwise the kernels
+ *     use element accesses.
  *   - Argument errors are detected on the host before any CUDA call and
  *     nothing is launched. M == 0 is a no-op that returns NORM_OK (pointers
  *     may then be NULL). Limits: 1 <= N <= 2^24 (the largest count fp32
@@ -114,9 +121,12 @@ norm_status rms_fwd(const void* x, const void* w, void* y, int64_t M, int64_t N,
 
 /*
  * The plan ln_fwd / rms_fwd would choose for M rows of N elements of
- * `dtype` on a device with `num_sms` SMs, with `aligned16` != 0 when every
- * pointer is 16-byte aligned. Host only: makes no CUDA call. Fills `plan`
- * (including `rounds`) and returns NORM_OK, or an argument error.
+ * `dtype` on a device with `num_sms` SMs. `aligned16`: 1 when every pointer
+ * is 16-byte aligned, 2 when the row tensors (x, y, and residual and h when
+ * fused) only share their offset within 16 bytes (or rows are not whole
+ * vectors), 0 otherwise (element accesses). Host only: makes no CUDA call.
+ * Fills `plan` (including `rounds`) and returns NORM_OK, or an argument
+ * error.
  */
 norm_status norm_make_plan(int64_t M, int64_t N, norm_dtype dtype, int aligned16,
                            int num_sms, norm_plan* plan);

@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <initializer_list>
 
 #include <cuda_runtime_api.h>
 
@@ -41,6 +42,46 @@ int64_t pow2_ceil(int64_t v) {
 }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// How the rows of a call can be accessed:
+//   kAlignNone   element accesses only;
+//   kAlignFull   every pointer 16-byte aligned and rows whole vectors: every
+//                row starts on a 16-byte boundary;
+//   kAlignPhase  the row tensors share their offset within 16 bytes (so
+//                every row's elements sit at the same phase in each of
+//                them): 16-byte vectors from each row's first aligned
+//                element, the few elements around them one by one (CTA
+//                mapping only).
+enum AlignMode { kAlignNone = 0, kAlignFull = 1, kAlignPhase = 2 };
+
+// The access mode of a call from its pointers: `rows` are the [M, N] row
+// tensors (x, y and, when fused, the residual and h), `params` gamma/beta
+// (or w); `y8` an FP8 output (one byte per element) or null.
+int align_mode(std::initializer_list<const void*> rows, std::initializer_list<const void*> params, const void* y8,
+               norm_dtype dtype, bool* vec_params) {
+    const uintptr_t s = static_cast<uintptr_t>(elem_size(dtype));
+    bool all16 = true, same = true;
+    uintptr_t phase = 16;
+    for (const void* p : rows) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+        if (a % s != 0) return kAlignNone;  // not even element-aligned: element accesses
+        if (phase == 16) phase = a & 15u;
+        same = same && (a & 15u) == phase;
+        all16 = all16 && (a & 15u) == 0;
+    }
+    bool pv = true;
+    for (const void* p : params) pv = pv && (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+    *vec_params = pv;
+    if (y8) {
+        // the FP8 row's vector stores start where x's do: y8 and x/s agree modulo 16/s
+        const uintptr_t vec = 16 / s;
+        const uintptr_t x = reinterpret_cast<uintptr_t>(*rows.begin()) / s;
+        if ((reinterpret_cast<uintptr_t>(y8) % vec) != (x % vec)) return kAlignNone;
+        all16 = all16 && (reinterpret_cast<uintptr_t>(y8) & 15u) == 0;
+    }
+    if (!same) return kAlignNone;
+    return (all16 && pv) ? kAlignFull : kAlignPhase;
+}
+
 // Checks shared by every entry point; M == 0 is legal.
 norm_status check_sizes(int64_t M, int64_t N, norm_dtype dtype) {
     if (!dtype_ok(dtype)) return NORM_ERR_DTYPE;
@@ -49,11 +90,18 @@ norm_status check_sizes(int64_t M, int64_t N, norm_dtype dtype) {
     return NORM_OK;
 }
 
-// Elements per access for this row shape: a 16-byte vector when every
-// pointer is 16-byte aligned and rows are whole vectors, else one element.
-int vec_for(int64_t N, norm_dtype dtype, bool all_aligned) {
+
+// Elements per access for this row shape and mode.
+int vec_for(int64_t N, norm_dtype dtype, int mode) {
     const int s = elem_size(dtype);
-    return (all_aligned && (N * s) % 16 == 0) ? 16 / s : 1;
+    if (mode == kAlignFull && (N * s) % 16 == 0) return 16 / s;
+    if (mode != kAlignNone) return 16 / s;  // phase-compatible rows (checked for the mapping by the caller)
+    return 1;
+}
+
+// True when rows are whole 16-byte vectors on 16-byte boundaries.
+bool rows_aligned(int64_t N, norm_dtype dtype, int mode) {
+    return mode == kAlignFull && (N * elem_size(dtype)) % 16 == 0;
 }
 
 // The planner, from plan sweeps on GB300: rows do best with 8 accesses (128
@@ -61,11 +109,12 @@ int vec_for(int64_t N, norm_dtype dtype, bool all_aligned) {
 // than 256 such threads go to a cluster of up to 8 CTAs of 128 threads, each
 // walking its share in two rounds; lane groups only pay off below 64
 // accesses per row.
-norm_status make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_aligned, int num_sms, bool add,
-                      norm_plan* p) {
+norm_status make_plan(int64_t M, int64_t N, norm_dtype dtype, int mode, int num_sms, bool add, norm_plan* p) {
     std::memset(p, 0, sizeof *p);
     const int max_threads = add ? libnorm::kFusedMaxThreads : kMaxThreads;
-    const int vec = vec_for(N, dtype, all_aligned);
+    int vec = vec_for(N, dtype, mode);
+    // Rows not on 16-byte boundaries take vectors only in the CTA mapping.
+    if (vec > 1 && !rows_aligned(N, dtype, mode) && ceil_div(N, vec) < 64) vec = 1;
     const int64_t nacc = ceil_div(N, vec);
     const int64_t busy_threads = int64_t(num_sms) * 1024;  // half of the resident-thread capacity
     p->vec_elems = vec;
@@ -121,7 +170,7 @@ norm_status make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_aligned, 
 
 // Validate an explicit plan against the call; derive `rounds`. The fused
 // residual add (`add`) has no ring kernel and smaller CTAs.
-norm_status check_plan(const norm_plan& in, int64_t N, norm_dtype dtype, bool all_aligned, bool add, bool q8,
+norm_status check_plan(const norm_plan& in, int64_t N, norm_dtype dtype, int mode, bool add, bool q8,
                        norm_plan* out) {
     norm_plan p = in;
     if (add && (p.stages != 0 || p.threads > libnorm::kFusedMaxThreads)) return NORM_ERR_PLAN;
@@ -129,7 +178,9 @@ norm_status check_plan(const norm_plan& in, int64_t N, norm_dtype dtype, bool al
     const int s = elem_size(dtype);
     if (p.mapping != NORM_MAP_GROUP && p.mapping != NORM_MAP_CTA) return NORM_ERR_PLAN;
     if (p.vec_elems != 1) {
-        if (p.vec_elems != 16 / s || !all_aligned || (N * s) % 16 != 0) return NORM_ERR_PLAN;
+        if (p.vec_elems != 16 / s || mode == kAlignNone) return NORM_ERR_PLAN;
+        // rows off 16-byte boundaries: the CTA register kernels only
+        if (!rows_aligned(N, dtype, mode) && (p.mapping != NORM_MAP_CTA || p.stages != 0)) return NORM_ERR_PLAN;
     }
     if (!is_pow2(p.per_thread) || p.per_thread > kMaxPerThread) return NORM_ERR_PLAN;
     if (p.threads < 32 || p.threads > kMaxThreads || p.threads % 32 != 0) return NORM_ERR_PLAN;
@@ -177,7 +228,7 @@ int bwd_vmax(bool ln, norm_dtype dtype, int vec) {
 norm_status bwd_make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_aligned, int num_sms, bool ln,
                           norm_plan* p) {
     std::memset(p, 0, sizeof *p);
-    const int vec = vec_for(N, dtype, all_aligned);
+    const int vec = (all_aligned && (N * elem_size(dtype)) % 16 == 0) ? 16 / elem_size(dtype) : 1;
     const int64_t nacc = ceil_div(N, vec);
     int per = bwd_vmax(ln, dtype, vec);
     int64_t cluster = 1;
@@ -286,23 +337,24 @@ Launcher pick_launcher(bool ln, bool add, bool q8, norm_dtype dtype) {
 
 // a.res != null selects the fused residual add; a.qscale != null the FP8
 // output.
-norm_status run(bool ln, const NormArgs& a, norm_dtype dtype, bool all_aligned, cudaStream_t stream,
+norm_status run(bool ln, const NormArgs& a, norm_dtype dtype, int mode, cudaStream_t stream,
                 const norm_plan* user_plan) {
     const bool add = a.res != nullptr;
     const bool q8 = a.qscale != nullptr;
     norm_plan plan;
     if (user_plan) {
-        const norm_status st = check_plan(*user_plan, a.N, dtype, all_aligned, add, q8, &plan);
+        const norm_status st = check_plan(*user_plan, a.N, dtype, mode, add, q8, &plan);
         if (st != NORM_OK) return st;
     }
     int dev = 0;
     const int sms = device_sm_count(&dev);
     if (sms <= 0) return NORM_ERR_CUDA;
-    if (!user_plan) make_plan(a.M, a.N, dtype, all_aligned, sms, add, &plan);
+    if (!user_plan) make_plan(a.M, a.N, dtype, mode, sms, add, &plan);
     NormArgs args = a;
     args.group = plan.group;
     args.rounds = plan.rounds;
     args.stages = plan.stages;
+    args.shift = plan.vec_elems > 1 && !rows_aligned(a.N, dtype, mode);
     const cudaError_t e = pick_launcher(ln, add, q8, dtype)(plan, args, stream, sms, dev);
     if (e != cudaSuccess) {
         g_last_cuda_error = static_cast<int>(e);
@@ -318,9 +370,11 @@ norm_status ln_impl(const void* x, const void* gamma, const void* beta, void* y,
     if (!std::isfinite(eps) || eps < 0.f) return NORM_ERR_ARG;
     if (M == 0) return NORM_OK;
     if (!x || !gamma || !beta || !y) return NORM_ERR_ARG;
-    const bool al = aligned16(x) && aligned16(y) && aligned16(gamma) && aligned16(beta);
+    bool vp = true;
+    const int mode = align_mode({x, y}, {gamma, beta}, nullptr, dtype, &vp);
     NormArgs a{x, gamma, beta, y, mean, rstd, nullptr, nullptr, nullptr, M, static_cast<int32_t>(N), eps, 0, 1, 0};
-    return run(true, a, dtype, al, stream, plan);
+    a.vec_params = vp;
+    return run(true, a, dtype, mode, stream, plan);
 }
 
 norm_status rms_impl(const void* x, const void* w, void* y, int64_t M, int64_t N, float eps, norm_dtype dtype,
@@ -330,9 +384,11 @@ norm_status rms_impl(const void* x, const void* w, void* y, int64_t M, int64_t N
     if (!std::isfinite(eps) || eps < 0.f) return NORM_ERR_ARG;
     if (M == 0) return NORM_OK;
     if (!x || !w || !y) return NORM_ERR_ARG;
-    const bool al = aligned16(x) && aligned16(y) && aligned16(w);
+    bool vp = true;
+    const int mode = align_mode({x, y}, {w}, nullptr, dtype, &vp);
     NormArgs a{x, w, nullptr, y, nullptr, nullptr, nullptr, nullptr, nullptr, M, static_cast<int32_t>(N), eps, 0, 1, 0};
-    return run(false, a, dtype, al, stream, plan);
+    a.vec_params = vp;
+    return run(false, a, dtype, mode, stream, plan);
 }
 
 // Fused residual add: h and y are both written, so they may not be the same
@@ -345,10 +401,11 @@ norm_status ln_add_impl(const void* x, const void* res, const void* gamma, const
     if (!std::isfinite(eps) || eps < 0.f) return NORM_ERR_ARG;
     if (M == 0) return NORM_OK;
     if (!x || !res || !gamma || !beta || !h || !y || h == y) return NORM_ERR_ARG;
-    const bool al = aligned16(x) && aligned16(res) && aligned16(h) && aligned16(y) && aligned16(gamma) &&
-                    aligned16(beta);
+    bool vp = true;
+    const int mode = align_mode({x, res, h, y}, {gamma, beta}, nullptr, dtype, &vp);
     NormArgs a{x, gamma, beta, y, mean, rstd, res, h, nullptr, M, static_cast<int32_t>(N), eps, 0, 1, 0};
-    return run(true, a, dtype, al, stream, plan);
+    a.vec_params = vp;
+    return run(true, a, dtype, mode, stream, plan);
 }
 
 norm_status rms_add_impl(const void* x, const void* res, const void* w, void* h, void* y, int64_t M, int64_t N,
@@ -358,9 +415,11 @@ norm_status rms_add_impl(const void* x, const void* res, const void* w, void* h,
     if (!std::isfinite(eps) || eps < 0.f) return NORM_ERR_ARG;
     if (M == 0) return NORM_OK;
     if (!x || !res || !w || !h || !y || h == y) return NORM_ERR_ARG;
-    const bool al = aligned16(x) && aligned16(res) && aligned16(h) && aligned16(y) && aligned16(w);
+    bool vp = true;
+    const int mode = align_mode({x, res, h, y}, {w}, nullptr, dtype, &vp);
     NormArgs a{x, w, nullptr, y, nullptr, nullptr, res, h, nullptr, M, static_cast<int32_t>(N), eps, 0, 1, 0};
-    return run(false, a, dtype, al, stream, plan);
+    a.vec_params = vp;
+    return run(false, a, dtype, mode, stream, plan);
 }
 
 // FP8 output: y8 holds one E4M3 byte per element; scale is one fp32 value
@@ -374,11 +433,13 @@ norm_status fp8_impl(bool ln, const void* x, const void* res, const void* gamma,
     if (M == 0) return NORM_OK;
     if (!x || !gamma || (ln && !beta) || !scale || !y8) return NORM_ERR_ARG;
     if (res && (!h || h == y8)) return NORM_ERR_ARG;
-    bool al = aligned16(x) && aligned16(y8) && aligned16(gamma) && (!ln || aligned16(beta));
-    if (res) al = al && aligned16(res) && aligned16(h);
+    bool vp = true;
+    const int mode = res ? align_mode({x, res, h}, {gamma, ln ? beta : gamma}, y8, dtype, &vp)
+                         : align_mode({x}, {gamma, ln ? beta : gamma}, y8, dtype, &vp);
     NormArgs a{x, gamma, ln ? beta : nullptr, y8, ln ? mean : nullptr, ln ? rstd : nullptr, res, res ? h : nullptr,
                scale, M, static_cast<int32_t>(N), eps, 0, 1, 0};
-    return run(ln, a, dtype, al, stream, plan);
+    a.vec_params = vp;
+    return run(ln, a, dtype, mode, stream, plan);
 }
 
 // Backward: dx = d(loss)/dx for y = norm(x); column gradients in fp32.
@@ -560,14 +621,16 @@ norm_status norm_make_plan(int64_t M, int64_t N, norm_dtype dtype, int aligned, 
     const norm_status st = check_sizes(M, N, dtype);
     if (st != NORM_OK) return st;
     if (!plan || num_sms < 1) return NORM_ERR_ARG;
-    return make_plan(M, N, dtype, aligned != 0, num_sms, false, plan);
+    if (aligned < kAlignNone || aligned > kAlignPhase) return NORM_ERR_ARG;
+    return make_plan(M, N, dtype, aligned, num_sms, false, plan);
 }
 
 norm_status norm_make_plan_add(int64_t M, int64_t N, norm_dtype dtype, int aligned, int num_sms, norm_plan* plan) {
     const norm_status st = check_sizes(M, N, dtype);
     if (st != NORM_OK) return st;
     if (!plan || num_sms < 1) return NORM_ERR_ARG;
-    return make_plan(M, N, dtype, aligned != 0, num_sms, true, plan);
+    if (aligned < kAlignNone || aligned > kAlignPhase) return NORM_ERR_ARG;
+    return make_plan(M, N, dtype, aligned, num_sms, true, plan);
 }
 
 const char* norm_status_string(norm_status s) {

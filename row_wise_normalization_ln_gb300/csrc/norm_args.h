@@ -30,6 +30,8 @@ struct NormArgs {
     int32_t group;      // GROUP mapping: lanes per row
     int32_t rounds;     // CTA mapping: register-sized rounds per row
     int32_t stages;     // pipelined CTA mapping: shared-memory ring stages
+    int32_t shift = 0;       // CTA mapping, 16-byte vectors: rows need not start on a 16-byte boundary
+    int32_t vec_params = 1;  // gamma (and beta) 16-byte aligned
 };
 
 // Backward pass. A CTA (row_cluster == 1) or a cluster of row_cluster CTAs

@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
                     for (int i = 0; i < 4; ++i) {
                         const float2 x2 = P::widen(Ops16<T, P>::w(xv[j], i));
                         const float2 d2 = P::widen(Ops16<T, P>::w(dv[j], i));
-                        float2 ov, av, bv = d2;
+                        float2 ov, av = make_float2(0.f, 0.f), bv = d2;
                         if constexpr (LN) {
                             const float2 xh = __fmul2_rn(__fadd2_rn(x2, nmu), rs2);
                             const float2 t = __fadd2_rn(__fmul2_rn(d2, gf[j][i]), nc0);

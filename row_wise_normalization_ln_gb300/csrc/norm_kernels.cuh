@@ -150,6 +150,11 @@ struct Ops<float, 4> {
     static __device__ __forceinline__ Raw load_param(const float* p) {
         return __ldg(reinterpret_cast<const uint4*>(p));
     }
+    // The same access assembled from element loads (p not 16-byte aligned).
+    static __device__ __forceinline__ Raw load_param_elems(const float* p) {
+        return make_uint4(__float_as_uint(__ldg(p)), __float_as_uint(__ldg(p + 1)), __float_as_uint(__ldg(p + 2)),
+                          __float_as_uint(__ldg(p + 3)));
+    }
     static __device__ __forceinline__ void store(float* p, const Raw& v) { *reinterpret_cast<uint4*>(p) = v; }
 };
 
@@ -244,6 +249,14 @@ struct Ops16 {
     static __device__ __forceinline__ Raw load_param(const T* p) {
         return __ldg(reinterpret_cast<const uint4*>(p));
     }
+    static __device__ __forceinline__ Raw load_param_elems(const T* p) {
+        const unsigned short* q = reinterpret_cast<const unsigned short*>(p);
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = static_cast<uint32_t>(__ldg(q + 2 * i)) | (static_cast<uint32_t>(__ldg(q + 2 * i + 1)) << 16);
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    }
     static __device__ __forceinline__ void store(T* p, const Raw& v) {
         *reinterpret_cast<uint4*>(p) = v;
     }
@@ -301,6 +314,7 @@ struct ScalarOps {
         else
             return __ldg(reinterpret_cast<const unsigned short*>(p));
     }
+    static __device__ __forceinline__ Raw load_param_elems(const T* p) { return load_param(p); }
     static __device__ __forceinline__ void store(T* p, Raw v) {
         if constexpr (sizeof(T) == 4)
             *reinterpret_cast<float*>(p) = __uint_as_float(v);
@@ -423,44 +437,49 @@ struct Slice {
     // LayerNorm: y = ((x - K) * rstd - mu * rstd) * gamma + beta, where mu is
     // the mean of x - K (so x - mean is never formed from a rounded fp32
     // mean); RMSNorm: y = (x * w) * rstd.
-    __device__ __forceinline__ void emit(const T* g, const T* b, T* y, int stride, int nvalid, float mu,
-                                         float rs) const {
+    // gamma/beta access j, as one vector load, or element by element when
+    // `sp` (their vectors are not 16-byte aligned in this row).
+    static __device__ __forceinline__ typename O::Raw param(const T* p, bool sp) {
+        return sp ? O::load_param_elems(p) : O::load_param(p);
+    }
+    __device__ __forceinline__ void emit(const T* g, const T* b, T* y, int stride, int nvalid, float mu, float rs,
+                                         bool sp = false) const {
         const float nmr = -mu * rs;
 #pragma unroll
         for (int j = 0; j < V; ++j)
             if (j < nvalid) {
                 if constexpr (LN)
-                    O::store(y + j * stride, O::ln_out(raw[j], K, rs, nmr, O::load_param(g + j * stride),
-                                                       O::load_param(b + j * stride)));
+                    O::store(y + j * stride, O::ln_out(raw[j], K, rs, nmr, param(g + j * stride, sp),
+                                                       param(b + j * stride, sp)));
                 else
-                    O::store(y + j * stride, O::rms_out(raw[j], rs, O::load_param(g + j * stride)));
+                    O::store(y + j * stride, O::rms_out(raw[j], rs, param(g + j * stride, sp)));
             }
     }
     // emit with an FP8 E4M3 output: the same fp32 values, scaled by `inv`
     // (1 / the static scale) and quantised; `y8` points at this thread's
     // first access in bytes (one byte per element).
     __device__ __forceinline__ void emit_q8(const T* g, const T* b, uint8_t* y8, int stride, int nvalid, float mu,
-                                            float rs, float inv) const {
+                                            float rs, float inv, bool sp = false) const {
         const float nmr = -mu * rs;
 #pragma unroll
         for (int j = 0; j < V; ++j)
             if (j < nvalid) {
                 float o[VEC];
                 if constexpr (LN)
-                    O::ln_vals(raw[j], K, rs, nmr, O::load_param(g + j * stride), O::load_param(b + j * stride), o);
+                    O::ln_vals(raw[j], K, rs, nmr, param(g + j * stride, sp), param(b + j * stride, sp), o);
                 else
-                    O::rms_vals(raw[j], rs, O::load_param(g + j * stride), o);
+                    O::rms_vals(raw[j], rs, param(g + j * stride, sp), o);
                 store_e4m3<VEC>(y8 + j * stride, o, inv);
             }
     }
     // Output step of either kind.
     template <bool Q8>
     __device__ __forceinline__ void out(const T* g, const T* b, void* y, int64_t offset, int stride, int nvalid,
-                                        float mu, float rs, float inv) const {
+                                        float mu, float rs, float inv, bool sp = false) const {
         if constexpr (Q8)
-            emit_q8(g, b, static_cast<uint8_t*>(y) + offset, stride, nvalid, mu, rs, inv);
+            emit_q8(g, b, static_cast<uint8_t*>(y) + offset, stride, nvalid, mu, rs, inv, sp);
         else
-            emit(g, b, static_cast<T*>(y) + offset, stride, nvalid, mu, rs);
+            emit(g, b, static_cast<T*>(y) + offset, stride, nvalid, mu, rs, sp);
     }
 };
 
@@ -599,9 +618,10 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_group(
 // store h as soon as it is formed and the output pass re-reads h, not x and
 // r. Every thread re-reads only its own accesses, so h (and y) may be the x
 // or r buffer itself.
-template <class T, int VEC, int V, bool LN, bool CL, bool ADD, bool Q8>
+template <class T, int VEC, int V, bool LN, bool CL, bool ADD, bool Q8, bool SHIFT>
 __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(const NormArgs a) {
     using S = Slice<T, VEC, V, LN>;
+    using SO = ScalarOps<T>;
     __shared__ RowReduceSmem red;
 
     const int T_ = blockDim.x;
@@ -631,17 +651,39 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
         const float K = LN ? (ADD ? first_elem_add(xr, rr) : first_elem(xr)) : 0.f;
         s.set_shift(K);
         T* hr = ADD ? static_cast<T*>(a.h) + row * a.N : nullptr;
+        // SHIFT: the row's vectors start at its first 16-byte aligned element
+        // h0; the h0 elements before them and the tail after the last whole
+        // vector (together fewer than 2*VEC) are taken one per thread by the
+        // first threads of CTA rank 0 (xi: the element, xraw its value).
+        int h0 = 0, nb = nacc;
+        bool sp = false;  // gamma/beta vectors not 16-byte aligned in this row
+        int xi = -1;
+        typename SO::Raw xraw = 0;
+        if constexpr (SHIFT) {
+            const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(xr)) & 15u;
+            h0 = min(static_cast<int>(((16u - mis) & 15u) / sizeof(T)), a.N);
+            nb = (a.N - h0) / VEC;
+            sp = h0 != 0 || !a.vec_params;
+            const int nextra = a.N - nb * VEC;
+            if (rank == 0 && tid < nextra) {
+                xi = tid < h0 ? tid : h0 + nb * VEC + (tid - h0);
+                xraw = ADD ? SO::add_round(SO::load(xr + xi), SO::load(rr + xi)) : SO::load(xr + xi);
+            }
+        }
+        const T* xb = xr + h0;  // the row's vector body
+        const T* rb = ADD ? rr + h0 : nullptr;
+        T* hb = ADD ? hr + h0 : nullptr;
         float n_t = 0.f, sum_t = 0.f, mean_t = 0.f, m2_t = 0.f, ss_t = 0.f;
         int nv = 0;
         for (int i = 0; i < rounds; ++i) {
             const int r = ADD ? rounds - 1 - i : i;
             const int f = (r * static_cast<int>(C) + rank) * V * T_ + in_slice;
-            nv = valid_runs(nacc, f, 32, V);
+            nv = valid_runs(nb, f, 32, V);
             if constexpr (ADD) {
-                s.load_add(xr + f * VEC, rr + f * VEC, stride, nv);
-                if (r != 0) s.store_h(hr + f * VEC, stride, nv);
+                s.load_add(xb + f * VEC, rb + f * VEC, stride, nv);
+                if (r != 0) s.store_h(hb + f * VEC, stride, nv);
             } else {
-                s.load(xr + f * VEC, stride, nv);
+                s.load(xb + f * VEC, stride, nv);
             }
             if constexpr (LN) {
                 const float n = static_cast<float>(nv * VEC);
@@ -662,32 +704,72 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
                 ss_t += s.sumsq(nv);
             }
         }
+        if constexpr (SHIFT) {
+            if (xi >= 0) {  // fold the extra element in: the one-element update ([Ch7] §7.4)
+                const float xe = SO::e(xraw);
+                if constexpr (LN) {
+                    const float d0 = xe - K;
+                    const float n1 = n_t + 1.f;
+                    const float d = d0 - mean_t;
+                    mean_t += d / n1;
+                    m2_t = fmaf(d, d0 - mean_t, m2_t);
+                    sum_t += d0;
+                    n_t = n1;
+                } else {
+                    ss_t = fmaf(xe, xe, ss_t);
+                }
+            }
+        }
         float mu, rs;
         row_stats<LN>(red, n_t, sum_t, mean_t, m2_t, ss_t, invN, a.eps, C, nwarps, wwidth, mu, rs);
         if (LN && rank == 0 && tid == 0) {
             if (a.mean) a.mean[row] = K + mu;
             if (a.rstd) a.rstd[row] = rs;
         }
+        const T* gb = static_cast<const T*>(a.gamma) + h0;
+        const T* bb = static_cast<const T*>(a.beta) + h0;
+        const int64_t yb = row * a.N + h0;
+        if constexpr (SHIFT) {
+            if (xi >= 0) {  // the extra element's output (and h), after the row's barrier
+                const T* g1 = static_cast<const T*>(a.gamma) + xi;
+                const float nmr = -mu * rs;
+                if constexpr (Q8) {
+                    float o;
+                    if constexpr (LN)
+                        SO::ln_vals(xraw, K, rs, nmr, SO::load_param(g1), SO::load_param(static_cast<const T*>(a.beta) + xi),
+                                    &o);
+                    else
+                        SO::rms_vals(xraw, rs, SO::load_param(g1), &o);
+                    store_e4m3<1>(static_cast<uint8_t*>(a.y) + row * a.N + xi, &o, inv);
+                } else {
+                    T* y1 = static_cast<T*>(a.y) + row * a.N + xi;
+                    if constexpr (LN)
+                        SO::store(y1, SO::ln_out(xraw, K, rs, nmr, SO::load_param(g1),
+                                                 SO::load_param(static_cast<const T*>(a.beta) + xi)));
+                    else
+                        SO::store(y1, SO::rms_out(xraw, rs, SO::load_param(g1)));
+                }
+                if constexpr (ADD) SO::store(hr + xi, xraw);
+            }
+        }
         if constexpr (ADD) {
             for (int r = 0; r < rounds; ++r) {
                 const int f = (r * static_cast<int>(C) + rank) * V * T_ + in_slice;
                 if (r != 0) {
-                    nv = valid_runs(nacc, f, 32, V);
-                    s.load(hr + f * VEC, stride, nv);  // only this thread wrote h there
+                    nv = valid_runs(nb, f, 32, V);
+                    s.load(hb + f * VEC, stride, nv);  // only this thread wrote h there
                 }
-                s.template out<Q8>(static_cast<const T*>(a.gamma) + f * VEC, static_cast<const T*>(a.beta) + f * VEC,
-                                   a.y, row * a.N + f * VEC, stride, nv, mu, rs, inv);
-                if (r == 0) s.store_h(hr + f * VEC, stride, nv);
+                s.template out<Q8>(gb + f * VEC, bb + f * VEC, a.y, yb + f * VEC, stride, nv, mu, rs, inv, sp);
+                if (r == 0) s.store_h(hb + f * VEC, stride, nv);
             }
         } else {
             for (int r = rounds - 1; r >= 0; --r) {
                 const int f = (r * static_cast<int>(C) + rank) * V * T_ + in_slice;
                 if (r != rounds - 1) {
-                    nv = valid_runs(nacc, f, 32, V);
-                    s.load(xr + f * VEC, stride, nv);
+                    nv = valid_runs(nb, f, 32, V);
+                    s.load(xb + f * VEC, stride, nv);
                 }
-                s.template out<Q8>(static_cast<const T*>(a.gamma) + f * VEC, static_cast<const T*>(a.beta) + f * VEC,
-                                   a.y, row * a.N + f * VEC, stride, nv, mu, rs, inv);
+                s.template out<Q8>(gb + f * VEC, bb + f * VEC, a.y, yb + f * VEC, stride, nv, mu, rs, inv, sp);
             }
         }
     }
@@ -793,19 +875,25 @@ __global__ void __launch_bounds__(1024) norm_fwd_pipe(const NormArgs a) {
 template <class T, bool LN>
 using KernelFn = void (*)(const NormArgs);
 
+// SHIFT variants exist for the 16-byte vector width only (element rows
+// need no alignment).
 template <class T, bool LN, bool ADD, bool Q8, int VEC, int V>
-KernelFn<T, LN> pick_cta(bool cl) {
-    return cl ? norm_fwd_cta<T, VEC, V, LN, true, ADD, Q8> : norm_fwd_cta<T, VEC, V, LN, false, ADD, Q8>;
+KernelFn<T, LN> pick_cta(bool cl, bool shift) {
+    if constexpr (VEC > 1) {
+        if (shift)
+            return cl ? norm_fwd_cta<T, VEC, V, LN, true, ADD, Q8, true> : norm_fwd_cta<T, VEC, V, LN, false, ADD, Q8, true>;
+    }
+    return cl ? norm_fwd_cta<T, VEC, V, LN, true, ADD, Q8, false> : norm_fwd_cta<T, VEC, V, LN, false, ADD, Q8, false>;
 }
 
 template <class T, bool LN, bool ADD, bool Q8, int VEC>
-KernelFn<T, LN> pick_kernel(int mapping, int per_thread, bool cl) {
+KernelFn<T, LN> pick_kernel(int mapping, int per_thread, bool cl, bool shift) {
     const bool group = mapping == NORM_MAP_GROUP;
     switch (per_thread) {
-        case 1: return group ? norm_fwd_group<T, VEC, 1, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 1>(cl);
-        case 2: return group ? norm_fwd_group<T, VEC, 2, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 2>(cl);
-        case 4: return group ? norm_fwd_group<T, VEC, 4, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 4>(cl);
-        case 8: return group ? norm_fwd_group<T, VEC, 8, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 8>(cl);
+        case 1: return group ? norm_fwd_group<T, VEC, 1, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 1>(cl, shift);
+        case 2: return group ? norm_fwd_group<T, VEC, 2, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 2>(cl, shift);
+        case 4: return group ? norm_fwd_group<T, VEC, 4, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 4>(cl, shift);
+        case 8: return group ? norm_fwd_group<T, VEC, 8, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 8>(cl, shift);
         default: return nullptr;
     }
 }
@@ -884,8 +972,8 @@ cudaError_t launch_norm(const norm_plan& p, const NormArgs& a, cudaStream_t stre
             if (e != cudaSuccess) return e;
         }
     } else {
-        k = p.vec_elems == 1 ? pick_kernel<T, LN, ADD, Q8, 1>(p.mapping, p.per_thread, cl)
-                             : pick_kernel<T, LN, ADD, Q8, ElemVec<T>::value>(p.mapping, p.per_thread, cl);
+        k = p.vec_elems == 1 ? pick_kernel<T, LN, ADD, Q8, 1>(p.mapping, p.per_thread, cl, false)
+                             : pick_kernel<T, LN, ADD, Q8, ElemVec<T>::value>(p.mapping, p.per_thread, cl, a.shift != 0);
         if (k == nullptr) return cudaErrorInvalidValue;
     }
     cudaLaunchConfig_t cfg = {};

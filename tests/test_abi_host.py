@@ -173,12 +173,29 @@ def test_bad_plans_rejected(lib, kw):
 
 
 def test_vector_plan_needs_alignment(lib):
-    # 0x1004 is not 16-byte aligned: a 128-bit plan is refused
+    # x at 0x1004 and y at 0x1000 sit at different offsets within 16 bytes:
+    # no 128-bit plan
     q = ctypes.c_void_p(0x1004)
     p = _plan()
     assert lib.rms_fwd_planned(q, P, P, 4, 1000, 1e-6, rn.NORM_F32, None, ctypes.byref(p)) == rn.NORM_ERR_PLAN
-    # rows of 1001 fp32 are not whole 16-byte vectors
-    assert lib.rms_fwd_planned(P, P, P, 4, 1001, 1e-6, rn.NORM_F32, None, ctypes.byref(p)) == rn.NORM_ERR_PLAN
+    # not even element-aligned
+    assert lib.rms_fwd_planned(ctypes.c_void_p(0x1002), P, ctypes.c_void_p(0x1002), 4, 1000, 1e-6, rn.NORM_F32, None,
+                               ctypes.byref(p)) == rn.NORM_ERR_PLAN
+    # rows of 1001 fp32 are not whole vectors: a vector plan needs the CTA mapping and no ring
+    for kw in (dict(mapping=rn.NORM_MAP_GROUP, group=32, per_thread=8, threads=128),
+               dict(stages=3, grid=0, threads=256, per_thread=1)):
+        pp = _plan(**kw)
+        assert lib.rms_fwd_planned(P, P, P, 4, 1001, 1e-6, rn.NORM_F32, None, ctypes.byref(pp)) == rn.NORM_ERR_PLAN
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on the fake pointers")
+def test_phase_plans_pass_the_host_checks(lib):
+    """x and y both at offset 4 within 16 bytes, or rows of 1001 fp32: a
+    128-bit CTA plan is accepted (the call then fails at the device query)."""
+    q, r = ctypes.c_void_p(0x1004), ctypes.c_void_p(0x2004)
+    p = _plan()
+    assert lib.rms_fwd_planned(q, P, r, 4, 1000, 1e-6, rn.NORM_F32, None, ctypes.byref(p)) == rn.NORM_ERR_CUDA
+    assert lib.rms_fwd_planned(P, P, P, 4, 1001, 1e-6, rn.NORM_F32, None, ctypes.byref(p)) == rn.NORM_ERR_CUDA
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on the fake pointers")
@@ -209,7 +226,13 @@ def test_plans_are_consistent(lib, dtype, aligned, M):
     s = 4 if dtype == torch.float32 else 2
     for N in NS:
         p = rn.make_plan(M, N, dtype, aligned, 152)
-        vec = 16 // s if aligned and (N * s) % 16 == 0 else 1
+        if aligned and (N * s) % 16 == 0:
+            vec = 16 // s                                  # every row on a 16-byte boundary
+        elif aligned and -(-N // (16 // s)) >= 64:
+            vec = 16 // s                                  # rows off boundaries: vector body, CTA mapping
+            assert p["mapping"] == rn.NORM_MAP_CTA
+        else:
+            vec = 1
         assert p["vec_elems"] == vec
         assert p["per_thread"] in (1, 2, 4, 8)
         assert p["threads"] % 32 == 0 and 32 <= p["threads"] <= 1024
