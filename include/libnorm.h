@@ -148,6 +148,25 @@ norm_status rms_fwd_planned(const void* x, const void* w, void* y, int64_t M, in
                             const norm_plan* plan);
 
 /*
+ * ln_fwd / rms_fwd on strided rows ([T3] §④: the host wrapper keeps a
+ * row-strided view and copies only when the innermost stride is not 1):
+ * row r of x starts at x + r * ldx and row r of y at y + r * ldy (pitches in
+ * elements, each >= N), e.g. a column block of a wider matrix. y may be x
+ * itself when ldy == ldx. `plan` may be NULL (the plan ln_fwd would choose);
+ * otherwise it is checked as for ln_fwd_planned. Rows whose pitches differ
+ * modulo 16 bytes, or that start at different offsets within 16 bytes, use
+ * element accesses.
+ */
+norm_status ln_fwd_strided(const void* x, int64_t ldx, const void* gamma, const void* beta,
+                           void* y, int64_t ldy, float* mean, float* rstd, int64_t M,
+                           int64_t N, float eps, norm_dtype dtype, cudaStream_t stream,
+                           const norm_plan* plan);
+
+norm_status rms_fwd_strided(const void* x, int64_t ldx, const void* w, void* y, int64_t ldy,
+                            int64_t M, int64_t N, float eps, norm_dtype dtype,
+                            cudaStream_t stream, const norm_plan* plan);
+
+/*
  * Fused residual add + LayerNorm ([Ch7] §7.9-7.10, the add + norm of a
  * transformer's residual stream; [T3] §⑤):
  *   h_ri = x_ri + residual_ri, rounded to `dtype` (exactly what a separate

@@ -98,6 +98,8 @@ def library() -> ctypes.CDLL:
     L.rms_bwd_planned.argtypes = L.rms_bwd.argtypes + [ctypes.POINTER(NormPlan)]
     L.norm_bwd_make_plan.argtypes = [i64, i64, i32, i32, i32, i32, ctypes.POINTER(NormPlan)]
     L.norm_bwd_workspace_bytes.argtypes = [ctypes.POINTER(NormPlan), i64, i32, ctypes.POINTER(sz)]
+    L.ln_fwd_strided.argtypes = [vp, i64, vp, vp, vp, i64, vp, vp, i64, i64, f32, i32, vp, ctypes.POINTER(NormPlan)]
+    L.rms_fwd_strided.argtypes = [vp, i64, vp, vp, i64, i64, i64, f32, i32, vp, ctypes.POINTER(NormPlan)]
     L.ln_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, f32, i32, vp]
     L.rms_fwd_fp8.argtypes = [vp, vp, vp, vp, i64, i64, f32, i32, vp]
     L.ln_fwd_add_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, f32, i32, vp]
@@ -108,7 +110,7 @@ def library() -> ctypes.CDLL:
               "ln_fwd_add_planned", "rms_fwd_add_planned", "norm_make_plan", "norm_make_plan_add",
               "ln_bwd", "rms_bwd", "ln_bwd_planned", "rms_bwd_planned", "norm_bwd_make_plan",
               "norm_bwd_workspace_bytes", "ln_fwd_fp8", "rms_fwd_fp8", "ln_fwd_add_fp8", "rms_fwd_add_fp8",
-              "ln_fwd_fp8_planned", "rms_fwd_fp8_planned",
+              "ln_fwd_fp8_planned", "rms_fwd_fp8_planned", "ln_fwd_strided", "rms_fwd_strided",
               "norm_last_cuda_error", "norm_abi_version"):
         getattr(L, f).restype = ctypes.c_int
     L.norm_status_string.argtypes = [ctypes.c_int]
@@ -166,6 +168,22 @@ def _rows(x: torch.Tensor) -> torch.Tensor:
     return x2 if x2.is_contiguous() else x2.contiguous()
 
 
+def _strided_rows(x: torch.Tensor) -> torch.Tensor:
+    """[M, N] rows of x without a copy when its rows are evenly strided with
+    unit inner stride (the T3 drill's host wrapper, §④); else a contiguous
+    copy."""
+    if x.dim() == 0:
+        raise ValueError("input must have at least one dimension")
+    x2 = x.reshape(-1, x.shape[-1])
+    if x2.stride(-1) == 1 and (x2.shape[0] <= 1 or x2.stride(0) >= x2.shape[1]):
+        return x2
+    return x2.contiguous()
+
+
+def _pitch(t: torch.Tensor) -> int:
+    return t.stride(0) if t.shape[0] > 1 else t.shape[1]
+
+
 def _param(p: torch.Tensor, x: torch.Tensor, name: str) -> torch.Tensor:
     if p.device != x.device or p.dtype != x.dtype:
         raise ValueError(f"{name} must be on {x.device} with dtype {x.dtype}")
@@ -180,6 +198,23 @@ def _out(t: Optional[torch.Tensor], x: torch.Tensor, x2: torch.Tensor, name: str
             or y.device != x.device:
         raise ValueError(f"{name} must be a contiguous tensor of x's shape, dtype and device")
     return y
+
+
+def _strided_out(out: Optional[torch.Tensor], x: torch.Tensor, x2: torch.Tensor) -> torch.Tensor:
+    """The output rows: a new contiguous tensor, or `out` (of x's shape and
+    dtype) as strided rows when its rows are evenly strided."""
+    if out is None:
+        return torch.empty(x2.shape, dtype=x.dtype, device=x.device)
+    if out.shape != x.shape and out.shape != x2.shape or out.dtype != x.dtype or out.device != x.device:
+        raise ValueError("out must have x's shape, dtype and device")
+    y = out.reshape(-1, x2.shape[1])   # a view when the leading dims collapse into one row stride
+    if y.data_ptr() != out.data_ptr() or y.stride(-1) != 1 or (y.shape[0] > 1 and y.stride(0) < y.shape[1]):
+        raise ValueError("out must have evenly strided rows with unit inner stride")
+    return y
+
+
+def _shaped(y: torch.Tensor, x: torch.Tensor, out: Optional[torch.Tensor]) -> torch.Tensor:
+    return out if out is not None else y.view(x.shape)
 
 
 def _residual(r: torch.Tensor, x: torch.Tensor) -> torch.Tensor:
@@ -226,21 +261,25 @@ def ln_fwd(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float 
     if not x.is_cuda:
         raise ValueError("ln_fwd needs a CUDA tensor")
     code = _dtype_code(x.dtype)
-    x2 = _rows(x)
+    x2 = _strided_rows(x)
     M, N = x2.shape
     g = _param(gamma, x, "gamma")
     b = _param(beta, x, "beta")
-    y = _out(out, x, x2, "out")
+    y = _strided_out(out, x, x2)
     mean, rstd = _stats(M, x, mean, rstd, stats)
     L = library()
-    args = (x2.data_ptr(), g.data_ptr(), b.data_ptr(), y.data_ptr(), _ptr(mean), _ptr(rstd),
-            M, N, float(eps), code)
     with torch.cuda.device(x.device):
         h = _stream_handle(stream, x.device)
-        st = (L.ln_fwd(*args, h) if plan is None else L.ln_fwd_planned(*args, h, _plan_ptr(plan)))
+        if x2.is_contiguous() and y.is_contiguous():
+            args = (x2.data_ptr(), g.data_ptr(), b.data_ptr(), y.data_ptr(), _ptr(mean), _ptr(rstd),
+                    M, N, float(eps), code)
+            st = (L.ln_fwd(*args, h) if plan is None else L.ln_fwd_planned(*args, h, _plan_ptr(plan)))
+        else:
+            st = L.ln_fwd_strided(x2.data_ptr(), _pitch(x2), g.data_ptr(), b.data_ptr(), y.data_ptr(), _pitch(y),
+                                  _ptr(mean), _ptr(rstd), M, N, float(eps), code, h, _plan_ptr(plan))
     if st != NORM_OK:
         raise NormError(st, "ln_fwd")
-    return y.view(x.shape), mean, rstd
+    return _shaped(y, x, out), mean, rstd
 
 
 def rms_fwd(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6, *, out: Optional[torch.Tensor] = None,
@@ -249,18 +288,22 @@ def rms_fwd(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6, *, out: Optiona
     if not x.is_cuda:
         raise ValueError("rms_fwd needs a CUDA tensor")
     code = _dtype_code(x.dtype)
-    x2 = _rows(x)
+    x2 = _strided_rows(x)
     M, N = x2.shape
     wv = _param(w, x, "w")
-    y = _out(out, x, x2, "out")
+    y = _strided_out(out, x, x2)
     L = library()
-    args = (x2.data_ptr(), wv.data_ptr(), y.data_ptr(), M, N, float(eps), code)
     with torch.cuda.device(x.device):
         h = _stream_handle(stream, x.device)
-        st = (L.rms_fwd(*args, h) if plan is None else L.rms_fwd_planned(*args, h, _plan_ptr(plan)))
+        if x2.is_contiguous() and y.is_contiguous():
+            args = (x2.data_ptr(), wv.data_ptr(), y.data_ptr(), M, N, float(eps), code)
+            st = (L.rms_fwd(*args, h) if plan is None else L.rms_fwd_planned(*args, h, _plan_ptr(plan)))
+        else:
+            st = L.rms_fwd_strided(x2.data_ptr(), _pitch(x2), wv.data_ptr(), y.data_ptr(), _pitch(y), M, N,
+                                   float(eps), code, h, _plan_ptr(plan))
     if st != NORM_OK:
         raise NormError(st, "rms_fwd")
-    return y.view(x.shape)
+    return _shaped(y, x, out)
 
 
 def ln_fwd_add(x: torch.Tensor, residual: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor,

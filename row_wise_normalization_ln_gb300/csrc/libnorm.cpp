@@ -351,6 +351,8 @@ norm_status run(bool ln, const NormArgs& a, norm_dtype dtype, int mode, cudaStre
     if (sms <= 0) return NORM_ERR_CUDA;
     if (!user_plan) make_plan(a.M, a.N, dtype, mode, sms, add, &plan);
     NormArgs args = a;
+    if (args.ldx == 0) args.ldx = a.N;  // contiguous rows
+    if (args.ldy == 0) args.ldy = a.N;
     args.group = plan.group;
     args.rounds = plan.rounds;
     args.stages = plan.stages;
@@ -420,6 +422,32 @@ norm_status rms_add_impl(const void* x, const void* res, const void* w, void* h,
     NormArgs a{x, w, nullptr, y, nullptr, nullptr, res, h, nullptr, M, static_cast<int32_t>(N), eps, 0, 1, 0};
     a.vec_params = vp;
     return run(false, a, dtype, mode, stream, plan);
+}
+
+// Strided rows: x and y rows ldx and ldy elements apart (>= N). The access
+// mode then also looks at the pitches: full vectors need pitches of whole
+// 16-byte vectors, a shared phase needs the pitches to agree modulo 16 bytes.
+norm_status strided_impl(bool ln, const void* x, int64_t ldx, const void* gamma, const void* beta, void* y,
+                         int64_t ldy, float* mean, float* rstd, int64_t M, int64_t N, float eps, norm_dtype dtype,
+                         cudaStream_t stream, const norm_plan* plan) {
+    norm_status st = check_sizes(M, N, dtype);
+    if (st != NORM_OK) return st;
+    if (!std::isfinite(eps) || eps < 0.f) return NORM_ERR_ARG;
+    if (ldx < N || ldy < N) return NORM_ERR_ARG;
+    if (M == 0) return NORM_OK;
+    if ((M - 1) > (INT64_MAX - N) / std::max(ldx, ldy)) return NORM_ERR_ARG;
+    if (!x || !gamma || (ln && !beta) || !y) return NORM_ERR_ARG;
+    const int64_t s = elem_size(dtype);
+    bool vp = true;
+    int mode = ln ? align_mode({x, y}, {gamma, beta}, nullptr, dtype, &vp) : align_mode({x, y}, {gamma}, nullptr, dtype, &vp);
+    if (mode != kAlignNone && ((ldx * s) & 15) != ((ldy * s) & 15)) mode = kAlignNone;
+    if (mode == kAlignFull && ((ldx * s) & 15) != 0) mode = kAlignPhase;
+    NormArgs a{x, gamma, ln ? beta : nullptr, y, ln ? mean : nullptr, ln ? rstd : nullptr, nullptr, nullptr, nullptr,
+               M, static_cast<int32_t>(N), eps, 0, 1, 0};
+    a.ldx = ldx;
+    a.ldy = ldy;
+    a.vec_params = vp;
+    return run(ln, a, dtype, mode, stream, plan);
 }
 
 // FP8 output: y8 holds one E4M3 byte per element; scale is one fp32 value
@@ -578,6 +606,17 @@ norm_status rms_fwd_add_planned(const void* x, const void* residual, const void*
                                 int64_t N, float eps, norm_dtype dtype, cudaStream_t stream,
                                 const norm_plan* plan) {
     return rms_add_impl(x, residual, w, h, y, M, N, eps, dtype, stream, plan);
+}
+
+norm_status ln_fwd_strided(const void* x, int64_t ldx, const void* gamma, const void* beta, void* y, int64_t ldy,
+                           float* mean, float* rstd, int64_t M, int64_t N, float eps, norm_dtype dtype,
+                           cudaStream_t stream, const norm_plan* plan) {
+    return strided_impl(true, x, ldx, gamma, beta, y, ldy, mean, rstd, M, N, eps, dtype, stream, plan);
+}
+
+norm_status rms_fwd_strided(const void* x, int64_t ldx, const void* w, void* y, int64_t ldy, int64_t M, int64_t N,
+                            float eps, norm_dtype dtype, cudaStream_t stream, const norm_plan* plan) {
+    return strided_impl(false, x, ldx, w, nullptr, y, ldy, nullptr, nullptr, M, N, eps, dtype, stream, plan);
 }
 
 norm_status ln_fwd_fp8(const void* x, const void* gamma, const void* beta, const float* scale, void* y8, float* mean,

@@ -15,10 +15,10 @@ namespace libnorm {
 constexpr int kFusedMaxThreads = 512;
 
 struct NormArgs {
-    const void* x;      // [M, N]
+    const void* x;      // [M, N], row pitch ldx
     const void* gamma;  // [N] (LayerNorm gamma, RMSNorm w)
     const void* beta;   // [N] (LayerNorm only)
-    void* y;            // [M, N]
+    void* y;            // [M, N], row pitch ldy
     float* mean;        // [M] or null (LayerNorm only)
     float* rstd;        // [M] or null (LayerNorm only)
     const void* res;    // [M, N] residual (fused residual add only)
@@ -30,6 +30,8 @@ struct NormArgs {
     int32_t group;      // GROUP mapping: lanes per row
     int32_t rounds;     // CTA mapping: register-sized rounds per row
     int32_t stages;     // pipelined CTA mapping: shared-memory ring stages
+    int64_t ldx = 0;         // row pitch of x in elements (set to N for contiguous rows)
+    int64_t ldy = 0;         // row pitch of y in elements (bytes for an FP8 y)
     int32_t shift = 0;       // CTA mapping, 16-byte vectors: rows need not start on a 16-byte boundary
     int32_t vec_params = 1;  // gamma (and beta) 16-byte aligned
 };

@@ -572,7 +572,7 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_group(
         const int64_t row = rb * rows_per_cta + tid / G;
         const bool row_ok = row < a.M;
         const int nv = row_ok ? nvalid : 0;
-        const T* xr = static_cast<const T*>(a.x) + row * a.N;
+        const T* xr = static_cast<const T*>(a.x) + row * a.ldx;
         const T* rr = ADD ? static_cast<const T*>(a.res) + row * a.N : nullptr;
         S s;
         const float K = (LN && row_ok) ? (ADD ? first_elem_add(xr, rr) : first_elem(xr)) : 0.f;
@@ -596,7 +596,7 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_group(
         } else {
             rs = rsqrtf(group_sum(s.sumsq(nv), G) * invN + a.eps);
         }
-        s.template out<Q8>(g, b, a.y, row * a.N + gl * VEC, stride, nv, mu, rs, inv);
+        s.template out<Q8>(g, b, a.y, row * a.ldy + gl * VEC, stride, nv, mu, rs, inv);
         if constexpr (ADD) s.store_h(static_cast<T*>(a.h) + row * a.N + gl * VEC, stride, nv);
     }
 }
@@ -645,7 +645,7 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
     const float inv = Q8 ? 1.f / *a.qscale : 0.f;
 
     for (int64_t row = first_row; row < a.M; row += row_step) {
-        const T* xr = static_cast<const T*>(a.x) + row * a.N;
+        const T* xr = static_cast<const T*>(a.x) + row * a.ldx;
         const T* rr = ADD ? static_cast<const T*>(a.res) + row * a.N : nullptr;
         S s;
         const float K = LN ? (ADD ? first_elem_add(xr, rr) : first_elem(xr)) : 0.f;
@@ -728,7 +728,7 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
         }
         const T* gb = static_cast<const T*>(a.gamma) + h0;
         const T* bb = static_cast<const T*>(a.beta) + h0;
-        const int64_t yb = row * a.N + h0;
+        const int64_t yb = row * a.ldy + h0;
         if constexpr (SHIFT) {
             if (xi >= 0) {  // the extra element's output (and h), after the row's barrier
                 const T* g1 = static_cast<const T*>(a.gamma) + xi;
@@ -740,9 +740,9 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
                                     &o);
                     else
                         SO::rms_vals(xraw, rs, SO::load_param(g1), &o);
-                    store_e4m3<1>(static_cast<uint8_t*>(a.y) + row * a.N + xi, &o, inv);
+                    store_e4m3<1>(static_cast<uint8_t*>(a.y) + row * a.ldy + xi, &o, inv);
                 } else {
-                    T* y1 = static_cast<T*>(a.y) + row * a.N + xi;
+                    T* y1 = static_cast<T*>(a.y) + row * a.ldy + xi;
                     if constexpr (LN)
                         SO::store(y1, SO::ln_out(xraw, K, rs, nmr, SO::load_param(g1),
                                                  SO::load_param(static_cast<const T*>(a.beta) + xi)));
@@ -823,12 +823,12 @@ __global__ void __launch_bounds__(1024) norm_fwd_pipe(const NormArgs a) {
     // in step.
     auto issue = [&](int64_t row, int st) {
         if (row < a.M) {
-            const T* src = static_cast<const T*>(a.x) + row * a.N + first * VEC;
+            const T* src = static_cast<const T*>(a.x) + row * a.ldx + first * VEC;
             uint4* dst = ring + st * stage_slots + in_slice;
 #pragma unroll
             for (int j = 0; j < V; ++j)
                 if (j < nvalid) cp_async16(dst + j * 32, src + j * stride);
-            if (LN && lane == 0) cp_async4(&kslot[st * 32 + warp], static_cast<const T*>(a.x) + row * a.N);
+            if (LN && lane == 0) cp_async4(&kslot[st * 32 + warp], static_cast<const T*>(a.x) + row * a.ldx);
         }
         cp_async_commit();
     };
@@ -863,7 +863,7 @@ __global__ void __launch_bounds__(1024) norm_fwd_pipe(const NormArgs a) {
             if (a.mean) a.mean[row] = K + mu;
             if (a.rstd) a.rstd[row] = rs;
         }
-        s.emit(g, b, static_cast<T*>(a.y) + row * a.N + first * VEC, stride, nvalid, mu, rs);
+        s.emit(g, b, static_cast<T*>(a.y) + row * a.ldy + first * VEC, stride, nvalid, mu, rs);
         st = st + 1 == stages ? 0 : st + 1;
     }
     cp_async_wait(0);  // nothing of ours may land after exit

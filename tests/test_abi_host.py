@@ -35,6 +35,7 @@ def test_header_declares_the_abi():
         "ln_bwd", "rms_bwd", "ln_bwd_planned", "rms_bwd_planned", "norm_bwd_make_plan", "norm_bwd_workspace_bytes",
         "ln_bwd_noalloc",
         "ln_fwd_fp8", "rms_fwd_fp8", "ln_fwd_add_fp8", "rms_fwd_add_fp8", "ln_fwd_fp8_planned", "rms_fwd_fp8_planned",
+        "ln_fwd_strided", "rms_fwd_strided",
         "norm_status_string", "norm_last_cuda_error", "norm_abi_version"}
 
 
@@ -436,3 +437,18 @@ def test_fp8_argument_checks(lib):
     p = _plan(stages=3, grid=0)
     assert lib.rms_fwd_fp8_planned(P, None, P, S, None, Q, 4, 1000, 1e-6, rn.NORM_F32, None,
                                    ctypes.byref(p)) == rn.NORM_ERR_PLAN
+
+
+
+# ---------------------------------------------------------------- strided rows
+
+def test_strided_argument_checks(lib):
+    # pitches below N, overflowing extents
+    assert lib.ln_fwd_strided(P, 7, P, P, Q, 8, None, None, 4, 8, 1e-5, rn.NORM_F32, None, None) == rn.NORM_ERR_ARG
+    assert lib.rms_fwd_strided(P, 8, P, Q, 3, 4, 8, 1e-6, rn.NORM_F32, None, None) == rn.NORM_ERR_ARG
+    assert lib.rms_fwd_strided(P, 1 << 40, P, Q, 8, 1 << 24, 8, 1e-6, rn.NORM_F32, None, None) == rn.NORM_ERR_ARG
+    assert lib.rms_fwd_strided(None, 8, None, None, 8, 0, 8, 1e-6, rn.NORM_F32, None, None) == rn.NORM_OK
+    # pitches that differ modulo 16 bytes: no vector plan
+    p = _plan(threads=256, per_thread=1, vec_elems=4)
+    assert lib.rms_fwd_strided(P, 1001, P, Q, 1002, 4, 1000, 1e-6, rn.NORM_F32, None,
+                               ctypes.byref(p)) == rn.NORM_ERR_PLAN
