@@ -500,8 +500,8 @@ def time_e2e(w, rn, inp, device, steps):
 
 # ------------------------------------------------------------------ CPU oracle
 
-def oracle_rows(w, inp, rows: int):
-    """One call of the fp64 oracle over the first `rows` rows (with an FP8
+def oracle_rows(w, inp, rows: int, r0: int = 0):
+    """One call of the fp64 oracle over rows [r0, r0 + rows) (with an FP8
     output: the norm, then the quantisation of its values)."""
     import numpy as np
     import oracle
@@ -511,15 +511,15 @@ def oracle_rows(w, inp, rows: int):
         t = t.contiguous()
         return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
 
-    x = npx(inp["x"][:rows])
+    x = npx(inp["x"][r0:r0 + rows])
     e = oracle.eps_as_f32(w.eps)
     if w.bwd:
-        dy = npx(inp["dy"][:rows])
+        dy = npx(inp["dy"][r0:r0 + rows])
         if w.op == "ln":
             return lambda: oracle.ln_bwd(dy, x, npx(inp["gamma"]), e)
         return lambda: oracle.rms_bwd(dy, x, npx(inp["w"]), e)
     if w.add:
-        r = npx(inp["r"][:rows])
+        r = npx(inp["r"][r0:r0 + rows])
         if w.op == "ln":
             norm = lambda: oracle.ln_fwd_add(x, r, npx(inp["gamma"]), npx(inp["beta"]), e)[1]
         else:
@@ -549,6 +549,33 @@ def cpu_baseline(w, inp, seconds: float):
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{passes} full pass(es) of {w.M}x{w.N} {w.dtype} in {el:.1f} s, fp64, 1 thread",
             "host_cores": os.cpu_count()}
+
+
+def cpu_baseline_all_cores(w, inp, seconds: float):
+    """The same oracle on every host core: the rows split into one block per
+    core, each block run over and over by its own thread (the oracle is C
+    called through ctypes, which releases the GIL) for about `seconds`."""
+    from concurrent.futures import ThreadPoolExecutor
+    n = max(1, min(os.cpu_count() or 1, w.M))
+    bounds = [(w.M * i // n, w.M * (i + 1) // n) for i in range(n)]
+    runs = [oracle_rows(w, inp, r1 - r0, r0) for r0, r1 in bounds]
+
+    def spin(run):
+        passes, t0 = 0, time.perf_counter()
+        while True:
+            run()
+            passes += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return passes, el
+
+    with ThreadPoolExecutor(n) as ex:
+        res = list(ex.map(spin, runs))
+    moved = sum(p * w.algorithmic_bytes(r1 - r0) for (p, _), (r0, r1) in zip(res, bounds))
+    el = max(e for _, e in res)
+    return {"value": round(moved / el / 1e9, 4), "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": f"{w.M} rows in {n} blocks, one thread each, {min(p for p, _ in res)}+ passes per block "
+                      f"in {el:.1f} s, fp64"}
 
 
 # ------------------------------------------------------------------ ranks
@@ -676,6 +703,7 @@ def main():
         return
 
     cpu = cpu_baseline(w, inp, args.cpu_seconds)
+    cpu_all = cpu_baseline_all_cores(w, inp, args.cpu_seconds)
     line = {
         "metric": metric_name(w), "value": round(value, 2), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
@@ -697,6 +725,7 @@ def main():
         "gpu_launches": args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "cpu_baseline_all_cores": cpu_all,
         "workloads": table,
         "gpu": props.name,
     }
