@@ -80,8 +80,9 @@ def measured_peak():
 # capture summarised in profiles/ (workload -> (kernel source hash at capture,
 # bytes per launch, summary file)).
 NCU_TRAFFIC = {
-    "rms_f32_8192x4096": ("2065e84ec5a8a594", 212_646_144, "profiles/norm_fwd_cta_rms_f32_8192x4096.md"),
-    "ln_bf16_4096x8192_outliers": ("2065e84ec5a8a594", 85_873_920, "profiles/norm_fwd_cta_ln_bf16_4096x8192.md"),
+    "rms_f32_8192x4096": ("3c51d76047e35e0d", 208_681_216, "profiles/norm_fwd_cta_rms_f32_8192x4096.md"),
+    "ln_bf16_4096x8192_outliers": ("3c51d76047e35e0d", 85_004_800, "profiles/norm_fwd_cta_ln_bf16_4096x8192.md"),
+    "ln_f32_8192x5001": ("3c51d76047e35e0d", 277_780_480, "profiles/norm_fwd_cta_shift_ln_f32_8192x5001.md"),
 }
 
 

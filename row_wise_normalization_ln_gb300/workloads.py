@@ -19,6 +19,7 @@ Workloads (shapes and value distributions of the source pages):
   ln_f32_2048x65536        LayerNorm fp32 long rows; x ~ N(3,1).
   ln_f32_8192x5000         LayerNorm fp32, N not a power of two; x ~ N(3,1).
   ln_f16_4096x8192         LayerNorm fp16 rows, the T3 drill's N; x ~ N(3,1).
+  ln_f32_8192x5001         LayerNorm fp32, odd N: rows off 16-byte boundaries.
   add_*                    the fused residual add + norm on the shape and
                            recipe of the workload it names: the residual r is
                            drawn from the same recipe, after the parameters.
@@ -106,6 +107,7 @@ WORKLOADS = {
         Workload("ln_f32_2048x65536", "ln", "f32", 2048, 65536, 1e-5, "normal31"),
         Workload("ln_f32_8192x5000", "ln", "f32", 8192, 5000, 1e-5, "normal31"),
         Workload("ln_f16_4096x8192", "ln", "f16", 4096, 8192, 1e-5, "normal31"),
+        Workload("ln_f32_8192x5001", "ln", "f32", 8192, 5001, 1e-5, "normal31"),
         Workload("add_rms_f32_8192x4096", "rms", "f32", 8192, 4096, 1e-6, "uniform_pm1", True),
         Workload("add_rms_bf16_65536x2048", "rms", "bf16", 65536, 2048, 1e-6, "uniform_pm1", True),
         Workload("add_ln_bf16_4096x8192_outliers", "ln", "bf16", 4096, 8192, 1e-5, "offset_outliers", True),

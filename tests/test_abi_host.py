@@ -277,6 +277,8 @@ def test_plans_for_the_workloads(lib):
         "ln_f32_2048x65536": dict(mapping=rn.NORM_MAP_CTA, per_thread=8, threads=128, cluster=8, rounds=2),
         "ln_f32_8192x5000": dict(mapping=rn.NORM_MAP_CTA, per_thread=8, threads=160, cluster=1, rounds=1),
         "ln_f16_4096x8192": dict(mapping=rn.NORM_MAP_CTA, per_thread=8, threads=128, cluster=1, rounds=1),
+        "ln_f32_8192x5001": dict(mapping=rn.NORM_MAP_CTA, vec_elems=4, per_thread=8, threads=160, cluster=1,
+                                 rounds=1),
     }
     got.update({name: rn.make_plan(w.M, w.N, w.torch_dtype, True, 152, add=True)
                 for name, w in WORKLOADS.items() if w.add})

@@ -51,7 +51,7 @@ def run_rms(x, w, eps, plan=None):
 PLAIN = [n for n, w in wl.WORKLOADS.items() if not (w.add or w.bwd or w.fp8)]   # the others: their own files
 SMALL_M = {"ln_f32_128x1024": 128, "rms_f32_8192x4096": 96, "ln_bf16_4096x8192_outliers": 64,
            "rms_bf16_65536x2048": 517, "ln_f32_2048x65536": 6, "ln_f32_8192x5000": 77,
-           "ln_f16_4096x8192": 64}
+           "ln_f16_4096x8192": 64, "ln_f32_8192x5001": 77}
 
 
 @pytest.mark.parametrize("name", PLAIN)
