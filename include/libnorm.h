@@ -188,9 +188,9 @@ norm_status rms_fwd_add(const void* x, const void* residual, const void* w, void
                         cudaStream_t stream);
 
 /* The plan ln_fwd_add / rms_fwd_add would choose: as norm_make_plan, with
- * CTAs of at most 512 threads (the fused kernels keep two rows' worth of
- * loads in flight and need the registers). `aligned16` covers all six
- * pointers. Host only. */
+ * CTAs of at most 512 threads (the fused kernels keep two loads per access
+ * in flight and need the registers). `aligned16` as for norm_make_plan
+ * (0, 1 or 2), over all six pointers. Host only. */
 norm_status norm_make_plan_add(int64_t M, int64_t N, norm_dtype dtype, int aligned16,
                                int num_sms, norm_plan* plan);
 
@@ -253,6 +253,8 @@ norm_status rms_bwd(const void* dy, const void* x, const void* w, void* dx, floa
  * distributed shared memory before one partial row goes to the workspace.
  * At most `grid` CTAs walk the rows in a grid-stride loop: the launch takes
  * no more than can be resident on the device at once (0 when M == 0).
+ * `aligned16` != 0 when dy, x, gamma and dx are 16-byte aligned (the
+ * backward has no shifted-row mode: other rows use element accesses).
  * Returns NORM_ERR_ARG for rows beyond the backward's limit.
  */
 norm_status norm_bwd_make_plan(int64_t M, int64_t N, norm_dtype dtype, int layer_norm,
