@@ -254,15 +254,19 @@ def test_plans_are_consistent(lib, dtype, aligned, M):
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("M", [1, 3, 128, 8192])
 def test_fused_add_plans_are_consistent(lib, dtype, M):
-    """The fused calls plan as the plain ones, with CTAs of at most 512
-    threads and no ring; where the plain plan already fits, it is the same."""
+    """The fused calls' plans: CTAs of at most 512 threads, no ring, the row
+    covered; short rows in lane groups as the plain calls; at most 4
+    accesses per thread per round."""
     for N in NS:
         p = rn.make_plan(M, N, dtype, True, 152, add=True)
         q = rn.make_plan(M, N, dtype, True, 152)
         assert 32 <= p["threads"] <= 512 and p["stages"] == 0
         assert _covers(p, N), (N, p)
-        if q["threads"] <= 512:
+        if q["mapping"] == rn.NORM_MAP_GROUP:
             assert p == q, (N, p, q)
+        else:
+            assert p["mapping"] == rn.NORM_MAP_CTA and p["per_thread"] <= 4
+            assert p["grid"] == M * p["cluster"]
 
 
 def test_plans_for_the_workloads(lib):
@@ -282,11 +286,12 @@ def test_plans_for_the_workloads(lib):
     }
     got.update({name: rn.make_plan(w.M, w.N, w.torch_dtype, True, 152, add=True)
                 for name, w in WORKLOADS.items() if w.add})
-    want.update({
-        "add_rms_f32_8192x4096": want["rms_f32_8192x4096"],
-        "add_rms_bf16_65536x2048": want["rms_bf16_65536x2048"],
-        "add_ln_bf16_4096x8192_outliers": want["ln_bf16_4096x8192_outliers"],
-        "add_ln_f32_2048x65536": want["ln_f32_2048x65536"],
+    want.update({   # the fused add: 4 accesses per thread per round, more rounds; long rows 2 per round
+        "add_rms_f32_8192x4096": dict(mapping=rn.NORM_MAP_CTA, per_thread=4, threads=128, cluster=1, rounds=2),
+        "add_rms_bf16_65536x2048": dict(mapping=rn.NORM_MAP_CTA, per_thread=4, threads=64, cluster=1, rounds=1),
+        "add_ln_bf16_4096x8192_outliers": dict(mapping=rn.NORM_MAP_CTA, per_thread=4, threads=128, cluster=1,
+                                               rounds=2),
+        "add_ln_f32_2048x65536": dict(mapping=rn.NORM_MAP_CTA, per_thread=2, threads=128, cluster=8, rounds=8),
     })
     for name, w in want.items():
         for k, v in w.items():
