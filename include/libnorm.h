@@ -80,9 +80,10 @@ typedef enum {
  * rounds are read again for the output (served from L2 when they fit).
  *
  * With `stages` >= 2 (CTA mapping, 16-byte vectors, one round) the CTAs are
- * persistent and keep the next stages-1 rows of their share in flight in a
- * ring of shared-memory stages (cp.async) while they reduce and store the
- * current row; `grid` 0 then means "as many CTAs as fit on the device",
+ * persistent and keep up to `stages` upcoming rows of their share in flight
+ * in a ring of shared-memory stages (one bulk copy per CTA and row) while
+ * they reduce and store the current row; each thread widens its elements
+ * to fp32 once. `grid` 0 then means "as many CTAs as fit on the device",
  * resolved at launch from the kernel's occupancy.
  */
 typedef struct {
@@ -356,6 +357,15 @@ int norm_last_cuda_error(void);
 
 /* Version of this interface (bumped on any incompatible change). */
 int norm_abi_version(void);
+
+/*
+ * The ring kernels (plans with `stages` >= 2) wait for their bulk copies
+ * with a time limit (2 s); a wait that runs out is counted on the device
+ * and the call's outputs are then not to be trusted. Reads the current
+ * device's count into *count and resets it to 0 (synchronises the device).
+ * NORM_ERR_ARG if count is NULL; NORM_ERR_CUDA on a runtime error.
+ */
+norm_status norm_wait_timeouts(uint32_t* count);
 
 #ifdef __cplusplus
 }

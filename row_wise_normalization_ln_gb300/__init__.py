@@ -111,12 +111,24 @@ def library() -> ctypes.CDLL:
               "ln_bwd", "rms_bwd", "ln_bwd_planned", "rms_bwd_planned", "norm_bwd_make_plan",
               "norm_bwd_workspace_bytes", "ln_fwd_fp8", "rms_fwd_fp8", "ln_fwd_add_fp8", "rms_fwd_add_fp8",
               "ln_fwd_fp8_planned", "rms_fwd_fp8_planned", "ln_fwd_strided", "rms_fwd_strided",
-              "norm_last_cuda_error", "norm_abi_version"):
+              "norm_last_cuda_error", "norm_abi_version", "norm_wait_timeouts"):
         getattr(L, f).restype = ctypes.c_int
+    L.norm_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     L.norm_status_string.argtypes = [ctypes.c_int]
     L.norm_status_string.restype = ctypes.c_char_p
     _lib = L
     return L
+
+
+def wait_timeouts() -> int:
+    """Waits of the ring kernels (plans with stages >= 2) that ran out of
+    time on the current device since the last call; resets the count.
+    Synchronises the device."""
+    n = ctypes.c_uint32(0)
+    st = library().norm_wait_timeouts(ctypes.byref(n))
+    if st != NORM_OK:
+        raise NormError(st, "norm_wait_timeouts")
+    return n.value
 
 
 def _dtype_code(t: torch.dtype) -> int:

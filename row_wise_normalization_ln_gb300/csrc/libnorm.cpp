@@ -227,8 +227,8 @@ norm_status check_plan(const norm_plan& in, int64_t N, norm_dtype dtype, int mod
     }
     if (p.stages != 0) {
         if (p.stages < 2 || p.stages > kMaxStages || p.vec_elems == 1 || p.rounds != 1) return NORM_ERR_PLAN;
-        const int64_t smem = int64_t(p.stages) * p.per_thread * p.threads * 16 + p.stages * 32 * 4;
-        if (smem > kMaxSmem) return NORM_ERR_PLAN;
+        if (p.threads > libnorm::kRingMaxThreads) return NORM_ERR_PLAN;
+        if (libnorm::ring_smem_bytes(p.stages, p.per_thread, p.threads) > kMaxSmem) return NORM_ERR_PLAN;
         if (p.grid == 0) {  // resolved at launch
             *out = p;
             return NORM_OK;

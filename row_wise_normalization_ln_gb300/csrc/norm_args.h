@@ -29,12 +29,16 @@ struct NormArgs {
     float eps;
     int32_t group;      // GROUP mapping: lanes per row
     int32_t rounds;     // CTA mapping: register-sized rounds per row
-    int32_t stages;     // pipelined CTA mapping: shared-memory ring stages
+    int32_t stages;     // ring CTA mapping: shared-memory stages
+    int16_t shift = 0;       // CTA mapping, 16-byte vectors: rows need not start on a 16-byte boundary
+    int16_t vec_params = 1;  // gamma (and beta) 16-byte aligned
     int64_t ldx = 0;         // row pitch of x in elements (set to N for contiguous rows)
     int64_t ldy = 0;         // row pitch of y in elements (bytes for an FP8 y)
-    int32_t shift = 0;       // CTA mapping, 16-byte vectors: rows need not start on a 16-byte boundary
-    int32_t vec_params = 1;  // gamma (and beta) 16-byte aligned
+    unsigned int* wait_timeouts = nullptr;  // ring kernels: device counter of waits that gave up
 };
+// Kept at 128 bytes: a larger argument block made ptxas spill the 64-register
+// long-row kernels.
+static_assert(sizeof(NormArgs) == 128, "kernel argument block: 128 bytes");
 
 // Backward pass. A CTA (row_cluster == 1) or a cluster of row_cluster CTAs
 // owns one row at a time; each thread accumulates the column gradients of
@@ -62,6 +66,21 @@ constexpr int kBwdMaxThreads = 512;
 // Record a CUDA error for norm_last_cuda_error() on the calling thread.
 void note_cuda_error(int e);
 
+// CTA size limit of the ring kernels: a thread holds its elements widened to
+// fp32, up to 64 registers of them.
+constexpr int kRingMaxThreads = 512;
+
+// Dynamic shared memory of a ring launch: the stages' 16-byte slots, then
+// one 16-byte slot (the row's first 16 bytes) and one 8-byte mbarrier per
+// stage.
+inline int64_t ring_smem_bytes(int stages, int per_thread, int threads) {
+    return int64_t(stages) * (int64_t(per_thread) * threads * 16 + 16 + 8);
+}
+
+// Device address of the current device's counter of ring-kernel waits that
+// gave up (norm_wait_timeouts reads it); null if it cannot be resolved.
+unsigned int* wait_counter(int dev);
+
 // Partial rows of the column gradients a backward plan produces (one per
 // cluster, or per CTA without clusters).
 inline int64_t bwd_partials(const norm_plan& p) { return p.group > 0 ? p.grid / p.group : 0; }
@@ -74,7 +93,7 @@ cudaError_t launch_ln_bwd_f16(const norm_plan& plan, const BwdArgs& a, cudaStrea
 cudaError_t launch_rms_bwd_f16(const norm_plan& plan, const BwdArgs& a, cudaStream_t s, int dev, int num_sms);
 
 // Launch the kernel variant `plan` names on the current device `dev` (with
-// `num_sms` SMs). The plan has been validated; a pipelined plan with grid 0
+// `num_sms` SMs). The plan has been validated; a ring plan with grid 0
 // gets a persistent grid sized by occupancy.
 cudaError_t launch_ln_f32(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);
 cudaError_t launch_ln_bf16(const norm_plan& plan, const NormArgs& a, cudaStream_t s, int num_sms, int dev);

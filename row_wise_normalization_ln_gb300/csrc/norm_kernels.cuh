@@ -8,8 +8,10 @@
 //   norm_fwd_cta    a CTA, or a thread-block cluster, owns a row; rows longer
 //                   than one pass of the cluster's registers are walked in
 //                   rounds. Also the element-access path for unaligned rows.
-//   norm_fwd_pipe   the CTA mapping on a persistent grid, with the next rows
-//                   of each CTA in flight in a shared-memory ring (cp.async).
+//   norm_fwd_ring   the CTA mapping on a persistent grid: bulk copies bring
+//                   each CTA's share of its next rows into a shared-memory
+//                   ring while it works on the current one, and each thread
+//                   widens its elements to fp32 once.
 //
 // Inside a CTA's slice the layout is warp-major: warp w holds V runs of 32
 // consecutive accesses, access (w*V + j)*32 + lane, so every instruction
@@ -497,10 +499,11 @@ __device__ __forceinline__ int valid_runs(int nacc, int first, int stride_acc, i
 // distributed shared memory. Every thread of every CTA of the cluster
 // returns the same bits.
 //
-// A row makes two such sums for LayerNorm (stage 0, then stage 1) and one
-// for RMSNorm (stage 0). Each stage has its own shared-memory slots and the
-// stages alternate, so a slot is written again only after a barrier that
-// every reader of its previous value has passed.
+// A row makes two such sums for LayerNorm (stage 0, then stage 1), so a
+// slot is written again only after a barrier that every reader of its
+// previous value has passed. RMSNorm makes one, in the stage its caller
+// names: kernels that walk several rows per CTA either alternate the stage
+// from row to row or put a barrier between rows.
 struct RowReduceSmem {
     float warp_part[2][32];  // [stage][warp]
     float cta_part[2];       // [stage], read by cluster peers
@@ -529,10 +532,11 @@ __device__ __forceinline__ float row_sum(RowReduceSmem& red, int stage, float v,
 // of every CTA of the cluster. (Merging each CTA's state first and
 // exchanging one state per CTA, with one cluster barrier per row instead of
 // two, measured slower on GB300.)
+// `stage`: the stage of RMSNorm's one sum (LayerNorm uses both).
 template <bool LN>
 __device__ __forceinline__ void row_stats(RowReduceSmem& red, float n_t, float sum_t, float mean_t, float m2_t,
                                           float ss_t, float invN, float eps, uint32_t C, int nwarps, int wwidth,
-                                          float& mu, float& rs) {
+                                          int stage, float& mu, float& rs) {
     if constexpr (LN) {
         mu = row_sum(red, 0, sum_t, C, nwarps, wwidth) * invN;
         const float d = mean_t - mu;
@@ -540,7 +544,7 @@ __device__ __forceinline__ void row_stats(RowReduceSmem& red, float n_t, float s
         rs = rsqrtf(m2 * invN + eps);
     } else {
         mu = 0.f;
-        rs = rsqrtf(row_sum(red, 0, ss_t, C, nwarps, wwidth) * invN + eps);
+        rs = rsqrtf(row_sum(red, stage, ss_t, C, nwarps, wwidth) * invN + eps);
     }
 }
 
@@ -721,7 +725,7 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
             }
         }
         float mu, rs;
-        row_stats<LN>(red, n_t, sum_t, mean_t, m2_t, ss_t, invN, a.eps, C, nwarps, wwidth, mu, rs);
+        row_stats<LN>(red, n_t, sum_t, mean_t, m2_t, ss_t, invN, a.eps, C, nwarps, wwidth, 0, mu, rs);
         if (LN && rank == 0 && tid == 0) {
             if (a.mean) a.mean[row] = K + mu;
             if (a.rstd) a.rstd[row] = rs;
@@ -772,24 +776,176 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
                 s.template out<Q8>(gb + f * VEC, bb + f * VEC, a.y, yb + f * VEC, stride, nv, mu, rs, inv, sp);
             }
         }
+        // RMSNorm reduces once per row, always in stage 0: before this CTA
+        // (cluster) writes the stage again for its next row, every thread of
+        // it must have read this row's values. (LayerNorm's two stages order
+        // that by themselves.) One-row-per-CTA launches never get here.
+        if constexpr (!LN) {
+            if (row + row_step < a.M) {
+                if (C > 1)
+                    cluster_barrier();
+                else
+                    __syncthreads();
+            }
+        }
     }
     // No CTA may exit while a peer can still read its shared memory.
     if (C > 1) cluster_barrier();
 }
 
-// ================================================================== PIPE
+// ================================================================== RING
+// fp32 pair arithmetic: the packed sm_100-family instructions for 16-bit
+// rows, scalar instructions for fp32 rows (as in the register kernels).
+template <bool PACKED>
+struct PairMath;
+template <>
+struct PairMath<true> {
+    static __device__ __forceinline__ float2 add(float2 a, float2 b) { return __fadd2_rn(a, b); }
+    static __device__ __forceinline__ float2 mul(float2 a, float2 b) { return __fmul2_rn(a, b); }
+    static __device__ __forceinline__ float2 fma(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+};
+template <>
+struct PairMath<false> {
+    static __device__ __forceinline__ float2 add(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
+    static __device__ __forceinline__ float2 mul(float2 a, float2 b) { return make_float2(a.x * b.x, a.y * b.y); }
+    static __device__ __forceinline__ float2 fma(float2 a, float2 b, float2 c) {
+        return make_float2(fmaf(a.x, b.x, c.x), fmaf(a.y, b.y, c.y));
+    }
+};
+
+// Element pair i of a 16-byte access, widened exactly to fp32, and the
+// reverse (nearest-even rounding to T).
+template <class T>
+struct PairCodec {
+    using P = typename std::conditional<std::is_same<T, __half>::value, F16Pair, Bf16Pair>::type;
+    static __device__ __forceinline__ float2 get(const uint4& r, int i) {
+        if constexpr (sizeof(T) == 4)
+            return i == 0 ? make_float2(__uint_as_float(r.x), __uint_as_float(r.y))
+                          : make_float2(__uint_as_float(r.z), __uint_as_float(r.w));
+        else
+            return P::widen(i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w);
+    }
+    static __device__ __forceinline__ uint4 put(const float2* v) {
+        if constexpr (sizeof(T) == 4)
+            return make_uint4(__float_as_uint(v[0].x), __float_as_uint(v[0].y), __float_as_uint(v[1].x),
+                              __float_as_uint(v[1].y));
+        else
+            return make_uint4(P::pack(v[0].x, v[0].y), P::pack(v[1].x, v[1].y), P::pack(v[2].x, v[2].y),
+                              P::pack(v[3].x, v[3].y));
+    }
+    // The first element of a 16-byte access.
+    static __device__ __forceinline__ float first(const uint4& r) { return get(r, 0).x; }
+};
+
+// A thread's V accesses of one row, widened once to fp32 pairs and kept in
+// registers: x - K for LayerNorm, x for RMSNorm. The first `nvalid` lie
+// inside the row. Every value is the one the register kernels form at each
+// use (x - K is rounded the same way), so the two statistics passes and the
+// output step read them without widening again.
+template <class T, int V, bool LN>
+struct WideSlice {
+    static constexpr int VEC = ElemVec<T>::value;
+    static constexpr int NP = VEC / 2;  // fp32 pairs per access
+    using PM = PairMath<sizeof(T) == 2>;
+    using PC = PairCodec<T>;
+    float2 d[V][NP];
+
+    __device__ __forceinline__ void set(int j, const uint4& r, float2 nk) {
+#pragma unroll
+        for (int i = 0; i < NP; ++i) d[j][i] = LN ? PM::add(PC::get(r, i), nk) : PC::get(r, i);
+    }
+    // Welford state of the valid elements ([Ch7] §7.4): the sum and mean of
+    // x - K, then M2 about that mean, two passes over the registers.
+    __device__ __forceinline__ void welford(int nvalid, float inv_n, float& sum, float& mean, float& m2) const {
+        float2 s0 = make_float2(0.f, 0.f), s1 = s0;
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            if (j < nvalid) {
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    if (i & 1)
+                        s1 = PM::add(s1, d[j][i]);
+                    else
+                        s0 = PM::add(s0, d[j][i]);
+                }
+            }
+        const float2 s = PM::add(s0, s1);
+        sum = s.x + s.y;
+        mean = sum * inv_n;
+        const float2 nm = f2_splat(-mean);
+        float2 q0 = make_float2(0.f, 0.f), q1 = q0;
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            if (j < nvalid) {
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    const float2 e = PM::add(d[j][i], nm);
+                    if (i & 1)
+                        q1 = PM::fma(e, e, q1);
+                    else
+                        q0 = PM::fma(e, e, q0);
+                }
+            }
+        const float2 q = PM::add(q0, q1);
+        m2 = q.x + q.y;
+    }
+    // Sum of squares of the valid elements (RMSNorm, [Ch7] §7.5.1).
+    __device__ __forceinline__ float sumsq(int nvalid) const {
+        float2 q0 = make_float2(0.f, 0.f), q1 = q0;
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            if (j < nvalid) {
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    if (i & 1)
+                        q1 = PM::fma(d[j][i], d[j][i], q1);
+                    else
+                        q0 = PM::fma(d[j][i], d[j][i], q0);
+                }
+            }
+        const float2 q = PM::add(q0, q1);
+        return q.x + q.y;
+    }
+    // y = ((x - K) * rstd - mu * rstd) * gamma + beta (LayerNorm) or
+    // (x * w) * rstd (RMSNorm), rounded to T and stored; `g`, `b` and `y`
+    // point at this thread's first access, `stride` elements apart.
+    __device__ __forceinline__ void emit(const T* g, const T* b, T* y, int stride, int nvalid, float mu,
+                                         float rs) const {
+        const float2 rs2 = f2_splat(rs), nm2 = f2_splat(-mu * rs);
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            if (j < nvalid) {
+                const uint4 gr = __ldg(reinterpret_cast<const uint4*>(g + j * stride));
+                uint4 br = make_uint4(0u, 0u, 0u, 0u);
+                if constexpr (LN) br = __ldg(reinterpret_cast<const uint4*>(b + j * stride));
+                float2 o[NP];
+#pragma unroll
+                for (int i = 0; i < NP; ++i)
+                    o[i] = LN ? PM::fma(PM::fma(d[j][i], rs2, nm2), PC::get(gr, i), PC::get(br, i))
+                              : PM::mul(PM::mul(d[j][i], PC::get(gr, i)), rs2);
+                *reinterpret_cast<uint4*>(y + j * stride) = PC::put(o);
+            }
+    }
+};
+
 // The CTA mapping (one CTA or cluster per row, one round) on a persistent
-// grid, with the next S-1 rows of this CTA in flight while it works on the
-// current one: each thread copies its own 16-byte slots of upcoming rows
-// into a ring of S shared-memory stages with cp.async, and reads a stage
-// only after its own copies into it have landed. The bytes in flight live in
-// shared memory, not registers, so HBM stays busy through the reduction and
-// the stores. Needs 16-byte aligned rows of whole vectors.
+// grid. A CTA's share of a row is one contiguous run of V*T accesses (the
+// warp-major layout), so thread 0 moves it into shared memory with a
+// single bulk copy, counted on the stage's mbarrier; a ring of `stages`
+// such stages keeps this CTA's next rows in flight while it reduces and
+// stores the current one. Each thread widens its accesses from its stage
+// once (WideSlice) and works from registers. A stage is refilled, with the
+// row `stages` steps ahead, right after the current row's statistics: the
+// barriers of that reduction come after every thread's reads of the stage.
+// LayerNorm's shift K (the row's first element) arrives with each stage in
+// a 16-byte slot of its own, so every CTA of a cluster has it. Needs
+// 16-byte aligned rows of whole vectors.
 template <class T, int V, bool LN, bool CL>
-__global__ void __launch_bounds__(1024) norm_fwd_pipe(const NormArgs a) {
+__global__ void __launch_bounds__(kRingMaxThreads) norm_fwd_ring(const NormArgs a) {
     constexpr int VEC = ElemVec<T>::value;
-    using S = Slice<T, VEC, V, LN>;
-    extern __shared__ uint4 ring[];  // [stages][V*T] 16-byte slots, then [stages][32] words for K
+    using S = WideSlice<T, V, LN>;
+    // [stages][V*T] 16-byte slots | [stages] first 16 bytes of the row | [stages] mbarriers
+    extern __shared__ __align__(128) uint4 ring[];
     __shared__ RowReduceSmem red;
 
     const int stages = a.stages;
@@ -806,67 +962,89 @@ __global__ void __launch_bounds__(1024) norm_fwd_pipe(const NormArgs a) {
     const int64_t row_step = gridDim.x / C;
     const int nacc = a.N / VEC;
     const int stride = 32 * VEC;
+    const int stage_slots = V * T_;
+    const int cbase = rank * stage_slots;  // this CTA's first access of every row
+    const int cslots = max(0, min(stage_slots, nacc - cbase));
+    const uint32_t cbytes = static_cast<uint32_t>(cslots) * 16u;
+    const uint32_t tx = cbytes + (LN ? 16u : 0u);
     const int in_slice = warp * V * 32 + lane;
-    const int first = rank * V * T_ + in_slice;  // this thread's first access of every row
-    const int nvalid = valid_runs(nacc, first, 32, V);
+    const int nvalid = valid_runs(cslots, in_slice, 32, V);
     const float n_t = static_cast<float>(nvalid * VEC);
     const float inv_n = nvalid > 0 ? 1.f / n_t : 0.f;
     const float invN = 1.f / static_cast<float>(a.N);
-    const int stage_slots = V * T_;
-    float* kslot = reinterpret_cast<float*>(ring + stages * stage_slots);
-    const T* g = static_cast<const T*>(a.gamma) + first * VEC;
-    const T* b = static_cast<const T*>(a.beta) + first * VEC;
+    uint4* kslot = ring + stages * stage_slots;
+    uint64_t* full = reinterpret_cast<uint64_t*>(kslot + stages);
+    const T* x = static_cast<const T*>(a.x);
+    const int64_t col = static_cast<int64_t>(cbase + in_slice) * VEC;  // this thread's first element
+    const T* g = static_cast<const T*>(a.gamma) + col;
+    const T* b = static_cast<const T*>(a.beta) + col;
 
-    // Copy this thread's slots of `row` into stage `st`, and for LayerNorm
-    // the row's first element (lane 0 of each warp; 4 bytes at the 16-byte
-    // aligned row start). Always commits one group, so groups and rows stay
-    // in step.
-    auto issue = [&](int64_t row, int st) {
-        if (row < a.M) {
-            const T* src = static_cast<const T*>(a.x) + row * a.ldx + first * VEC;
-            uint4* dst = ring + st * stage_slots + in_slice;
-#pragma unroll
-            for (int j = 0; j < V; ++j)
-                if (j < nvalid) cp_async16(dst + j * 32, src + j * stride);
-            if (LN && lane == 0) cp_async4(&kslot[st * 32 + warp], static_cast<const T*>(a.x) + row * a.ldx);
-        }
-        cp_async_commit();
-    };
-
+    if (tid == 0) {
+        for (int k = 0; k < stages; ++k) mbar_init(&full[k], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
     grid_release();
     grid_wait();
-    for (int k = 0; k < stages - 1; ++k) issue(first_row + k * row_step, k);
-    int st = 0;
-    for (int64_t row = first_row; row < a.M; row += row_step) {
-        issue(row + (stages - 1) * row_step, st == 0 ? stages - 1 : st - 1);
-        cp_async_wait(stages - 1);  // this thread's copies of `row` have landed
 
-        S s;
+    // Thread 0: fill stage `st` with this CTA's share of `row`.
+    auto issue = [&](int64_t row, int st) {
+        const T* xr = x + row * a.ldx;
+        mbar_arrive_expect(&full[st], tx);
+        if (cbytes) bulk_load(ring + st * stage_slots, xr + cbase * VEC, cbytes, &full[st]);
+        if (LN) bulk_load(kslot + st, xr, 16u, &full[st]);
+    };
+    if (tid == 0)
+        for (int k = 0; k < stages; ++k)
+            if (first_row + k * row_step < a.M) issue(first_row + k * row_step, k);
+
+    int st = 0;
+    uint32_t parity = 0;
+    int64_t k = 0;        // rows of this CTA done so far
+    int64_t late = -1;    // the row whose wait ran out, if any
+    for (int64_t row = first_row; row < a.M; row += row_step, ++k) {
+        // After one wait has run out this CTA neither waits nor copies any
+        // more (its outputs are void by then), so the kernel still ends in
+        // bounded time.
+        if (late < 0 && !mbar_wait(&full[st], parity)) late = k;
         float K = 0.f;
-        if constexpr (LN) {
-            const float kw = __shfl_sync(kFullMask, lane == 0 ? kslot[st * 32 + warp] : 0.f, 0);
-            K = sizeof(T) == 4 ? kw : __uint_as_float(__float_as_uint(kw) << 16);
-        }
-        s.set_shift(K);
+        if constexpr (LN) K = PairCodec<T>::first(kslot[st]);
+        S s;
         const uint4* src = ring + st * stage_slots + in_slice;
+        const float2 nk = f2_splat(-K);
 #pragma unroll
         for (int j = 0; j < V; ++j)
-            if (j < nvalid) s.set(j, src[j * 32]);
+            if (j < nvalid) s.set(j, src[j * 32], nk);
         float sum = 0.f, mean = 0.f, m2 = 0.f, ss = 0.f;
         if constexpr (LN)
             s.welford(nvalid, inv_n, sum, mean, m2);
         else
             ss = s.sumsq(nvalid);
         float mu, rs;
-        row_stats<LN>(red, n_t, sum, mean, m2, ss, invN, a.eps, C, nwarps, wwidth, mu, rs);
+        row_stats<LN>(red, n_t, sum, mean, m2, ss, invN, a.eps, C, nwarps, wwidth, static_cast<int>(k & 1), mu, rs);
         if (LN && rank == 0 && tid == 0) {
             if (a.mean) a.mean[row] = K + mu;
             if (a.rstd) a.rstd[row] = rs;
         }
-        s.emit(g, b, static_cast<T*>(a.y) + row * a.ldy + first * VEC, stride, nvalid, mu, rs);
-        st = st + 1 == stages ? 0 : st + 1;
+        if (tid == 0 && late < 0) {
+            const int64_t next = row + stages * row_step;
+            if (next < a.M) {
+                fence_proxy_async();
+                issue(next, st);
+            }
+        }
+        s.emit(g, b, static_cast<T*>(a.y) + row * a.ldy + col, stride, nvalid, mu, rs);
+        if (++st == stages) st = 0, parity ^= 1u;
     }
-    cp_async_wait(0);  // nothing of ours may land after exit
+    if (late >= 0 && tid == 0) {
+        // Copies still in flight (rows late .. late+stages-1 of this CTA)
+        // get one more bounded wait each, so that none lands after this CTA
+        // has gone; then tell the host.
+        for (int64_t kk = late; kk < late + stages; ++kk)
+            if (first_row + kk * row_step < a.M)
+                mbar_wait(&full[kk % stages], static_cast<uint32_t>((kk / stages) & 1));
+        atomicAdd(a.wait_timeouts, 1u);
+    }
     // No CTA may exit while a peer can still read its shared memory.
     if (C > 1) cluster_barrier();
 }
@@ -899,27 +1077,22 @@ KernelFn<T, LN> pick_kernel(int mapping, int per_thread, bool cl, bool shift) {
 }
 
 template <class T, bool LN, int V>
-KernelFn<T, LN> pick_pipe_v(bool cl) {
-    return cl ? norm_fwd_pipe<T, V, LN, true> : norm_fwd_pipe<T, V, LN, false>;
+KernelFn<T, LN> pick_ring_v(bool cl) {
+    return cl ? norm_fwd_ring<T, V, LN, true> : norm_fwd_ring<T, V, LN, false>;
 }
 
 template <class T, bool LN>
-KernelFn<T, LN> pick_pipe(int per_thread, bool cl) {
+KernelFn<T, LN> pick_ring(int per_thread, bool cl) {
     switch (per_thread) {
-        case 1: return pick_pipe_v<T, LN, 1>(cl);
-        case 2: return pick_pipe_v<T, LN, 2>(cl);
-        case 4: return pick_pipe_v<T, LN, 4>(cl);
-        case 8: return pick_pipe_v<T, LN, 8>(cl);
+        case 1: return pick_ring_v<T, LN, 1>(cl);
+        case 2: return pick_ring_v<T, LN, 2>(cl);
+        case 4: return pick_ring_v<T, LN, 4>(cl);
+        case 8: return pick_ring_v<T, LN, 8>(cl);
         default: return nullptr;
     }
 }
 
-// Bytes of dynamic shared memory a pipelined launch needs.
-inline size_t pipe_smem_bytes(const norm_plan& p, bool ln) {
-    return static_cast<size_t>(p.stages) * p.per_thread * p.threads * 16 + (ln ? p.stages * 32 * 4 : 0);
-}
-
-// Opt a pipelined kernel in to the device's largest dynamic shared memory
+// Opt a ring kernel in to the device's largest dynamic shared memory
 // per block (once per kernel and device; the call is not a stream operation).
 template <class T, int V, bool LN, bool CL>
 cudaError_t opt_in_smem(int dev) {
@@ -930,9 +1103,9 @@ cudaError_t opt_in_smem(int dev) {
     cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, norm_fwd_pipe<T, V, LN, CL>);
+    e = cudaFuncGetAttributes(&fa, norm_fwd_ring<T, V, LN, CL>);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(norm_fwd_pipe<T, V, LN, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(norm_fwd_ring<T, V, LN, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              optin - static_cast<int>(fa.sharedSizeBytes));
     if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_relaxed);
     return e;
@@ -965,9 +1138,9 @@ cudaError_t launch_norm(const norm_plan& p, const NormArgs& a, cudaStream_t stre
         if constexpr (ADD || Q8) {
             return cudaErrorInvalidValue;
         } else {
-            k = pick_pipe<T, LN>(p.per_thread, cl);
+            k = pick_ring<T, LN>(p.per_thread, cl);
             if (k == nullptr) return cudaErrorInvalidValue;
-            smem = pipe_smem_bytes(p, LN);
+            smem = ring_smem_bytes(p.stages, p.per_thread, p.threads);
             const cudaError_t e = allow_smem<T, LN>(p.per_thread, cl, dev);
             if (e != cudaSuccess) return e;
         }
@@ -993,6 +1166,11 @@ cudaError_t launch_norm(const norm_plan& p, const NormArgs& a, cudaStream_t stre
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
+    NormArgs args = a;
+    if (p.stages > 0) {
+        args.wait_timeouts = wait_counter(dev);
+        if (args.wait_timeouts == nullptr) return cudaErrorInvalidSymbol;
+    }
     if (p.stages > 0 && p.grid == 0) {
         // Persistent grid: as many CTAs (whole clusters) as can be resident at
         // once, so that no row waits for a CTA that never finishes early.
@@ -1012,7 +1190,7 @@ cudaError_t launch_norm(const norm_plan& p, const NormArgs& a, cudaStream_t stre
         if (clusters < 1) return cudaErrorInvalidConfiguration;
         cfg.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(a.M, clusters) * p.cluster), 1, 1);
     }
-    return cudaLaunchKernelEx(&cfg, k, a);
+    return cudaLaunchKernelEx(&cfg, k, args);
 }
 
 }  // namespace libnorm

@@ -36,7 +36,7 @@ def test_header_declares_the_abi():
         "ln_bwd_noalloc",
         "ln_fwd_fp8", "rms_fwd_fp8", "ln_fwd_add_fp8", "rms_fwd_add_fp8", "ln_fwd_fp8_planned", "rms_fwd_fp8_planned",
         "ln_fwd_strided", "rms_fwd_strided",
-        "norm_status_string", "norm_last_cuda_error", "norm_abi_version"}
+        "norm_status_string", "norm_last_cuda_error", "norm_abi_version", "norm_wait_timeouts"}
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -78,6 +78,11 @@ def test_null_pointers_rejected(lib):
         assert lib.ln_fwd(*args, None, None, 4, 8, 1e-5, rn.NORM_F32, None) == rn.NORM_ERR_ARG
     for args in [(None, P, P), (P, None, P), (P, P, None)]:
         assert lib.rms_fwd(*args, 4, 8, 1e-6, rn.NORM_F32, None) == rn.NORM_ERR_ARG
+
+
+def test_wait_timeouts_needs_a_destination(lib):
+    # checked before any CUDA call
+    assert lib.norm_wait_timeouts(None) == rn.NORM_ERR_ARG
 
 
 def test_zero_rows_is_a_noop(lib):
@@ -164,8 +169,10 @@ def _plan(**kw):
     dict(stages=3, vec_elems=1),                # the ring needs 16-byte vectors
     dict(stages=3, threads=64, per_thread=1),   # 64*1*4 < N: two rounds, not allowed with a ring
     dict(stages=4, threads=1024, per_thread=8, grid=0),  # 4*1024*8*16 B of ring > 225 KB
+    dict(stages=2, threads=1024, per_thread=1, grid=0),  # ring CTAs hold at most 512 threads
     dict(mapping=rn.NORM_MAP_GROUP, group=32, per_thread=8, stages=2),
     dict(grid=0),                               # grid 0 only for ring plans
+    dict(mapping=3),
 ])
 def test_bad_plans_rejected(lib, kw):
     p = _plan(**kw)
@@ -246,7 +253,7 @@ def test_plans_are_consistent(lib, dtype, aligned, M):
             assert p["cluster"] in (1, 2, 4, 8)
             if p["stages"]:
                 assert p["grid"] == 0 and p["rounds"] == 1 and p["vec_elems"] > 1
-                assert p["stages"] * p["threads"] * p["per_thread"] * 16 + p["stages"] * 128 <= 225 * 1024
+                assert p["stages"] * (p["threads"] * p["per_thread"] * 16 + 24) <= 225 * 1024 and p["threads"] <= 512
             else:
                 assert p["grid"] % p["cluster"] == 0 and p["grid"] == M * p["cluster"]
 

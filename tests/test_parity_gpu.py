@@ -11,7 +11,7 @@ from parity import check_ln, check_rms, np_of, sample_rows
 
 pytestmark = pytest.mark.gpu
 
-DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -163,7 +163,7 @@ def _variants():
                                                     group=0, threads=T, cluster=C, grid=C * 3), N))
                         # the shared-memory ring (vector rows, one round)
                         for S in (2, 3, 4):
-                            if not v or S * T * per * 16 + S * 128 > 225 * 1024 or cap > 300000:
+                            if not v or T > 512 or S * (T * per * 16 + 24) > 225 * 1024 or cap > 300000:
                                 continue
                             for N, grid in ((cap, C * 2), (max(ve, cap - 3 * ve), 0)):
                                 out.append((dtype, dict(mapping=rn.NORM_MAP_CTA, vec_elems=ve, per_thread=per,
@@ -189,6 +189,37 @@ def test_every_variant(dtype, plan, N):
     check_ln(x, g, b, 1e-5, y, mean, rstd)
     y = run_rms(x, g, 1e-6, plan=plan)
     check_rms(x, g, 1e-6, y)
+    if plan.get("stages"):
+        assert rn.wait_timeouts() == 0
+
+
+RING = [(dt, T, per, C, S, N)
+        for dt, vec in (("f32", 4), ("bf16", 8), ("f16", 8))
+        for (T, per, C, S, N) in ((128, 8, 1, 2, 128 * 8 * vec), (256, 4, 1, 3, 256 * 4 * vec - 5 * vec),
+                                  (512, 4, 8, 2, 8 * 512 * 4 * vec), (64, 2, 2, 4, 2 * 64 * 2 * vec - vec),
+                                  (32, 1, 1, 4, 32 * vec))]
+
+
+@pytest.mark.parametrize("dtype,T,per,C,S,N", RING, ids=[f"{r[0]}-t{r[1]}-p{r[2]}-c{r[3]}-s{r[4]}-N{r[5]}" for r in RING])
+def test_ring_many_rows(dtype, T, per, C, S, N):
+    """The ring kernels on a persistent grid (grid 0: as many CTAs as fit)
+    over many more rows than CTAs, so every stage is refilled many times;
+    also in place (y written over x). No wait may run out."""
+    vec = 4 if dtype == "f32" else 8
+    plan = dict(mapping=rn.NORM_MAP_CTA, vec_elems=vec, per_thread=per, group=0, threads=T, cluster=C, stages=S,
+                grid=0)
+    M = 3000 if N <= 8192 else 400
+    x, g, b = _rand(M, N, DT[dtype], seed=N + T + S, loc=3.0, scale=1.5)
+    y, mean, rstd = run_ln(x, g, b, 1e-5, plan=plan)
+    check_ln(x, g, b, 1e-5, y, mean, rstd)
+    y = run_rms(x, g, 1e-6, plan=plan)
+    check_rms(x, g, 1e-6, y)
+    xd = x.cuda()
+    y2, _, _ = rn.ln_fwd(xd, g.cuda(), b.cuda(), 1e-5, out=xd, plan=plan)
+    torch.cuda.synchronize()
+    assert y2.data_ptr() == xd.data_ptr()
+    check_ln(x, g, b, 1e-5, xd.cpu(), mean, rstd)
+    assert rn.wait_timeouts() == 0
 
 
 # ------------------------------------------------------------ layouts
