@@ -39,6 +39,9 @@
 
 #include <algorithm>
 #include <atomic>
+#include <map>
+#include <mutex>
+#include <tuple>
 #include <type_traits>
 
 #include "norm_args.h"
@@ -622,12 +625,36 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_group(
 // store h as soon as it is formed and the output pass re-reads h, not x and
 // r. Every thread re-reads only its own accesses, so h (and y) may be the x
 // or r buffer itself.
+// Bulk L2 prefetch of row `row` of x, `slots` 16-byte accesses from the
+// start of its vector body (the first 16-byte aligned element), clipped to
+// the row's whole vectors: no register is written and nothing waits for it.
+template <class T, int VEC, bool SHIFT>
+__device__ __forceinline__ void prefetch_row_body(const NormArgs& a, int64_t row, int slots) {
+    const T* xr = static_cast<const T*>(a.x) + row * a.ldx;
+    int h0 = 0;
+    if constexpr (SHIFT) {
+        const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(xr)) & 15u;
+        h0 = min(static_cast<int>(((16u - mis) & 15u) / sizeof(T)), a.N);
+    }
+    const int n = min(slots, (a.N - h0) / VEC);
+    if (n > 0) prefetch_l2_bulk(xr + h0, static_cast<uint32_t>(n) * 16u);
+}
+
 template <class T, int VEC, int V, bool LN, bool CL, bool ADD, bool Q8, bool SHIFT>
 __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(const NormArgs a) {
     using S = Slice<T, VEC, V, LN>;
     using SO = ScalarOps<T>;
     __shared__ RowReduceSmem red;
 
+    if constexpr (!CL && !ADD && VEC > 1) {
+        // One CTA per row: warm L2 with the row a.group rows after this
+        // CTA's first (set at launch; 0 for none), which a CTA about to
+        // start will read. Only moves data towards L2, so it may run before
+        // the previous grid has finished; L2 is where its writes land.
+        const int64_t ahead = static_cast<int64_t>(blockIdx.x) + a.group;
+        if (threadIdx.x == 0 && a.group > 0 && ahead < a.M)
+            prefetch_row_body<T, VEC, SHIFT>(a, ahead, V * static_cast<int>(blockDim.x) * a.rounds);
+    }
     const int T_ = blockDim.x;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -1127,6 +1154,34 @@ cudaError_t allow_smem(int per_thread, bool cl, int dev) {
     }
 }
 
+// CTAs of kernel `k` with `threads` threads (no dynamic shared memory) that
+// fit on device `dev` at once; queried once per kernel, size and device.
+inline cudaError_t resident_ctas(const void* k, int threads, int dev, int num_sms, int64_t* out) {
+    struct Key {
+        const void* fn;
+        int threads, dev;
+        bool operator<(const Key& o) const { return std::tie(fn, threads, dev) < std::tie(o.fn, o.threads, o.dev); }
+    };
+    static std::mutex mu;
+    static std::map<Key, int64_t> cache;
+    const Key key{k, threads, dev};
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) {
+        *out = it->second;
+        return cudaSuccess;
+    }
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, threads, 0);
+    if (e != cudaSuccess) return e;
+    cache[key] = int64_t(n) * num_sms;
+    *out = cache[key];
+    return cudaSuccess;
+}
+
+// Rows at least this long (bytes of x) get the next-row L2 prefetch.
+constexpr int64_t kPrefetchMinRowBytes = 8192;
+
 // ADD: the fused residual add; Q8: FP8 E4M3 output (register kernels only;
 // no ring).
 template <class T, bool LN, bool ADD, bool Q8 = false>
@@ -1167,6 +1222,18 @@ cudaError_t launch_norm(const norm_plan& p, const NormArgs& a, cudaStream_t stre
         cfg.numAttrs = 2;
     }
     NormArgs args = a;
+    if (!ADD && p.mapping == NORM_MAP_CTA && p.cluster == 1 && p.stages == 0 && p.vec_elems > 1 &&
+        int64_t(a.N) * int64_t(sizeof(T)) >= kPrefetchMinRowBytes) {
+        // One CTA per row, long rows: each CTA prefetches into L2 the row
+        // 3/8 of the resident CTAs ahead, just past the rows in flight
+        // (measured on GB300: 1/4 to 1/2 of the resident CTAs ahead all
+        // gain 2-3 %; a whole resident set ahead loses, and clusters lose
+        // at any distance).
+        int64_t resident = 0;
+        const cudaError_t e = resident_ctas(reinterpret_cast<const void*>(k), p.threads, dev, num_sms, &resident);
+        if (e != cudaSuccess) return e;
+        args.group = static_cast<int32_t>(std::min<int64_t>(resident * 3 / 8, a.M));
+    }
     if (p.stages > 0) {
         args.wait_timeouts = wait_counter(dev);
         if (args.wait_timeouts == nullptr) return cudaErrorInvalidSymbol;
