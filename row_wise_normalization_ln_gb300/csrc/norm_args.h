@@ -27,7 +27,7 @@ struct NormArgs {
     int64_t M;
     int32_t N;
     float eps;
-    int32_t group;      // GROUP mapping: lanes per row; CTA mapping: rows ahead to prefetch into L2 (0: none)
+    int32_t group;      // GROUP mapping: lanes per row; CTA mapping: L2 prefetch of the row group-1 ahead (0: none)
     int32_t rounds;     // CTA mapping: register-sized rounds per row
     int32_t stages;     // ring CTA mapping: shared-memory stages
     int16_t shift = 0;       // CTA mapping, 16-byte vectors: rows need not start on a 16-byte boundary

@@ -625,19 +625,25 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_group(
 // store h as soon as it is formed and the output pass re-reads h, not x and
 // r. Every thread re-reads only its own accesses, so h (and y) may be the x
 // or r buffer itself.
-// Bulk L2 prefetch of row `row` of x, `slots` 16-byte accesses from the
-// start of its vector body (the first 16-byte aligned element), clipped to
-// the row's whole vectors: no register is written and nothing waits for it.
+// Bulk L2 prefetch of the share of row `row` of x that CTA `rank` of a row's
+// `C` CTAs reads: per round, `slots` 16-byte accesses at (round*C + rank) *
+// slots from the start of the row's vector body (its first 16-byte aligned
+// element), clipped to the row's whole vectors. No register is written and
+// nothing waits for it.
 template <class T, int VEC, bool SHIFT>
-__device__ __forceinline__ void prefetch_row_body(const NormArgs& a, int64_t row, int slots) {
+__device__ __forceinline__ void prefetch_row_share(const NormArgs& a, int64_t row, int rank, int C, int slots) {
     const T* xr = static_cast<const T*>(a.x) + row * a.ldx;
     int h0 = 0;
     if constexpr (SHIFT) {
         const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(xr)) & 15u;
         h0 = min(static_cast<int>(((16u - mis) & 15u) / sizeof(T)), a.N);
     }
-    const int n = min(slots, (a.N - h0) / VEC);
-    if (n > 0) prefetch_l2_bulk(xr + h0, static_cast<uint32_t>(n) * 16u);
+    const int nb = (a.N - h0) / VEC;
+    for (int r = 0; r < a.rounds; ++r) {
+        const int f0 = (r * C + rank) * slots;
+        const int n = min(slots, nb - f0);
+        if (n > 0) prefetch_l2_bulk(xr + h0 + static_cast<int64_t>(f0) * VEC, static_cast<uint32_t>(n) * 16u);
+    }
 }
 
 template <class T, int VEC, int V, bool LN, bool CL, bool ADD, bool Q8, bool SHIFT>
@@ -646,14 +652,19 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
     using SO = ScalarOps<T>;
     __shared__ RowReduceSmem red;
 
-    if constexpr (!CL && !ADD && VEC > 1) {
-        // One CTA per row: warm L2 with the row a.group rows after this
-        // CTA's first (set at launch; 0 for none), which a CTA about to
-        // start will read. Only moves data towards L2, so it may run before
-        // the previous grid has finished; L2 is where its writes land.
-        const int64_t ahead = static_cast<int64_t>(blockIdx.x) + a.group;
-        if (threadIdx.x == 0 && a.group > 0 && ahead < a.M)
-            prefetch_row_body<T, VEC, SHIFT>(a, ahead, V * static_cast<int>(blockDim.x) * a.rounds);
+    if constexpr (!ADD && VEC > 1) {
+        // L2 prefetch of this CTA's share of the row a.group - 1 rows after
+        // its first (a.group set at launch; 0: none): one CTA per row
+        // prefetches a row that a CTA about to start will read, a cluster
+        // its own row. It only moves data towards L2, so it runs before the
+        // previous grid has finished (L2 is where that grid's writes land).
+        if (threadIdx.x == 0 && a.group > 0) {
+            const uint32_t cn = CL ? cluster_size() : 1u;
+            const int64_t target = static_cast<int64_t>(blockIdx.x / cn) + (a.group - 1);
+            if (target < a.M)
+                prefetch_row_share<T, VEC, SHIFT>(a, target, CL ? static_cast<int>(cluster_rank()) : 0,
+                                                  static_cast<int>(cn), V * static_cast<int>(blockDim.x));
+        }
     }
     const int T_ = blockDim.x;
     const int tid = threadIdx.x;
@@ -1222,17 +1233,22 @@ cudaError_t launch_norm(const norm_plan& p, const NormArgs& a, cudaStream_t stre
         cfg.numAttrs = 2;
     }
     NormArgs args = a;
-    if (!ADD && p.mapping == NORM_MAP_CTA && p.cluster == 1 && p.stages == 0 && p.vec_elems > 1 &&
+    if (!ADD && p.mapping == NORM_MAP_CTA && p.stages == 0 && p.vec_elems > 1 &&
         int64_t(a.N) * int64_t(sizeof(T)) >= kPrefetchMinRowBytes) {
-        // One CTA per row, long rows: each CTA prefetches into L2 the row
+        // L2 prefetch (args.group = rows ahead + 1). One CTA per row: the row
         // 3/8 of the resident CTAs ahead, just past the rows in flight
-        // (measured on GB300: 1/4 to 1/2 of the resident CTAs ahead all
-        // gain 2-3 %; a whole resident set ahead loses, and clusters lose
-        // at any distance).
-        int64_t resident = 0;
-        const cudaError_t e = resident_ctas(reinterpret_cast<const void*>(k), p.threads, dev, num_sms, &resident);
-        if (e != cudaSuccess) return e;
-        args.group = static_cast<int32_t>(std::min<int64_t>(resident * 3 / 8, a.M));
+        // (measured on GB300: 1/4 to 1/2 ahead gain 2-14 %, a whole resident
+        // set ahead loses). A cluster per row: its own row (a row ahead loses
+        // at any distance; its own row gains 2.6 % on 65536-wide rows). The
+        // fused add measured slower with it and has none.
+        if (p.cluster > 1) {
+            args.group = 1;
+        } else {
+            int64_t resident = 0;
+            const cudaError_t e = resident_ctas(reinterpret_cast<const void*>(k), p.threads, dev, num_sms, &resident);
+            if (e != cudaSuccess) return e;
+            args.group = static_cast<int32_t>(std::min<int64_t>(resident * 3 / 8, a.M) + 1);
+        }
     }
     if (p.stages > 0) {
         args.wait_timeouts = wait_counter(dev);
