@@ -193,6 +193,33 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
                     *d = 0.f;
             }
 
+    // Rows ahead go to L2 by bulk prefetch: this CTA's contiguous slice of x
+    // and dy (16-byte vector rows only) and the row's statistics, issued by
+    // one thread, two rows ahead of the row being worked on.
+    const int64_t cta_first = static_cast<int64_t>(rank) * V * T_ * VEC;  // first element of the CTA's slice
+    const uint32_t slice_bytes = static_cast<uint32_t>(
+        (cta_first < N ? min(static_cast<int64_t>(V) * T_ * VEC, N - cta_first) : 0) * sizeof(T));
+    auto prefetch_row = [&](int64_t r) {
+        if (r >= a.M) return;
+        if constexpr (VEC > 1) {
+            if (slice_bytes > 0) {
+                prefetch_l2_bulk(static_cast<const T*>(a.x) + r * N + cta_first, slice_bytes);
+                prefetch_l2_bulk(static_cast<const T*>(a.dy) + r * N + cta_first, slice_bytes);
+            }
+        }
+        if constexpr (LN) {
+            prefetch_l2_line(a.mean + r);
+            prefetch_l2_line(a.rstd + r);
+        }
+    };
+    // The first two rows are requested before the dependent-launch wait,
+    // overlapping the previous grid's tail (a prefetch only moves data
+    // towards L2, where that grid's writes land).
+    if (tid == 0) {
+        prefetch_row(first_row);
+        prefetch_row(first_row + row_step);
+    }
+
     grid_release();
     grid_wait();
 
@@ -216,29 +243,6 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
     }
     const T* xbase = static_cast<const T*>(a.x) + f0 * VEC;
     const T* dybase = static_cast<const T*>(a.dy) + f0 * VEC;
-    // Rows ahead go to L2 by bulk prefetch: this CTA's contiguous slice of x
-    // and dy (16-byte vector rows only) and the row's statistics, issued by
-    // one thread, two rows ahead of the row being worked on.
-    const int64_t cta_first = static_cast<int64_t>(rank) * V * T_ * VEC;  // first element of the CTA's slice
-    const uint32_t slice_bytes = static_cast<uint32_t>(
-        (cta_first < N ? min(static_cast<int64_t>(V) * T_ * VEC, N - cta_first) : 0) * sizeof(T));
-    auto prefetch_row = [&](int64_t r) {
-        if (r >= a.M) return;
-        if constexpr (VEC > 1) {
-            if (slice_bytes > 0) {
-                prefetch_l2_bulk(static_cast<const T*>(a.x) + r * N + cta_first, slice_bytes);
-                prefetch_l2_bulk(static_cast<const T*>(a.dy) + r * N + cta_first, slice_bytes);
-            }
-        }
-        if constexpr (LN) {
-            prefetch_l2_line(a.mean + r);
-            prefetch_l2_line(a.rstd + r);
-        }
-    };
-    if (tid == 0) {
-        prefetch_row(first_row);
-        prefetch_row(first_row + row_step);
-    }
 
     int it = 0;
     for (int64_t row = first_row; row < a.M; row += row_step, ++it) {
