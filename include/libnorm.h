@@ -256,6 +256,10 @@ norm_status rms_bwd(const void* dy, const void* x, const void* w, void* dx, floa
  * no more than can be resident on the device at once (0 when M == 0).
  * `aligned16` != 0 when dy, x, gamma and dx are 16-byte aligned (the
  * backward has no shifted-row mode: other rows use element accesses).
+ * `stages` 2..4 (16-byte vector rows): each CTA keeps its slices of x and dy
+ * of that many upcoming rows in a shared-memory ring filled by bulk copies
+ * (bounded waits, counted by norm_wait_timeouts); 0: rows are read from
+ * L2 after a prefetch. The planner takes 2 stages for fp32 rows.
  * Returns NORM_ERR_ARG for rows beyond the backward's limit.
  */
 norm_status norm_bwd_make_plan(int64_t M, int64_t N, norm_dtype dtype, int layer_norm,
@@ -359,8 +363,8 @@ int norm_last_cuda_error(void);
 int norm_abi_version(void);
 
 /*
- * The ring kernels (plans with `stages` >= 2) wait for their bulk copies
- * with a time limit (2 s); a wait that runs out is counted on the device
+ * The ring kernels (forward and backward plans with `stages` >= 2) wait for
+ * their bulk copies with a time limit (2 s); a wait that runs out is counted on the device
  * and the call's outputs are then not to be trusted. Reads the current
  * device's count into *count and resets it to 0 (synchronises the device).
  * NORM_ERR_ARG if count is NULL; NORM_ERR_CUDA on a runtime error.

@@ -59,6 +59,8 @@ struct BwdArgs {
     int32_t N;
     float eps;            // RMSNorm (rstd is recomputed from x)
     int32_t row_cluster;  // CTAs per row
+    int32_t stages = 0;   // ring kernels: shared-memory stages of upcoming rows (0: none)
+    unsigned int* wait_timeouts = nullptr;  // ring kernels: device counter of waits that gave up
 };
 
 constexpr int kBwdMaxThreads = 512;
@@ -70,9 +72,9 @@ void note_cuda_error(int e);
 // fp32, up to 64 registers of them.
 constexpr int kRingMaxThreads = 512;
 
-// Dynamic shared memory of a ring launch: the stages' 16-byte slots, then
-// one 16-byte slot (the row's first 16 bytes) and one 8-byte mbarrier per
-// stage.
+// Dynamic shared memory of a forward ring launch: the stages' 16-byte
+// slots, then one 16-byte slot (the row's first 16 bytes) and one 8-byte
+// mbarrier per stage.
 inline int64_t ring_smem_bytes(int stages, int per_thread, int threads) {
     return int64_t(stages) * (int64_t(per_thread) * threads * 16 + 16 + 8);
 }
@@ -80,6 +82,14 @@ inline int64_t ring_smem_bytes(int stages, int per_thread, int threads) {
 // Device address of the current device's counter of ring-kernel waits that
 // gave up (norm_wait_timeouts reads it); null if it cannot be resolved.
 unsigned int* wait_counter(int dev);
+
+// Dynamic shared memory of a backward launch: the column accumulators
+// ([2 for LayerNorm | 1][threads * per_thread * vec] fp32), then, for a ring
+// (stages > 0), per stage two slices of 16-byte slots (x, dy) and an 8-byte
+// mbarrier.
+inline int64_t bwd_smem_bytes(bool ln, int threads, int per_thread, int vec, int stages) {
+    return int64_t(ln ? 2 : 1) * threads * per_thread * vec * 4 + int64_t(stages) * (2 * int64_t(threads) * per_thread * 16 + 8);
+}
 
 // Partial rows of the column gradients a backward plan produces (one per
 // cluster, or per CTA without clusters).

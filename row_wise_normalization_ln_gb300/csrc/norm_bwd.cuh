@@ -135,8 +135,9 @@ __device__ __forceinline__ float2 row_sum2(PairReduceSmem& red, int stage, float
 // (in this thread's shared-memory slots for the 16-bit variants of 4
 // accesses per thread); at the end they sit in dynamic shared memory,
 // [NA][T*V*VEC] floats, each thread at the positions of its own columns.
-template <class T, int VEC, int V, bool LN>
+template <class T, int VEC, int V, bool LN, bool RING>
 __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) {
+    static_assert(!RING || VEC > 1, "the ring moves 16-byte vectors");
     using O = OpsFor<T, VEC>;
     using E = BwdElem<T, VEC>;
     using Raw = typename O::Raw;
@@ -167,6 +168,12 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
     const float invN = 1.f / static_cast<float>(N);
     const int slice = T_ * V * VEC;  // floats per accumulator array
     float* my_acc = acc_s + local * VEC;
+    // RING: after the accumulators, `stages` stages of this CTA's slices of
+    // an upcoming row, x then dy (V*T 16-byte slots each), then one mbarrier
+    // per stage.
+    const int stages = RING ? a.stages : 0;
+    uint4* ring = reinterpret_cast<uint4*>(acc_s + NA * slice);
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + 2 * stages * V * T_);
 
     // Column accumulators in registers where they fit beside the row data
     // (all but the 16-bit variants of 4 accesses per thread); otherwise in
@@ -212,16 +219,41 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
             prefetch_l2_line(a.rstd + r);
         }
     };
-    // The first two rows are requested before the dependent-launch wait,
-    // overlapping the previous grid's tail (a prefetch only moves data
-    // towards L2, where that grid's writes land).
-    if (tid == 0) {
-        prefetch_row(first_row);
-        prefetch_row(first_row + row_step);
+    // Rows are prefetched `ahead` rows before their turn: 2 without a ring;
+    // with one, one row beyond those in the ring, so that each bulk copy
+    // into the ring reads L2. The first rows are requested before the
+    // dependent-launch wait, overlapping the previous grid's tail (a
+    // prefetch only moves data towards L2, where that grid's writes land).
+    const int ahead = RING ? stages + 1 : 2;
+    if (tid == 0)
+        for (int k = 0; k < ahead; ++k) prefetch_row(first_row + k * row_step);
+    if constexpr (RING) {
+        if (tid == 0) {
+            for (int k = 0; k < stages; ++k) mbar_init(&full[k], 1);
+            mbar_init_fence();
+        }
+        __syncthreads();
     }
 
     grid_release();
     grid_wait();
+
+    // RING, thread 0: fill stage `st` with this CTA's slices of x and dy of
+    // row `r` (copies read memory: only after the wait above).
+    auto issue = [&](int64_t r, int st) {
+        mbar_arrive_expect(&full[st], 2u * slice_bytes);
+        if (slice_bytes > 0) {
+            bulk_load(ring + (2 * st) * V * T_, static_cast<const T*>(a.x) + r * N + cta_first, slice_bytes,
+                      &full[st]);
+            bulk_load(ring + (2 * st + 1) * V * T_, static_cast<const T*>(a.dy) + r * N + cta_first, slice_bytes,
+                      &full[st]);
+        }
+    };
+    if constexpr (RING) {
+        if (tid == 0)
+            for (int k = 0; k < stages; ++k)
+                if (first_row + k * row_step < a.M) issue(first_row + k * row_step, k);
+    }
 
     // 16-bit rows work on fp32 pairs with the packed instructions and keep
     // gamma widened (gf); other rows work on scalars.
@@ -245,15 +277,32 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
     const T* dybase = static_cast<const T*>(a.dy) + f0 * VEC;
 
     int it = 0;
+    int st = 0;            // RING: this row's stage
+    uint32_t parity = 0;   // ... and the phase parity to wait for
+    int64_t late = -1;     // RING: the row (count) whose wait ran out, if any
     for (int64_t row = first_row; row < a.M; row += row_step, ++it) {
-        if (tid == 0) prefetch_row(row + 2 * row_step);
+        if (tid == 0) prefetch_row(row + ahead * row_step);
         Raw xv[V], dv[V];
+        if constexpr (RING) {
+            // After one wait has run out this CTA neither waits nor copies
+            // any more (its outputs are void by then); the kernel still ends.
+            if (late < 0 && !mbar_wait(&full[st], parity)) late = it;
+            const uint4* xs = ring + (2 * st) * V * T_ + local;
+            const uint4* ds = xs + V * T_;
 #pragma unroll
-        for (int j = 0; j < V; ++j)
-            if (j < nv) {
-                xv[j] = O::load(xbase + row * N + j * stride);
-                dv[j] = O::load(dybase + row * N + j * stride);
-            }
+            for (int j = 0; j < V; ++j)
+                if (j < nv) {
+                    xv[j] = xs[j * 32];
+                    dv[j] = ds[j * 32];
+                }
+        } else {
+#pragma unroll
+            for (int j = 0; j < V; ++j)
+                if (j < nv) {
+                    xv[j] = O::load(xbase + row * N + j * stride);
+                    dv[j] = O::load(dybase + row * N + j * stride);
+                }
+        }
         float mu = 0.f, rs = 0.f;
         if constexpr (LN) {
             mu = a.mean[row];
@@ -303,6 +352,15 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
                 }
         }
         const float2 S = row_sum2(red, it & 1, make_float2(s0, s1), C, nwarps, wwidth);
+        if constexpr (RING) {
+            // Every thread has read this stage before the barrier above:
+            // refill it with the row `stages` turns ahead.
+            if (tid == 0 && late < 0 && row + stages * row_step < a.M) {
+                fence_proxy_async();
+                issue(row + stages * row_step, st);
+            }
+            if (++st == stages) st = 0, parity ^= 1u;
+        }
         T* dxr = static_cast<T*>(a.dx) + row * N + f0 * VEC;
         float c0, c1;  // LayerNorm: mean(g), mean(g xhat); RMSNorm: rstd, rstd^3 mean(dy w x)
         if constexpr (LN) {
@@ -408,6 +466,18 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
             }
     }
 
+    if constexpr (RING) {
+        if (late >= 0 && tid == 0) {
+            // Copies still in flight (rows late .. late+stages-1 of this CTA)
+            // get one more bounded wait each, so that none lands after this
+            // CTA has gone; then tell the host.
+            for (int64_t kk = late; kk < late + stages; ++kk)
+                if (first_row + kk * row_step < a.M)
+                    mbar_wait(&full[kk % stages], static_cast<uint32_t>((kk / stages) & 1));
+            atomicAdd(a.wait_timeouts, 1u);
+        }
+    }
+
     if constexpr (ACC_REG) {
         // Hand the register accumulators to this thread's shared-memory
         // slots (column positions), where the steps below expect them.
@@ -505,16 +575,25 @@ constexpr int bwd_vmax(bool ln, int elem_size, int vec) {
     return vec == 1 ? 8 : (ln && elem_size == 2) ? 2 : 4;
 }
 
-template <class T, bool LN, int VEC>
-BwdKernel pick_bwd(int V) {
+template <class T, bool LN, int VEC, bool RING>
+BwdKernel pick_bwd_r(int V) {
     constexpr int vmax = bwd_vmax(LN, sizeof(T), VEC);
     switch (V) {
-        case 1: return norm_bwd_cta<T, VEC, 1, LN>;
-        case 2: return vmax >= 2 ? norm_bwd_cta<T, VEC, 2, LN> : nullptr;
-        case 4: if constexpr (vmax >= 4) return norm_bwd_cta<T, VEC, 4, LN>; else return nullptr;
-        case 8: if constexpr (vmax >= 8) return norm_bwd_cta<T, VEC, 8, LN>; else return nullptr;
+        case 1: return norm_bwd_cta<T, VEC, 1, LN, RING>;
+        case 2: return vmax >= 2 ? norm_bwd_cta<T, VEC, 2, LN, RING> : nullptr;
+        case 4: if constexpr (vmax >= 4) return norm_bwd_cta<T, VEC, 4, LN, RING>; else return nullptr;
+        case 8: if constexpr (vmax >= 8) return norm_bwd_cta<T, VEC, 8, LN, RING>; else return nullptr;
         default: return nullptr;
     }
+}
+
+// The ring variants exist for 16-byte vector rows only.
+template <class T, bool LN, int VEC>
+BwdKernel pick_bwd(int V, bool ring) {
+    if constexpr (VEC > 1) {
+        if (ring) return pick_bwd_r<T, LN, VEC, true>(V);
+    }
+    return ring ? nullptr : pick_bwd_r<T, LN, VEC, false>(V);
 }
 
 inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, unsigned cluster,
@@ -542,7 +621,8 @@ inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem
 // CTAs of `k` (with `threads` threads, `smem` bytes of dynamic shared memory,
 // launched in clusters of `q`) that can be resident on device `dev` at
 // once, a multiple of q; queried once per configuration and device. Also
-// opts the kernel in to more than 48 KB of dynamic shared memory.
+// opts the kernel in to the device's largest dynamic shared memory when it
+// needs more than 48 KB.
 inline cudaError_t bwd_resident_ctas(BwdKernel k, int threads, size_t smem, int q, int dev, int num_sms,
                                      int64_t* out) {
     struct Key {
@@ -563,8 +643,17 @@ inline cudaError_t bwd_resident_ctas(BwdKernel k, int threads, size_t smem, int 
         return cudaSuccess;
     }
     if (smem > 48 * 1024) {
-        const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k),
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        // Opt in to the device's largest dynamic shared memory per block (not
+        // just this configuration's: another configuration of the same
+        // kernel must never lower the limit below what a cached one needs).
+        int optin = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return e;
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(k));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin - static_cast<int>(fa.sharedSizeBytes));
         if (e != cudaSuccess) return e;
     }
     int64_t ctas = 0;
@@ -605,16 +694,22 @@ template <class T, bool LN>
 cudaError_t launch_norm_bwd(const norm_plan& p, const BwdArgs& a, cudaStream_t stream, int dev, int num_sms) {
     int64_t grid = 0;
     if (a.M > 0 && p.grid > 0) {
-        const BwdKernel k = p.vec_elems == 1 ? pick_bwd<T, LN, 1>(p.per_thread)
-                                             : pick_bwd<T, LN, ElemVec<T>::value>(p.per_thread);
+        const bool ring = p.stages > 0;
+        const BwdKernel k = p.vec_elems == 1 ? pick_bwd<T, LN, 1>(p.per_thread, ring)
+                                             : pick_bwd<T, LN, ElemVec<T>::value>(p.per_thread, ring);
         if (k == nullptr) return cudaErrorInvalidValue;
-        const size_t smem = static_cast<size_t>(LN ? 2 : 1) * p.threads * p.per_thread * p.vec_elems * sizeof(float);
+        const size_t smem = static_cast<size_t>(bwd_smem_bytes(LN, p.threads, p.per_thread, p.vec_elems, p.stages));
         int64_t resident = 0;
         const cudaError_t e0 = bwd_resident_ctas(k, p.threads, smem, p.group, dev, num_sms, &resident);
         if (e0 != cudaSuccess) return e0;
         if (resident < p.group) return cudaErrorInvalidConfiguration;  // not even one cluster fits
         grid = std::min<int64_t>(p.grid, resident);
         BwdArgs args = a;
+        args.stages = p.stages;
+        if (ring) {
+            args.wait_timeouts = wait_counter(dev);
+            if (args.wait_timeouts == nullptr) return cudaErrorInvalidSymbol;
+        }
         void* kargs[] = {&args};
         const cudaError_t e = launch_pdl(reinterpret_cast<const void*>(k), dim3(static_cast<unsigned>(grid)),
                                          dim3(static_cast<unsigned>(p.threads)), smem,

@@ -388,14 +388,17 @@ def test_bwd_workspace_checked_on_the_host(lib):
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on the fake pointers")
-def test_bwd_valid_plan_passes_the_host_checks(lib):
-    p = _bwd_plan()
+@pytest.mark.parametrize("stages", [0, 2, 4])
+def test_bwd_valid_plan_passes_the_host_checks(lib, stages):
+    p = _bwd_plan(stages=stages)
     need = rn.bwd_workspace_bytes(p, 1024, True)
     assert _ln_bwd(lib, 40, 1024, nbytes=need, plan=p) == rn.NORM_ERR_CUDA
 
 
 @pytest.mark.parametrize("kw", [
-    dict(mapping=rn.NORM_MAP_GROUP), dict(stages=2),
+    dict(mapping=rn.NORM_MAP_GROUP), dict(stages=1), dict(stages=5), dict(stages=-1),
+    dict(stages=2, vec_elems=1),                # the ring moves 16-byte vectors
+    dict(stages=4, threads=512, per_thread=4),  # 2*512*4*16 B per stage: the ring exceeds 225 KB
     dict(vec_elems=8), dict(per_thread=8), dict(per_thread=3),
     dict(threads=1024), dict(threads=48),
     dict(cluster=3), dict(cluster=16), dict(group=16), dict(group=3),
@@ -422,7 +425,10 @@ def test_bwd_plans_are_consistent(lib, dtype, ln, M):
                 rn.make_bwd_plan(M, N, dtype, ln, True, 152)
             continue
         p = rn.make_bwd_plan(M, N, dtype, ln, True, 152)
-        assert p["vec_elems"] == vec and p["rounds"] == 1 and p["stages"] == 0
+        assert p["vec_elems"] == vec and p["rounds"] == 1
+        # a 2-stage ring for fp32 vector rows whose ring fits; none otherwise
+        smem = (2 if ln else 1) * p["threads"] * p["per_thread"] * vec * 4 + 2 * (2 * p["threads"] * p["per_thread"] * 16 + 8)
+        assert p["stages"] == (2 if (vec == 4 and smem <= 225 * 1024) else 0)
         assert p["cluster"] * p["threads"] * p["per_thread"] * vec >= N
         assert p["threads"] % 32 == 0 and 32 <= p["threads"] <= 512
         assert p["cluster"] in (1, 2, 4, 8) and p["group"] in (1, 2, 4, 8)

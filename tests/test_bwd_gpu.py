@@ -17,7 +17,7 @@ from parity import check_ln_bwd, check_rms_bwd, ln_stats_f32, sample_rows
 
 pytestmark = pytest.mark.gpu
 
-DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -188,6 +188,50 @@ def test_every_variant(dtype, ln, plan, N):
 
 # ------------------------------------------------------------ layouts and errors
 
+def _ring_variants():
+    out = []
+    for dtype, vec in (("f32", 4), ("bf16", 8), ("f16", 8)):
+        for ln in (True, False):
+            vmax = 2 if (ln and dtype != "f32") else 4
+            for per in (1, 2, 4):
+                if per > vmax:
+                    continue
+                for T in (32, 512):
+                    for C in (1, 2, 8):
+                        cap = C * T * per * vec
+                        if cap > 140000:
+                            continue
+                        Q = C if C > 1 else 2
+                        for S in (2, 3):
+                            smem = (2 if ln else 1) * T * per * vec * 4 + S * (2 * T * per * 16 + 8)
+                            if smem > 225 * 1024:
+                                continue
+                            for N in sorted({cap, max(vec, cap - 3 * vec)}):
+                                out.append((dtype, ln, dict(mapping=rn.NORM_MAP_CTA, vec_elems=vec, per_thread=per,
+                                                            group=Q, threads=T, cluster=C, stages=S, grid=2 * Q), N))
+    return out
+
+
+RING = _ring_variants()
+
+
+@pytest.mark.parametrize("dtype,ln,plan,N", RING,
+                         ids=[f"{d}-{'ln' if ln else 'rms'}-p{p['per_thread']}-t{p['threads']}-c{p['cluster']}"
+                              f"-s{p['stages']}-N{n}" for d, ln, p, n in RING])
+def test_ring_variants(dtype, ln, plan, N):
+    """Plans with a shared-memory ring of upcoming rows (bulk copies): an
+    exact and a ragged row, two clusters walking 37 rows, so every stage is
+    refilled several times. No wait may run out."""
+    x, dy, g = _rand(37, N, DT[dtype], seed=N + 3 * plan["threads"] + plan["stages"], loc=0.5, scale=2.0)
+    if ln:
+        dx, dg, db = run_ln_bwd(dy, x, g, 1e-5, plan=plan)
+        check_ln_bwd(dy, x, g, 1e-5, dx, dg, db)
+    else:
+        dx, dw = run_rms_bwd(dy, x, g, 1e-6, plan=plan)
+        check_rms_bwd(dy, x, g, 1e-6, dx, dw)
+    assert rn.wait_timeouts() == 0
+
+
 def test_unaligned_pointers_take_the_element_path():
     N, M = 1000, 37
     base = torch.randn(2 * M * N + 3, device="cuda")
@@ -221,6 +265,19 @@ def test_in_place(N):
         dx, dw = rn.rms_bwd(dyd, xd, g.cuda(), 1e-6, dx=target)
         torch.cuda.synchronize()
         check_rms_bwd(dy, x, g, 1e-6, dx, dw)
+
+
+def test_smem_limit_survives_smaller_configurations():
+    """One kernel (LayerNorm fp32, 4 accesses per thread, ring) launched with
+    192 KB of shared memory, then for the first time with 144 KB, then with
+    192 KB again: a configuration first seen later must not lower the
+    kernel's shared-memory limit below what an earlier one needs."""
+    big = dict(mapping=rn.NORM_MAP_CTA, vec_elems=4, per_thread=4, group=8, threads=512, cluster=8, stages=2, grid=16)
+    small = dict(mapping=rn.NORM_MAP_CTA, vec_elems=4, per_thread=4, group=2, threads=384, cluster=1, stages=2, grid=4)
+    for N, plan in ((65536, big), (6144, small), (65536, big)):
+        x, dy, g = _rand(5, N, torch.float32, seed=N)
+        dx, dg, db = run_ln_bwd(dy, x, g, 1e-5, plan=plan)
+        check_ln_bwd(dy, x, g, 1e-5, dx, dg, db)
 
 
 def test_deterministic():
