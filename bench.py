@@ -79,9 +79,9 @@ def measured_peak():
 # capture summarised in profiles/ (workload -> (kernel source hash at capture,
 # bytes per launch, summary file)).
 NCU_TRAFFIC = {
-    "rms_f32_8192x4096": ("c0bac7c1ac746e55", 208_613_376, "profiles/norm_fwd_cta_rms_f32_8192x4096.md"),
-    "ln_bf16_4096x8192_outliers": ("c0bac7c1ac746e55", 84_946_944, "profiles/norm_fwd_cta_ln_bf16_4096x8192.md"),
-    "ln_f32_8192x5001": ("c0bac7c1ac746e55", 277_643_776, "profiles/norm_fwd_cta_shift_ln_f32_8192x5001.md"),
+    "rms_f32_8192x4096": ("959df36da0004bd0", 207_211_264, "profiles/norm_fwd_cta_rms_f32_8192x4096.md"),
+    "ln_bf16_4096x8192_outliers": ("959df36da0004bd0", 85_750_272, "profiles/norm_fwd_cta_ln_bf16_4096x8192.md"),
+    "ln_f32_8192x5001": ("959df36da0004bd0", 278_338_048, "profiles/norm_fwd_cta_shift_ln_f32_8192x5001.md"),
 }
 
 
