@@ -80,6 +80,10 @@ __device__ __forceinline__ float2 bf16x2_widen(uint32_t w) { return make_float2(
 struct Bf16Pair {
     static __device__ __forceinline__ float2 widen(uint32_t w) { return bf16x2_widen(w); }
     static __device__ __forceinline__ uint32_t pack(float lo, float hi) { return pack_bf16x2(lo, hi); }
+    // (lo + c, hi + c) in fp32, each widened exactly and rounded once. For
+    // bf16 the widening is a shift and a mask and one packed add follows
+    // (the mixed-precision add measured more instructions here).
+    static __device__ __forceinline__ float2 add(uint32_t w, float c) { return __fadd2_rn(widen(w), f2_splat(c)); }
 };
 struct F16Pair {
     static __device__ __forceinline__ float2 widen(uint32_t w) {
@@ -88,6 +92,17 @@ struct F16Pair {
     static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
         const __half2 h = __floats2half2_rn(lo, hi);  // round to nearest-even
         return *reinterpret_cast<const uint32_t*>(&h);
+    }
+    // The same for fp16 with the sm_100-family mixed-precision add, which
+    // takes the 16-bit halves directly (measured faster than converting
+    // the pair and adding).
+    static __device__ __forceinline__ float2 add(uint32_t w, float c) {
+        float2 r;
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+            "add.rn.f32.f16 %0, l, %3;\n\tadd.rn.f32.f16 %1, h, %3;\n\t}"
+            : "=f"(r.x), "=f"(r.y)
+            : "r"(w), "f"(c));
+        return r;
     }
 };
 
@@ -170,19 +185,20 @@ struct Ops16 {
     static __device__ __forceinline__ uint32_t w(const Raw& r, int i) {
         return i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w;
     }
+    // x - K of a word's two elements (exact widening, one rounding).
+    static __device__ __forceinline__ float2 shifted(uint32_t wd, float K) { return P::add(wd, -K); }
     static __device__ __forceinline__ float shifted_sum(const Raw& r, float K) {
-        const float2 nk = f2_splat(-K);
-        const float2 a = __fadd2_rn(__fadd2_rn(P::widen(r.x), nk), __fadd2_rn(P::widen(r.y), nk));
-        const float2 b = __fadd2_rn(__fadd2_rn(P::widen(r.z), nk), __fadd2_rn(P::widen(r.w), nk));
+        const float2 a = __fadd2_rn(shifted(r.x, K), shifted(r.y, K));
+        const float2 b = __fadd2_rn(shifted(r.z, K), shifted(r.w, K));
         const float2 s = __fadd2_rn(a, b);
         return s.x + s.y;
     }
     static __device__ __forceinline__ float dev2(const Raw& r, float K, float mu, float acc) {
-        const float2 nk = f2_splat(-K), nm = f2_splat(-mu);
+        const float2 nm = f2_splat(-mu);
         float2 q = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float2 d = __fadd2_rn(__fadd2_rn(P::widen(w(r, i)), nk), nm);
+            const float2 d = __fadd2_rn(shifted(w(r, i), K), nm);
             q = __ffma2_rn(d, d, q);
         }
         return acc + (q.x + q.y);
@@ -198,12 +214,11 @@ struct Ops16 {
     }
     static __device__ __forceinline__ Raw ln_out(const Raw& r, float K, float rs, float nmr, const Raw& g,
                                                  const Raw& b) {
-        const float2 nk = f2_splat(-K), rs2 = f2_splat(rs), nm2 = f2_splat(nmr);
+        const float2 rs2 = f2_splat(rs), nm2 = f2_splat(nmr);
         uint32_t o[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float2 y = __ffma2_rn(__ffma2_rn(__fadd2_rn(P::widen(w(r, i)), nk), rs2, nm2),
-                                        P::widen(w(g, i)), P::widen(w(b, i)));
+            const float2 y = __ffma2_rn(__ffma2_rn(shifted(w(r, i), K), rs2, nm2), P::widen(w(g, i)), P::widen(w(b, i)));
             o[i] = P::pack(y.x, y.y);
         }
         return make_uint4(o[0], o[1], o[2], o[3]);
@@ -220,11 +235,10 @@ struct Ops16 {
     }
     static __device__ __forceinline__ void ln_vals(const Raw& r, float K, float rs, float nmr, const Raw& g,
                                                    const Raw& b, float* o) {
-        const float2 nk = f2_splat(-K), rs2 = f2_splat(rs), nm2 = f2_splat(nmr);
+        const float2 rs2 = f2_splat(rs), nm2 = f2_splat(nmr);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float2 y = __ffma2_rn(__ffma2_rn(__fadd2_rn(P::widen(w(r, i)), nk), rs2, nm2),
-                                        P::widen(w(g, i)), P::widen(w(b, i)));
+            const float2 y = __ffma2_rn(__ffma2_rn(shifted(w(r, i), K), rs2, nm2), P::widen(w(g, i)), P::widen(w(b, i)));
             o[2 * i] = y.x;
             o[2 * i + 1] = y.y;
         }
