@@ -21,7 +21,9 @@
 // LayerNorm statistics ([Ch7] §7.4, §7.4.1): each thread forms the Welford
 // state (n_t, mean_t, M2_t) of its own elements, shifted by the row's first
 // element K, by two passes over its registers ([T3] §② trap 2: the row is
-// in registers, so "two passes" cost no memory traffic). The states of all
+// in registers, so "two passes" cost no memory traffic); on 16-bit rows, by
+// two passes over each 16-byte access and the pairwise merge of the access
+// states (Slice::welford). The states of all
 // threads of the row are then merged with the merge rule in its k-way form,
 //     mean = sum_t n_t mean_t / N,    M2 = sum_t (M2_t + n_t (mean_t - mean)^2),
 // which is what any sequence of pairwise merges reaches; each sum is an xor
@@ -413,9 +415,52 @@ struct Slice {
         for (int j = 0; j < V; ++j)
             if (j < nvalid) O::store(ph + j * stride, raw[j]);
     }
-    // Welford state of the valid elements, two passes over the registers:
-    // the sum and mean of x - K, then M2 about that mean.
+    // Welford state of the valid elements. 16-bit rows: each access's eight
+    // values of x - K get their own two-pass state (sum, mean, M2 about
+    // that mean) and are merged into the thread's running state with the
+    // pairwise merge rule ([Ch7] §7.4.1); after j accesses the thread holds
+    // 8j values, so the weights 1/(j+1) and 8j/(j+1) are constants. This
+    // widens each value once for the statistics. Other rows: two passes
+    // over the registers, the sum and mean of x - K, then M2 about that mean.
+    // STREAM selects the per-access form for 16-bit rows (the fused-add
+    // kernels measured slower with it, and the cluster kernels, which no
+    // benchmark shape measured, keep the two passes too).
+    template <bool STREAM = true>
     __device__ __forceinline__ void welford(int nvalid, float inv_n, float& sum, float& mean, float& m2) const {
+        if constexpr (VEC == 8 && STREAM) {
+            float sum_r = 0.f, mean_r = 0.f, m2_r = 0.f;
+#pragma unroll
+            for (int j = 0; j < V; ++j)
+                if (j < nvalid) {
+                    float2 d[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) d[i] = O::shifted(O::w(raw[j], i), K);
+                    const float2 t = __fadd2_rn(__fadd2_rn(d[0], d[1]), __fadd2_rn(d[2], d[3]));
+                    const float sj = t.x + t.y;
+                    const float mj = sj * 0.125f;
+                    const float2 nm = f2_splat(-mj);
+                    float2 q = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 e = __fadd2_rn(d[i], nm);
+                        q = __ffma2_rn(e, e, q);
+                    }
+                    const float qj = q.x + q.y;
+                    if (j == 0) {
+                        mean_r = mj;
+                        m2_r = qj;
+                    } else {
+                        const float dm = mj - mean_r;
+                        mean_r = fmaf(dm, 1.f / static_cast<float>(j + 1), mean_r);
+                        m2_r = fmaf(dm * dm, 8.f * static_cast<float>(j) / static_cast<float>(j + 1), m2_r + qj);
+                    }
+                    sum_r += sj;
+                }
+            sum = sum_r;
+            mean = mean_r;
+            m2 = m2_r;
+            return;
+        }
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
         for (int j = 0; j < V; ++j)
@@ -605,7 +650,7 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_group(
         float mu = 0.f, rs;
         if constexpr (LN) {
             float sum = 0.f, mean = 0.f, m2 = 0.f;
-            s.welford(nv, inv_n, sum, mean, m2);
+            s.template welford<!ADD>(nv, inv_n, sum, mean, m2);
             mu = group_sum(sum, G) * invN;
             const float d = mean - mu;
             const float M2 = group_sum(nv > 0 ? fmaf(n_t * d, d, m2) : 0.f, G);
@@ -744,7 +789,7 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
             if constexpr (LN) {
                 const float n = static_cast<float>(nv * VEC);
                 float sum = 0.f, mean = 0.f, m2 = 0.f;
-                s.welford(nv, nv > 0 ? 1.f / n : 0.f, sum, mean, m2);
+                s.template welford<!ADD && !CL>(nv, nv > 0 ? 1.f / n : 0.f, sum, mean, m2);
                 if (i == 0) {
                     n_t = n, sum_t = sum, mean_t = mean, m2_t = m2;
                 } else if (n > 0.f) {  // pairwise merge ([Ch7] §7.4.1)
