@@ -437,51 +437,50 @@ def time_e2e_bwd(w, rn, inp, device, steps):
 
 
 def time_e2e(w, rn, inp, device, steps):
-    """Host buffers in, host buffers out: H2D of x (and r) and the
-    parameters, the call, D2H of y (and h, and the statistics), every step,
-    on one stream."""
+    """Host buffers in, host buffers out, through the library's public API:
+    every step copies the parameters to the device and runs the call over
+    the rows with ``host_rows_pipeline`` (row chunks copied in, normalised
+    and copied back on three streams, so the two copy directions and the
+    kernels overlap): x (and r) in, y (and h, and the statistics) out."""
     if w.bwd:
         return time_e2e_bwd(w, rn, inp, device, steps)
     import torch
     hin = {k: v.pin_memory() for k, v in inp.items()}
-    din = {k: torch.empty_like(v, device=device) for k, v in hin.items()}
+    rowin = ["x"] + (["r"] if w.add else [])
+    params = [k for k in hin if k not in rowin]
+    dpar = {k: torch.empty_like(hin[k], device=device) for k in params}
     ydt = torch.uint8 if w.fp8 else w.torch_dtype
-    dy = torch.empty(w.M, w.N, dtype=ydt, device=device)
     hy = torch.empty(w.M, w.N, dtype=ydt).pin_memory()
-    dh = torch.empty_like(din["x"]) if w.add else None
     hh = torch.empty_like(hin["x"]).pin_memory() if w.add else None
     sc = torch.tensor([w.qscale], dtype=torch.float32, device=device) if w.fp8 else None
     ln = w.op == "ln"
-    if ln:
-        dm = torch.empty(w.M, dtype=torch.float32, device=device)
-        dr = torch.empty_like(dm)
-        hm = torch.empty(w.M, dtype=torch.float32).pin_memory()
-        hr = torch.empty_like(hm).pin_memory()
+    hm = torch.empty(w.M, dtype=torch.float32).pin_memory() if ln else None
+    hr = torch.empty_like(hm).pin_memory() if ln else None
+    outs = [hy] + ([hh] if w.add else []) + ([hm, hr] if ln else [])
     h2d = sum(v.numel() * v.element_size() for v in hin.values())
     d2h = hy.numel() * hy.element_size() + (hh.numel() * hh.element_size() if w.add else 0) + (8 * w.M if ln else 0)
 
-    def one():
-        for k in hin:
-            din[k].copy_(hin[k], non_blocking=True)
+    def call(ins, o):
+        x, r = ins[0], (ins[1] if w.add else None)
+        y, h = o[0], (o[1] if w.add else None)
+        m, rs = (o[-2], o[-1]) if ln else (None, None)
         if w.fp8 and ln:
-            rn.ln_fwd_fp8(din["x"], din["gamma"], din["beta"], sc, w.eps, residual=din.get("r"), h_out=dh, out=dy,
-                          mean=dm, rstd=dr)
+            rn.ln_fwd_fp8(x, dpar["gamma"], dpar["beta"], sc, w.eps, residual=r, h_out=h, out=y, mean=m, rstd=rs)
         elif w.fp8:
-            rn.rms_fwd_fp8(din["x"], din["w"], sc, w.eps, residual=din.get("r"), h_out=dh, out=dy)
+            rn.rms_fwd_fp8(x, dpar["w"], sc, w.eps, residual=r, h_out=h, out=y)
         elif ln and w.add:
-            rn.ln_fwd_add(din["x"], din["r"], din["gamma"], din["beta"], w.eps, h_out=dh, out=dy, mean=dm, rstd=dr)
+            rn.ln_fwd_add(x, r, dpar["gamma"], dpar["beta"], w.eps, h_out=h, out=y, mean=m, rstd=rs)
         elif ln:
-            rn.ln_fwd(din["x"], din["gamma"], din["beta"], w.eps, out=dy, mean=dm, rstd=dr)
+            rn.ln_fwd(x, dpar["gamma"], dpar["beta"], w.eps, out=y, mean=m, rstd=rs)
         elif w.add:
-            rn.rms_fwd_add(din["x"], din["r"], din["w"], w.eps, h_out=dh, out=dy)
+            rn.rms_fwd_add(x, r, dpar["w"], w.eps, h_out=h, out=y)
         else:
-            rn.rms_fwd(din["x"], din["w"], w.eps, out=dy)
-        if ln:
-            hm.copy_(dm, non_blocking=True)
-            hr.copy_(dr, non_blocking=True)
-        if w.add:
-            hh.copy_(dh, non_blocking=True)
-        hy.copy_(dy, non_blocking=True)
+            rn.rms_fwd(x, dpar["w"], w.eps, out=y)
+
+    def one():
+        for k in params:
+            dpar[k].copy_(hin[k], non_blocking=True)
+        rn.host_rows_pipeline([hin[k] for k in rowin], outs, call, device=device)
 
     for _ in range(3):
         one()

@@ -18,7 +18,7 @@ import torch
 
 __all__ = [
     "ln_fwd", "rms_fwd", "ln_fwd_add", "rms_fwd_add", "ln_fwd_fp8", "rms_fwd_fp8", "ln_bwd", "rms_bwd",
-    "make_plan", "make_bwd_plan", "NormPlan", "NormError", "LibraryNotBuilt", "library",
+    "make_plan", "make_bwd_plan", "NormPlan", "NormError", "LibraryNotBuilt", "library", "host_rows_pipeline",
     "NORM_F32", "NORM_BF16", "NORM_F16", "NORM_MAP_GROUP", "NORM_MAP_CTA",
 ]
 
@@ -534,3 +534,88 @@ def rms_fwd_fp8(x: torch.Tensor, w: torch.Tensor, scale, eps: float = 1e-6, *,
     if residual is not None:
         return hh.view(x.shape), y8
     return y8
+
+
+# ------------------------------------------------------------ host buffers
+_PIPELINES = {}
+
+
+def _pipeline_streams(dev: torch.device):
+    """The copy-in and copy-back streams and the per-buffer events of
+    host_rows_pipeline on `dev`, made once (events are reused: each wait is
+    queued after the record it refers to)."""
+    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    p = _PIPELINES.get(key)
+    if p is None:
+        p = (torch.cuda.Stream(dev), torch.cuda.Stream(dev), [torch.cuda.Event() for _ in range(2)],
+             [torch.cuda.Event() for _ in range(2)],  # the kernels of the buffer's last chunk
+             [torch.cuda.Event() for _ in range(2)])  # the copy back of the buffer's last chunk
+        _PIPELINES[key] = p
+    return p
+
+
+def host_rows_pipeline(inputs, outputs, call, *, chunk_rows: Optional[int] = None,
+                       device: Optional[torch.device] = None):
+    """Run a row-wise library call over pinned host tensors, overlapping the
+    copies in both directions with the kernels.
+
+    ``inputs`` and ``outputs`` are lists of pinned CPU tensors whose first
+    dimension is the row count M (an FP8 output is a uint8 tensor; per-row
+    statistics are ``[M]`` fp32 tensors). The rows are taken in chunks of
+    ``chunk_rows`` (default: M/4, at least 256 rows): chunk c+1 is copied to
+    the device on one stream while chunk c runs on the current stream and
+    chunk c-1 is copied back on a third, through two device staging buffers
+    per tensor (allocated with torch). ``call(ins, outs)`` receives device
+    tensors holding one chunk's rows and launches the library call for them
+    on the current stream, e.g. ``lambda i, o: rms_fwd(i[0], w, eps,
+    out=o[0])`` with ``w`` already on the device. Returns when all work is
+    queued; the current stream waits for the last copy back, so a
+    ``torch.cuda.synchronize()`` (or an event on the current stream) makes
+    the host outputs readable. Not for calls that reduce over rows (the
+    backward's column gradients)."""
+    if not inputs or not outputs:
+        raise ValueError("inputs and outputs must be non-empty lists of pinned host tensors")
+    M = inputs[0].shape[0]
+    for t in list(inputs) + list(outputs):
+        if t.device.type != "cpu" or t.shape[0] != M or not t.is_contiguous():
+            raise ValueError("host tensors must be contiguous CPU tensors with the same number of rows")
+    if M == 0:
+        return  # nothing to copy (an empty tensor has no storage to pin)
+    for t in list(inputs) + list(outputs):
+        if not t.is_pinned():
+            raise ValueError("host tensors must be pinned (tensor.pin_memory())")
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    chunk = chunk_rows if chunk_rows is not None else max(256, -(-M // 4))
+    chunk = max(1, min(chunk, M))
+    comp = torch.cuda.current_stream(dev)
+    s_in, s_out, in_ready, done, copied = _pipeline_streams(dev)
+    d_in = [[torch.empty((chunk,) + tuple(t.shape[1:]), dtype=t.dtype, device=dev) for t in inputs] for _ in range(2)]
+    d_out = [[torch.empty((chunk,) + tuple(t.shape[1:]), dtype=t.dtype, device=dev) for t in outputs] for _ in range(2)]
+    s_in.wait_stream(comp)                            # staging memory and inputs as of now
+    s_out.wait_stream(comp)
+    for c, r0 in enumerate(range(0, M, chunk)):
+        b = c % 2
+        n = min(M, r0 + chunk) - r0
+        if c >= 2:
+            s_in.wait_event(done[b])                  # the kernels reading d_in[b] have run
+        with torch.cuda.stream(s_in):
+            for d, h in zip(d_in[b], inputs):
+                d[:n].copy_(h[r0:r0 + n], non_blocking=True)
+            in_ready[b].record(s_in)
+        comp.wait_event(in_ready[b])
+        if c >= 2:
+            comp.wait_event(copied[b])                # d_out[b] has been copied back
+        call([d[:n] for d in d_in[b]], [d[:n] for d in d_out[b]])
+        done[b].record(comp)
+        s_out.wait_event(done[b])
+        with torch.cuda.stream(s_out):
+            for h, d in zip(outputs, d_out[b]):
+                h[r0:r0 + n].copy_(d[:n], non_blocking=True)
+            copied[b].record(s_out)
+    comp.wait_stream(s_out)
+    comp.wait_stream(s_in)
+    # keep the staging buffers alive until the queued work has used them
+    for bufs in d_in + d_out:
+        for t in bufs:
+            t.record_stream(s_in)
+            t.record_stream(s_out)

@@ -472,3 +472,12 @@ def test_strided_argument_checks(lib):
     p = _plan(threads=256, per_thread=1, vec_elems=4)
     assert lib.rms_fwd_strided(P, 1001, P, Q, 1002, 4, 1000, 1e-6, rn.NORM_F32, None,
                                ctypes.byref(p)) == rn.NORM_ERR_PLAN
+
+
+def test_host_pipeline_refuses_unpinned_tensors():
+    # checked before any device work
+    x = torch.zeros(4, 8)
+    with pytest.raises(ValueError):
+        rn.host_rows_pipeline([x], [torch.zeros(4, 8)], lambda i, o: None)
+    with pytest.raises(ValueError):
+        rn.host_rows_pipeline([], [x], lambda i, o: None)
