@@ -79,9 +79,9 @@ def measured_peak():
 # capture summarised in profiles/ (workload -> (kernel source hash at capture,
 # bytes per launch, summary file)).
 NCU_TRAFFIC = {
-    "rms_f32_8192x4096": ("959df36da0004bd0", 207_211_264, "profiles/norm_fwd_cta_rms_f32_8192x4096.md"),
-    "ln_bf16_4096x8192_outliers": ("959df36da0004bd0", 85_750_272, "profiles/norm_fwd_cta_ln_bf16_4096x8192.md"),
-    "ln_f32_8192x5001": ("959df36da0004bd0", 278_338_048, "profiles/norm_fwd_cta_shift_ln_f32_8192x5001.md"),
+    "rms_f32_8192x4096": ("9734921bab6fa0dd", 207_655_680, "profiles/norm_fwd_cta_rms_f32_8192x4096.md"),
+    "ln_bf16_4096x8192_outliers": ("9734921bab6fa0dd", 85_753_088, "profiles/norm_fwd_cta_ln_bf16_4096x8192.md"),
+    "ln_f32_8192x5001": ("9734921bab6fa0dd", 278_236_416, "profiles/norm_fwd_cta_shift_ln_f32_8192x5001.md"),
 }
 
 
