@@ -12,6 +12,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import threading
 from typing import Optional
 
 import torch
@@ -538,19 +539,23 @@ def rms_fwd_fp8(x: torch.Tensor, w: torch.Tensor, scale, eps: float = 1e-6, *,
 
 # ------------------------------------------------------------ host buffers
 _PIPELINES = {}
+_PIPELINES_LOCK = threading.Lock()
 
 
 def _pipeline_streams(dev: torch.device):
-    """The copy-in and copy-back streams and the per-buffer events of
-    host_rows_pipeline on `dev`, made once (events are reused: each wait is
-    queued after the record it refers to)."""
+    """The copy-in and copy-back streams, the per-buffer events and a lock of
+    host_rows_pipeline on `dev`, made once. Events are reused: each wait is
+    queued after the record it refers to, which the lock keeps true when
+    several host threads call at once."""
     key = dev.index if dev.index is not None else torch.cuda.current_device()
-    p = _PIPELINES.get(key)
-    if p is None:
-        p = (torch.cuda.Stream(dev), torch.cuda.Stream(dev), [torch.cuda.Event() for _ in range(2)],
-             [torch.cuda.Event() for _ in range(2)],  # the kernels of the buffer's last chunk
-             [torch.cuda.Event() for _ in range(2)])  # the copy back of the buffer's last chunk
-        _PIPELINES[key] = p
+    with _PIPELINES_LOCK:
+        p = _PIPELINES.get(key)
+        if p is None:
+            p = (torch.cuda.Stream(dev), torch.cuda.Stream(dev), [torch.cuda.Event() for _ in range(2)],
+                 [torch.cuda.Event() for _ in range(2)],  # the kernels of the buffer's last chunk
+                 [torch.cuda.Event() for _ in range(2)],  # the copy back of the buffer's last chunk
+                 threading.Lock())
+            _PIPELINES[key] = p
     return p
 
 
@@ -588,7 +593,12 @@ def host_rows_pipeline(inputs, outputs, call, *, chunk_rows: Optional[int] = Non
     chunk = chunk_rows if chunk_rows is not None else max(256, -(-M // 4))
     chunk = max(1, min(chunk, M))
     comp = torch.cuda.current_stream(dev)
-    s_in, s_out, in_ready, done, copied = _pipeline_streams(dev)
+    s_in, s_out, in_ready, done, copied, lock = _pipeline_streams(dev)
+    with lock:
+        _enqueue_pipeline(inputs, outputs, call, M, chunk, dev, comp, s_in, s_out, in_ready, done, copied)
+
+
+def _enqueue_pipeline(inputs, outputs, call, M, chunk, dev, comp, s_in, s_out, in_ready, done, copied):
     d_in = [[torch.empty((chunk,) + tuple(t.shape[1:]), dtype=t.dtype, device=dev) for t in inputs] for _ in range(2)]
     d_out = [[torch.empty((chunk,) + tuple(t.shape[1:]), dtype=t.dtype, device=dev) for t in outputs] for _ in range(2)]
     s_in.wait_stream(comp)                            # staging memory and inputs as of now

@@ -88,3 +88,36 @@ def test_zero_rows_and_a_consumer_on_the_stream():
     back = hy.to("cuda", non_blocking=True)   # ordered after the pipeline on the current stream
     torch.cuda.synchronize()
     check_rms(x, g, 1e-6, back)
+
+
+def test_two_host_threads_at_once():
+    """Two host threads, each on its own stream, run pipelines on the same
+    device at the same time; both results match the oracle."""
+    import threading
+    N = 2048
+    cases = []
+    for k in range(2):
+        x, _, g, _ = _rand(600, N, torch.float32, seed=40 + k)
+        cases.append((x, g, x.pin_memory(), torch.empty(600, N).pin_memory(), g.cuda()))
+    errs = []
+
+    def work(c):
+        try:
+            x, g, hx, hy, gd = c
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(5):
+                    rn.host_rows_pipeline([hx], [hy], lambda i, o: rn.rms_fwd(i[0], gd, 1e-6, out=o[0]), chunk_rows=128)
+            s.synchronize()
+        except Exception as e:  # reported below
+            errs.append(e)
+
+    ts = [threading.Thread(target=work, args=(c,)) for c in cases]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errs, errs
+    torch.cuda.synchronize()
+    for x, g, hx, hy, gd in cases:
+        check_rms(x, g, 1e-6, hy)
