@@ -54,6 +54,20 @@ __device__ __forceinline__ void cluster_barrier() {
         "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
+// The two halves of cluster_barrier, for a barrier whose arrival can come
+// early: a thread arrives once it has finished the accesses its peers must
+// see completed (its reads of their shared memory), does other work, and
+// waits later, right before what those accesses must precede (a peer
+// rewriting or releasing that memory). A thread's arrives and waits
+// alternate; every CTA of the cluster makes the same sequence of them.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
 // Address of `p` (a __shared__ variable of this CTA) in the shared memory
 // window of cluster peer `rank`.
 __device__ __forceinline__ uint32_t peer_smem_addr(const void* p, uint32_t rank) {

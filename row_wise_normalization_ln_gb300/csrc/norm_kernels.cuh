@@ -587,6 +587,7 @@ __device__ __forceinline__ float2 cta_sum2(RowReduceSmem& red, float a, float b,
     return make_float2(sum_first_lanes(w.x, wwidth), sum_first_lanes(w.y, wwidth));
 }
 
+template <bool EARLY = false>
 __device__ __forceinline__ float row_sum(RowReduceSmem& red, int stage, float v, uint32_t C, int nwarps,
                                          int wwidth) {
     const int tid = threadIdx.x;
@@ -601,6 +602,7 @@ __device__ __forceinline__ float row_sum(RowReduceSmem& red, int stage, float v,
         v = sum_first_lanes(
             lane < static_cast<int>(C) ? ld_peer_f32(peer_smem_addr(&red.cta_part[stage], lane)) : 0.f,
             static_cast<int>(C));
+        if constexpr (EARLY) cluster_arrive();  // done with the peers' slots; the caller waits
     }
     return v;
 }
@@ -616,7 +618,12 @@ __device__ __forceinline__ float row_sum(RowReduceSmem& red, int stage, float v,
 // rows). `stage`: the stage of RMSNorm's one sum, and of the CTA state a
 // LayerNorm cluster publishes (callers that walk several rows per CTA
 // alternate it or put a barrier between rows).
-template <bool LN>
+// EARLY (C > 1 only): each thread arrives at the next cluster barrier as
+// soon as it has read the peers' values, and the caller waits on it before
+// this CTA's slot is written again or the CTA exits, so that the wait
+// costs nothing once the peers are past their own reads (a full barrier
+// there would wait for the slowest peer's whole output pass).
+template <bool LN, bool EARLY = false>
 __device__ __forceinline__ void row_stats(RowReduceSmem& red, float n_t, float sum_t, float mean_t, float m2_t,
                                           float ss_t, float invN, float eps, uint32_t C, int nwarps, int wwidth,
                                           int stage, float& mu, float& rs) {
@@ -649,11 +656,13 @@ __device__ __forceinline__ void row_stats(RowReduceSmem& red, float n_t, float s
             mu = sum_first_lanes(sq, static_cast<int>(C)) * invN;
             const float dq = (nq > 0.f ? sq / nq : 0.f) - mu;
             const float m2 = sum_first_lanes(fmaf(nq * dq, dq, mq), static_cast<int>(C));
+            // every peer value consumed, the warp converged by the shuffles
+            if constexpr (EARLY) cluster_arrive();  // the caller waits
             rs = rsqrtf(m2 * invN + eps);
         }
     } else {
         mu = 0.f;
-        rs = rsqrtf(row_sum(red, stage, ss_t, C, nwarps, wwidth) * invN + eps);
+        rs = rsqrtf(row_sum<EARLY>(red, stage, ss_t, C, nwarps, wwidth) * invN + eps);
     }
 }
 
@@ -869,7 +878,7 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
             }
         }
         float mu, rs;
-        row_stats<LN>(red, n_t, sum_t, mean_t, m2_t, ss_t, invN, a.eps, C, nwarps, wwidth, 0, mu, rs);
+        row_stats<LN, CL>(red, n_t, sum_t, mean_t, m2_t, ss_t, invN, a.eps, C, nwarps, wwidth, 0, mu, rs);
         if (LN && rank == 0 && tid == 0) {
             if (a.mean) a.mean[row] = K + mu;
             if (a.rstd) a.rstd[row] = rs;
@@ -925,18 +934,23 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
         // this CTA (cluster) writes that slot again for its next row, every
         // thread of it (and of its peers) must have read this row's values.
         // (One CTA's LayerNorm sums use two stages and order that by
-        // themselves.) One-row-per-CTA launches never get here.
+        // themselves.) One-row-per-CTA launches never get here. In a
+        // cluster every thread arrived right after reading its peers'
+        // values (row_stats, EARLY), so the wait here is for the peers'
+        // reads only, not for their output passes.
         if constexpr (!LN || CL) {
             if (row + row_step < a.M) {
                 if (C > 1)
-                    cluster_barrier();
+                    cluster_wait();
                 else
                     __syncthreads();
             }
         }
     }
-    // No CTA may exit while a peer can still read its shared memory.
-    if (C > 1) cluster_barrier();
+    // No CTA may exit while a peer can still read its shared memory: wait
+    // on the arrive of the last row's exchange (CTAs of a cluster share
+    // their rows, so a cluster without rows made no exchange at all).
+    if (C > 1 && first_row < a.M) cluster_wait();
 }
 
 // ================================================================== RING
