@@ -83,6 +83,15 @@ __device__ __forceinline__ float ld_peer_f32(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ float4 ld_peer_f32x4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // ----------------------------------------------------------- dependent launch
 // Programmatic dependent launch: a kernel launched with the programmatic
 // stream-serialization attribute may be scheduled before the previous kernel

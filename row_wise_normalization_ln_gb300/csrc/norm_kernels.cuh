@@ -569,8 +569,16 @@ __device__ __forceinline__ int valid_runs(int nacc, int first, int stride_acc, i
 struct RowReduceSmem {
     float warp_part[2][32];   // [stage][warp]
     float cta_part[2];        // [stage], read by cluster peers
+    static constexpr bool kWarpStates = false;
     float2 warp_pair[32];     // [warp]: LayerNorm in a cluster, (sum, count) of each warp
     float cta_state[2][4];    // [stage]: LayerNorm in a cluster, (count, sum, M2) of this CTA, read by peers
+};
+
+// Kernels launched with clusters: also each warp's LayerNorm state
+// (count, sum, M2, -), read by peers when the cluster has at most 32 warps.
+struct RowReduceSmemCl : RowReduceSmem {
+    static constexpr bool kWarpStates = true;
+    float4 warp_state[2][32];  // [stage][warp]
 };
 
 // Sums of a pair per thread over the CTA (no cluster): butterflies in each
@@ -623,8 +631,8 @@ __device__ __forceinline__ float row_sum(RowReduceSmem& red, int stage, float v,
 // this CTA's slot is written again or the CTA exits, so that the wait
 // costs nothing once the peers are past their own reads (a full barrier
 // there would wait for the slowest peer's whole output pass).
-template <bool LN, bool EARLY = false>
-__device__ __forceinline__ void row_stats(RowReduceSmem& red, float n_t, float sum_t, float mean_t, float m2_t,
+template <bool LN, bool EARLY = false, class Red>
+__device__ __forceinline__ void row_stats(Red& red, float n_t, float sum_t, float mean_t, float m2_t,
                                           float ss_t, float invN, float eps, uint32_t C, int nwarps, int wwidth,
                                           int stage, float& mu, float& rs) {
     if constexpr (LN) {
@@ -633,6 +641,32 @@ __device__ __forceinline__ void row_stats(RowReduceSmem& red, float n_t, float s
             const float d = mean_t - mu;
             const float m2 = row_sum(red, 1, fmaf(n_t * d, d, m2_t), 1u, nwarps, wwidth);
             rs = rsqrtf(m2 * invN + eps);
+        } else if (Red::kWarpStates && nwarps * static_cast<int>(C) <= 32) {
+            // At most 32 warps in the cluster: every warp merges its lanes'
+            // states with butterflies and publishes its own (n, sum, M2);
+            // one exchange through distributed shared memory then hands
+            // lane l of every warp the state of warp l % nwarps of CTA
+            // l / nwarps, and the warp merges the cluster's warp states by
+            // the same rule. One barrier per row and no CTA-level pass.
+            if constexpr (Red::kWarpStates) {
+                const int lane = threadIdx.x & 31;
+                const float n_w = group_sum(n_t, 32);
+                const float s_w = group_sum(sum_t, 32);
+                const float dw = mean_t - (n_w > 0.f ? s_w / n_w : 0.f);
+                const float m2_w = group_sum(fmaf(n_t * dw, dw, m2_t), 32);
+                if (lane == 0) red.warp_state[stage][threadIdx.x >> 5] = make_float4(n_w, s_w, m2_w, 0.f);
+                cluster_barrier();
+                float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (lane < nwarps * static_cast<int>(C))
+                    q = ld_peer_f32x4(peer_smem_addr(&red.warp_state[stage][lane % nwarps],
+                                                     static_cast<uint32_t>(lane / nwarps)));
+                mu = group_sum(q.y, 32) * invN;
+                const float dq = (q.x > 0.f ? q.y / q.x : 0.f) - mu;
+                const float m2 = group_sum(fmaf(q.x * dq, dq, q.z), 32);
+                // every peer value consumed, the warp converged by the shuffles
+                if constexpr (EARLY) cluster_arrive();  // the caller waits
+                rs = rsqrtf(m2 * invN + eps);
+            }
         } else {
             const float2 sn = cta_sum2(red, sum_t, n_t, nwarps, wwidth);  // this CTA's sum of x - K, count
             const float mean_c = sn.y > 0.f ? sn.x / sn.y : 0.f;
@@ -765,7 +799,7 @@ template <class T, int VEC, int V, bool LN, bool CL, bool ADD, bool Q8, bool SHI
 __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(const NormArgs a) {
     using S = Slice<T, VEC, V, LN>;
     using SO = ScalarOps<T>;
-    __shared__ RowReduceSmem red;
+    __shared__ std::conditional_t<CL, RowReduceSmemCl, RowReduceSmem> red;
 
     if constexpr (!ADD && VEC > 1) {
         // L2 prefetch of this CTA's share of the row a.group - 1 rows after
@@ -1106,7 +1140,7 @@ __global__ void __launch_bounds__(kRingMaxThreads) norm_fwd_ring(const NormArgs 
     using S = WideSlice<T, V, LN>;
     // [stages][V*T] 16-byte slots | [stages] first 16 bytes of the row | [stages] mbarriers
     extern __shared__ __align__(128) uint4 ring[];
-    __shared__ RowReduceSmem red;
+    __shared__ std::conditional_t<CL, RowReduceSmemCl, RowReduceSmem> red;
 
     const int stages = a.stages;
     const int T_ = blockDim.x;
