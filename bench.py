@@ -79,9 +79,10 @@ def measured_peak():
 # capture summarised in profiles/ (workload -> (kernel source hash at capture,
 # bytes per launch, summary file)).
 NCU_TRAFFIC = {
-    "rms_f32_8192x4096": ("9734921bab6fa0dd", 207_655_680, "profiles/norm_fwd_cta_rms_f32_8192x4096.md"),
-    "ln_bf16_4096x8192_outliers": ("9734921bab6fa0dd", 85_753_088, "profiles/norm_fwd_cta_ln_bf16_4096x8192.md"),
-    "ln_f32_8192x5001": ("9734921bab6fa0dd", 278_236_416, "profiles/norm_fwd_cta_shift_ln_f32_8192x5001.md"),
+    "rms_f32_8192x4096": ("5a1182033b41c6d5", 207_114_496, "profiles/norm_fwd_cta_rms_f32_8192x4096.md"),
+    "ln_bf16_4096x8192_outliers": ("5a1182033b41c6d5", 85_719_552, "profiles/norm_fwd_cta_ln_bf16_4096x8192.md"),
+    "ln_f32_8192x5001": ("5a1182033b41c6d5", 278_216_960, "profiles/norm_fwd_cta_shift_ln_f32_8192x5001.md"),
+    "ln_f32_2048x65536": ("5a1182033b41c6d5", 1_033_014_528, "profiles/norm_fwd_cta_ln_f32_2048x65536.md"),
 }
 
 
