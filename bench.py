@@ -56,14 +56,42 @@ def parse_args():
 FWD_KERNEL_SOURCES = ("norm_kernels.cuh", "norm_device.cuh", "norm_args.h")
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments and with runs of whitespace
+    collapsed (string and character literals kept as written), so that the
+    hash below follows the code and not its commentary."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the forward kernel sources' code (comments and layout
+    ignored): a traffic figure taken at one hash holds for any source with
+    the same code."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "row_wise_normalization_ln_gb300", "csrc")
-    files = [os.path.join(csrc, f) for f in FWD_KERNEL_SOURCES]
-    for f in files:
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode())
-            h.update(fh.read())
+    for f in FWD_KERNEL_SOURCES:
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode())
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -79,10 +107,10 @@ def measured_peak():
 # capture summarised in profiles/ (workload -> (kernel source hash at capture,
 # bytes per launch, summary file)).
 NCU_TRAFFIC = {
-    "rms_f32_8192x4096": ("5a1182033b41c6d5", 207_114_496, "profiles/norm_fwd_cta_rms_f32_8192x4096.md"),
-    "ln_bf16_4096x8192_outliers": ("5a1182033b41c6d5", 85_719_552, "profiles/norm_fwd_cta_ln_bf16_4096x8192.md"),
-    "ln_f32_8192x5001": ("5a1182033b41c6d5", 278_216_960, "profiles/norm_fwd_cta_shift_ln_f32_8192x5001.md"),
-    "ln_f32_2048x65536": ("5a1182033b41c6d5", 1_033_014_528, "profiles/norm_fwd_cta_ln_f32_2048x65536.md"),
+    "rms_f32_8192x4096": ("46ce0b042e1bfeb1", 207_114_496, "profiles/norm_fwd_cta_rms_f32_8192x4096.md"),
+    "ln_bf16_4096x8192_outliers": ("46ce0b042e1bfeb1", 85_719_552, "profiles/norm_fwd_cta_ln_bf16_4096x8192.md"),
+    "ln_f32_8192x5001": ("46ce0b042e1bfeb1", 278_216_960, "profiles/norm_fwd_cta_shift_ln_f32_8192x5001.md"),
+    "ln_f32_2048x65536": ("46ce0b042e1bfeb1", 1_033_014_528, "profiles/norm_fwd_cta_ln_f32_2048x65536.md"),
 }
 
 

@@ -618,14 +618,16 @@ __device__ __forceinline__ float row_sum(RowReduceSmem& red, int stage, float v,
 // Row statistics from each thread's Welford state (LayerNorm) or sum of
 // squares (RMSNorm): the shifted mean mu and rstd, identical in every thread
 // of every CTA of the cluster. LayerNorm, one CTA per row: the k-way merge
-// of the threads' states, two sums. LayerNorm over a cluster: each CTA
-// first merges its threads' states into its own (n_c, mean_c, M2_c), then
-// one exchange through distributed shared memory gives every thread the C
-// CTA states, merged in rank order by the same rule ([Ch7] §7.4.1): one
-// cluster barrier per row instead of two (measured 12 % on 65536-wide
-// rows). `stage`: the stage of RMSNorm's one sum, and of the CTA state a
-// LayerNorm cluster publishes (callers that walk several rows per CTA
-// alternate it or put a barrier between rows).
+// of the threads' states, two sums. LayerNorm over a cluster, one cluster
+// barrier per row: with at most 32 warps in the cluster (every default
+// plan), each warp merges its lanes' states and publishes its own, and every
+// warp merges all the cluster's warp states after the exchange; with more,
+// each CTA first merges its threads' states into its own (n_c, mean_c,
+// M2_c) and every thread merges the C CTA states in rank order. Both use
+// the merge rule of [Ch7] §7.4.1 in its k-way form. `stage`: the stage of
+// RMSNorm's one sum, and of the states a LayerNorm cluster publishes
+// (callers that walk several rows per CTA alternate it or put a barrier
+// between rows).
 // EARLY (C > 1 only): each thread arrives at the next cluster barrier as
 // soon as it has read the peers' values, and the caller waits on it before
 // this CTA's slot is written again or the CTA exits, so that the wait
