@@ -481,3 +481,14 @@ def test_host_pipeline_refuses_unpinned_tensors():
         rn.host_rows_pipeline([x], [torch.zeros(4, 8)], lambda i, o: None)
     with pytest.raises(ValueError):
         rn.host_rows_pipeline([], [x], lambda i, o: None)
+    with pytest.raises(ValueError):  # row counts differ
+        rn.host_rows_pipeline([x], [torch.zeros(3, 8)], lambda i, o: None)
+    with pytest.raises(ValueError):  # not contiguous
+        rn.host_rows_pipeline([torch.zeros(8, 4).t()], [x], lambda i, o: None)
+
+
+def test_host_pipeline_zero_rows_is_a_no_op():
+    # nothing to copy: returns before any device work or pinning check
+    calls = []
+    assert rn.host_rows_pipeline([torch.zeros(0, 8)], [torch.zeros(0, 8)], lambda i, o: calls.append(1)) is None
+    assert calls == []
