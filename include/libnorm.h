@@ -60,7 +60,9 @@ typedef enum {
     NORM_ERR_ARG = -1,    /* bad size, NULL pointer or eps */
     NORM_ERR_DTYPE = -2,  /* dtype not one of norm_dtype */
     NORM_ERR_CUDA = -3,   /* CUDA runtime error (device query or launch) */
-    NORM_ERR_PLAN = -4    /* an explicit plan is inconsistent with the call */
+    NORM_ERR_PLAN = -4,   /* an explicit plan is inconsistent with the call */
+    NORM_ERR_TIMEOUT = -5 /* norm_synchronize: a ring kernel's wait for a
+                             bulk copy ran out; those calls' outputs are void */
 } norm_status;
 
 /* How rows map onto the GPU. */
@@ -298,7 +300,8 @@ norm_status rms_bwd_planned(const void* dy, const void* x, const void* w, void* 
  * ln_bwd refuses.
  * The first call on each device looks up that array's device address (with
  * the device current) and the SM count; make that first call before any
- * stream capture. Nothing in the array needs to start at zero: each call
+ * stream capture. The address is kept for the life of the process: a
+ * cudaDeviceReset while the library is loaded is not supported. Nothing in the array needs to start at zero: each call
  * writes every partial row before reading it. All calls on a device share
  * the array, so calls that overlap on the GPU (on different streams, or
  * from different threads) race and corrupt each other's column gradients:
@@ -363,13 +366,43 @@ int norm_last_cuda_error(void);
 int norm_abi_version(void);
 
 /*
- * The ring kernels (forward and backward plans with `stages` >= 2) wait for
- * their bulk copies with a time limit (2 s); a wait that runs out is counted on the device
- * and the call's outputs are then not to be trusted. Reads the current
- * device's count into *count and resets it to 0 (synchronises the device).
- * NORM_ERR_ARG if count is NULL; NORM_ERR_CUDA on a runtime error.
+ * Bounded waits. The only kernels that poll are the ring kernels (forward
+ * plans with `stages` >= 2, and the backward plans norm_bwd_make_plan picks
+ * for fp32 rows): a CTA waits for each bulk copy of an upcoming row on an
+ * mbarrier, for at most the device's wait limit (2 s by default). When a
+ * wait runs out, the whole CTA stops waiting and copying, gives the copies
+ * it still has in flight one more wait of 2 s each (so that none lands in
+ * the shared memory of a CTA that has gone), finishes and adds 1 to a count
+ * on the device. The call's outputs are then void. Calls are asynchronous,
+ * so they cannot return the timeout themselves: the caller asks afterwards.
+ * The count and the limit belong to the current device; all calls on a
+ * device share them. A cudaDeviceReset while the library is loaded is not
+ * supported (the device address of that state is looked up once per device
+ * and process).
  */
+
+/* Reads the current device's count into *count and resets it to 0
+ * (synchronises the device). NORM_ERR_ARG if count is NULL; NORM_ERR_CUDA on
+ * a runtime error. */
 norm_status norm_wait_timeouts(uint32_t* count);
+
+/* Synchronises the current device and reports whether any ring wait ran out
+ * since the last check: NORM_ERR_TIMEOUT if one did (and resets the count),
+ * NORM_OK if none did, NORM_ERR_CUDA on a runtime error (for example one a
+ * kernel raised). */
+norm_status norm_synchronize(void);
+
+/* Sets the current device's limit for the ring kernels' per-row waits, in
+ * nanoseconds, for kernels launched after the call returns (synchronous;
+ * call it while no ring kernel runs on the device). 0 makes every wait test
+ * its copy once and give up if it has not landed yet (a way to exercise the
+ * timeout path); the waits for copies in flight before a CTA exits keep
+ * their own 2 s. NORM_ERR_ARG above 60 s (6e10 ns). */
+norm_status norm_set_wait_limit(uint64_t ns);
+
+/* The current device's per-row wait limit in nanoseconds (NORM_ERR_ARG if
+ * ns is NULL). */
+norm_status norm_wait_limit(uint64_t* ns);
 
 #ifdef __cplusplus
 }

@@ -26,7 +26,7 @@ __all__ = [
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnorm.so")
 
 NORM_F32, NORM_BF16, NORM_F16 = 0, 1, 2
-NORM_OK, NORM_ERR_ARG, NORM_ERR_DTYPE, NORM_ERR_CUDA, NORM_ERR_PLAN = 0, -1, -2, -3, -4
+NORM_OK, NORM_ERR_ARG, NORM_ERR_DTYPE, NORM_ERR_CUDA, NORM_ERR_PLAN, NORM_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
 NORM_MAP_GROUP, NORM_MAP_CTA = 0, 1
 
 
@@ -112,9 +112,13 @@ def library() -> ctypes.CDLL:
               "ln_bwd", "rms_bwd", "ln_bwd_planned", "rms_bwd_planned", "norm_bwd_make_plan",
               "norm_bwd_workspace_bytes", "ln_fwd_fp8", "rms_fwd_fp8", "ln_fwd_add_fp8", "rms_fwd_add_fp8",
               "ln_fwd_fp8_planned", "rms_fwd_fp8_planned", "ln_fwd_strided", "rms_fwd_strided",
-              "norm_last_cuda_error", "norm_abi_version", "norm_wait_timeouts"):
+              "norm_last_cuda_error", "norm_abi_version", "norm_wait_timeouts", "norm_synchronize",
+              "norm_set_wait_limit", "norm_wait_limit"):
         getattr(L, f).restype = ctypes.c_int
     L.norm_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    L.norm_synchronize.argtypes = []
+    L.norm_set_wait_limit.argtypes = [ctypes.c_uint64]
+    L.norm_wait_limit.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
     L.norm_status_string.argtypes = [ctypes.c_int]
     L.norm_status_string.restype = ctypes.c_char_p
     _lib = L
@@ -130,6 +134,33 @@ def wait_timeouts() -> int:
     if st != NORM_OK:
         raise NormError(st, "norm_wait_timeouts")
     return n.value
+
+
+def synchronize() -> None:
+    """Synchronise the current device and raise NormError (status
+    NORM_ERR_TIMEOUT) if a ring kernel's wait for a bulk copy ran out since
+    the last check; the count is reset either way."""
+    st = library().norm_synchronize()
+    if st != NORM_OK:
+        raise NormError(st, "norm_synchronize")
+
+
+def set_wait_limit(ns: int) -> None:
+    """Time limit, in nanoseconds, of the ring kernels' per-row waits on the
+    current device (default 2e9; 0 tests each copy once and gives up if it
+    has not landed; at most 6e10). Applies to kernels launched afterwards."""
+    st = library().norm_set_wait_limit(int(ns))
+    if st != NORM_OK:
+        raise NormError(st, "norm_set_wait_limit")
+
+
+def wait_limit() -> int:
+    """The current device's per-row wait limit in nanoseconds."""
+    v = ctypes.c_uint64(0)
+    st = library().norm_wait_limit(ctypes.byref(v))
+    if st != NORM_OK:
+        raise NormError(st, "norm_wait_limit")
+    return v.value
 
 
 def _dtype_code(t: torch.dtype) -> int:

@@ -310,8 +310,11 @@ norm_status bwd_check_plan(const norm_plan& in, int64_t M, int64_t N, norm_dtype
     if (p.vec_elems != 1) {
         if (p.vec_elems != 16 / s || !all_aligned || (N * s) % 16 != 0) return NORM_ERR_PLAN;
     }
-    // stages 2..4: the ring of upcoming rows in shared memory (vector rows)
-    if (p.stages != 0 && (p.stages < 2 || p.stages > kMaxStages || p.vec_elems == 1)) return NORM_ERR_PLAN;
+    // stages 1: the register pipeline (a CTA per row); 2..4: the ring of
+    // upcoming rows in shared memory (vector rows)
+    if (p.stages == 1 && p.cluster != 1) return NORM_ERR_PLAN;
+    if (p.stages != 0 && p.stages != 1 && (p.stages < 2 || p.stages > kMaxStages || p.vec_elems == 1))
+        return NORM_ERR_PLAN;
     if (libnorm::bwd_smem_bytes(ln, p.threads, p.per_thread, p.vec_elems, p.stages) > kMaxSmem) return NORM_ERR_PLAN;
     if (!is_pow2(p.per_thread) || p.per_thread > bwd_vmax(ln, dtype, p.vec_elems)) return NORM_ERR_PLAN;
     if (p.threads < 32 || p.threads > kBwdMaxThreads || p.threads % 32 != 0) return NORM_ERR_PLAN;
@@ -716,6 +719,7 @@ const char* norm_status_string(norm_status s) {
         case NORM_ERR_DTYPE: return "unsupported dtype";
         case NORM_ERR_CUDA: return "CUDA runtime error (see norm_last_cuda_error)";
         case NORM_ERR_PLAN: return "plan inconsistent with the call";
+        case NORM_ERR_TIMEOUT: return "a ring kernel's wait for a bulk copy ran out (outputs void)";
         default: return "unknown status";
     }
 }

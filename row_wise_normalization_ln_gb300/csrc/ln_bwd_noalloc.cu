@@ -18,8 +18,10 @@ namespace {
 constexpr size_t kScratchFloats = size_t(1) << 20;
 static __device__ __align__(256) float g_scratch[kScratchFloats];
 
-// Device address of g_scratch and SM count, per device. In host code the
-// name g_scratch is only a stand-in for the symbol, never a device address.
+// Device address of g_scratch and SM count, per device, looked up once per
+// device and process (a cudaDeviceReset while the library is loaded is not
+// supported). In host code the name g_scratch is only a stand-in for the
+// symbol, never a device address.
 struct DeviceScratch {
     float* ptr;
     int sms;
@@ -67,8 +69,13 @@ extern "C" norm_status ln_bwd_noalloc(const void* dy, const void* x, const void*
                                       const float* rstd, void* dx, float* dgamma, float* dbeta, int64_t M,
                                       int64_t N, norm_dtype dtype, cudaStream_t stream) {
     const int al = aligned16(dy) && aligned16(x) && aligned16(gamma) && aligned16(dx);
-    // Sizes first, on the host: the backward's own limits, then the scratch
-    // limit (one partial row of dgamma and dbeta must fit).
+    // Every argument check on the host before any CUDA call: the pointers
+    // ln_bwd requires, the backward's own size limits, then the scratch
+    // limit (one partial row of dgamma and dbeta must fit; the backward
+    // refuses every N for which this guard could fail, so it only states the
+    // array's bound).
+    if (!dgamma || !dbeta) return NORM_ERR_ARG;
+    if (M > 0 && (!dy || !x || !gamma || !dx || !mean || !rstd)) return NORM_ERR_ARG;
     norm_plan plan;
     norm_status st = norm_bwd_make_plan(M, N, dtype, 1, al, 1, &plan);
     if (st != NORM_OK) return st;

@@ -14,6 +14,24 @@ namespace libnorm {
 // leaves each thread.
 constexpr int kFusedMaxThreads = 512;
 
+// Per-device state of the ring kernels' bounded waits (one instance per
+// device, in device memory): the count of CTAs whose wait for a bulk copy
+// gave up, and the time limit of the per-row waits. The host reads and
+// resets the count (norm_wait_timeouts, norm_synchronize) and sets the limit
+// (norm_set_wait_limit).
+struct WaitState {
+    unsigned int timeouts;
+    unsigned int pad;
+    unsigned long long limit_ns;
+};
+
+// Default limit of a per-row wait, and the fixed limit of the waits a CTA
+// makes before it exits for copies still in flight (those always get the
+// full time, so that no copy lands in the shared memory of a CTA that has
+// gone).
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
+constexpr unsigned long long kMaxWaitLimitNs = 60000000000ull;
+
 struct NormArgs {
     const void* x;      // [M, N], row pitch ldx
     const void* gamma;  // [N] (LayerNorm gamma, RMSNorm w)
@@ -34,7 +52,7 @@ struct NormArgs {
     int16_t vec_params = 1;  // gamma (and beta) 16-byte aligned
     int64_t ldx = 0;         // row pitch of x in elements (set to N for contiguous rows)
     int64_t ldy = 0;         // row pitch of y in elements (bytes for an FP8 y)
-    unsigned int* wait_timeouts = nullptr;  // ring kernels: device counter of waits that gave up
+    WaitState* wait = nullptr;  // ring kernels: this device's wait limit and count of waits that gave up
 };
 // Kept at 128 bytes: a larger argument block made ptxas spill the 64-register
 // long-row kernels.
@@ -59,8 +77,8 @@ struct BwdArgs {
     int32_t N;
     float eps;            // RMSNorm (rstd is recomputed from x)
     int32_t row_cluster;  // CTAs per row
-    int32_t stages = 0;   // ring kernels: shared-memory stages of upcoming rows (0: none)
-    unsigned int* wait_timeouts = nullptr;  // ring kernels: device counter of waits that gave up
+    int32_t stages = 0;   // 1: register pipeline; 2..4: shared-memory stages of upcoming rows; 0: neither
+    WaitState* wait = nullptr;  // ring and pipeline kernels: this device's wait limit and count of waits that gave up
 };
 
 constexpr int kBwdMaxThreads = 512;
@@ -79,16 +97,17 @@ inline int64_t ring_smem_bytes(int stages, int per_thread, int threads) {
     return int64_t(stages) * (int64_t(per_thread) * threads * 16 + 16 + 8);
 }
 
-// Device address of the current device's counter of ring-kernel waits that
-// gave up (norm_wait_timeouts reads it); null if it cannot be resolved.
-unsigned int* wait_counter(int dev);
+// Device address of the current device's WaitState (the ring kernels' wait
+// limit and count); null if it cannot be resolved.
+WaitState* wait_state(int dev);
 
 // Dynamic shared memory of a backward launch: the column accumulators
 // ([2 for LayerNorm | 1][threads * per_thread * vec] fp32), then, for a ring
-// (stages > 0), per stage two slices of 16-byte slots (x, dy) and an 8-byte
+// (stages >= 2), per stage two slices of 16-byte slots (x, dy) and an 8-byte
 // mbarrier.
 inline int64_t bwd_smem_bytes(bool ln, int threads, int per_thread, int vec, int stages) {
-    return int64_t(ln ? 2 : 1) * threads * per_thread * vec * 4 + int64_t(stages) * (2 * int64_t(threads) * per_thread * 16 + 8);
+    const int64_t ring = stages >= 2 ? stages : 0;  // stages 1, the register pipeline, keeps no rows here
+    return int64_t(ln ? 2 : 1) * threads * per_thread * vec * 4 + ring * (2 * int64_t(threads) * per_thread * 16 + 8);
 }
 
 // Partial rows of the column gradients a backward plan produces (one per

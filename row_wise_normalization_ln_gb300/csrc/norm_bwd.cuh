@@ -121,148 +121,55 @@ __device__ __forceinline__ float2 row_sum2(PairReduceSmem& red, int stage, float
     return w;
 }
 
-// ------------------------------------------------------------ main kernel
-// Layout as the forward's CTA mapping: CTA rank k of a row's cluster holds
-// accesses [k*V*T, (k+1)*V*T), warp-major. Launched as clusters of Q CTAs:
-// Q == row_cluster when a row spans a cluster; with row_cluster == 1 the Q
-// CTAs of a cluster each take their own rows and meet only at the end.
+// ------------------------------------------------------------ row arithmetic
+// The per-row work of a thread, shared by the backward kernels: its gamma
+// (w) slice, its column accumulators and the two passes over one row's
+// accesses (the pair of row sums; then dx and the column terms).
 //
-// Each thread keeps gamma (w) of its columns in registers for the whole
-// kernel. Rows two steps ahead are prefetched into L2 (bulk, by one thread),
-// so a row's own loads are L2 hits while HBM already serves the rows after
-// it. (Loads into registers issued a row ahead did not overlap: the row's
-// block barrier waits for them.) The column accumulators live in registers
-// (in this thread's shared-memory slots for the 16-bit variants of 4
-// accesses per thread); at the end they sit in dynamic shared memory,
-// [NA][T*V*VEC] floats, each thread at the positions of its own columns.
-template <class T, int VEC, int V, bool LN, bool RING>
-__global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) {
-    static_assert(!RING || VEC > 1, "the ring moves 16-byte vectors");
+// The column accumulators live in registers (in this thread's shared-memory
+// slots for the 16-bit variants of 4 accesses per thread); at the end they
+// go to dynamic shared memory, [NA][T*V*VEC] floats, each thread at the
+// positions of its own columns.
+template <class T, int VEC, int V, bool LN>
+struct BwdRow {
     using O = OpsFor<T, VEC>;
     using E = BwdElem<T, VEC>;
     using Raw = typename O::Raw;
-    constexpr int NA = LN ? 2 : 1;
-    __shared__ PairReduceSmem red;
-    extern __shared__ float4 acc_v[];
-    float* acc_s = reinterpret_cast<float*>(acc_v);
-
-    const int T_ = blockDim.x;
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
-    const int nwarps = T_ >> 5;
-    int wwidth = 1;
-    while (wwidth < nwarps) wwidth <<= 1;
-    const uint32_t Q = cluster_size();
-    const uint32_t crank = cluster_rank();
-    const int C = a.row_cluster;
-    const int rank = C > 1 ? static_cast<int>(crank) : 0;
-    const int64_t first_row = C > 1 ? blockIdx.x / C : blockIdx.x;
-    const int64_t row_step = C > 1 ? gridDim.x / C : gridDim.x;
-    const int N = a.N;
-    const int nacc = (N + VEC - 1) / VEC;
-    const int stride = 32 * VEC;
-    const int local = warp * V * 32 + lane;  // first access within this CTA's slice
-    const int f0 = rank * V * T_ + local;    // ... within the row
-    const int nv = valid_runs(nacc, f0, 32, V);
-    const float invN = 1.f / static_cast<float>(N);
-    const int slice = T_ * V * VEC;  // floats per accumulator array
-    float* my_acc = acc_s + local * VEC;
-    // RING: after the accumulators, `stages` stages of this CTA's slices of
-    // an upcoming row, x then dy (V*T 16-byte slots each), then one mbarrier
-    // per stage.
-    const int stages = RING ? a.stages : 0;
-    uint4* ring = reinterpret_cast<uint4*>(acc_s + NA * slice);
-    uint64_t* full = reinterpret_cast<uint64_t*>(ring + 2 * stages * V * T_);
-
-    // Column accumulators in registers where they fit beside the row data
-    // (all but the 16-bit variants of 4 accesses per thread); otherwise in
-    // this thread's shared-memory slots.
-    constexpr bool ACC_REG = !(VEC == 8 && V >= 4);
-    float acc[ACC_REG ? NA : 1][ACC_REG ? V : 1][ACC_REG ? VEC : 1];
-#pragma unroll
-    for (int k = 0; k < (ACC_REG ? NA : 1); ++k)
-#pragma unroll
-        for (int j = 0; j < (ACC_REG ? V : 1); ++j)
-#pragma unroll
-            for (int e = 0; e < (ACC_REG ? VEC : 1); ++e) acc[k][j][e] = 0.f;
-    // Shared-memory accumulator slots start at zero.
-#pragma unroll
-    for (int k = 0; k < (ACC_REG ? 0 : NA); ++k)
-#pragma unroll
-        for (int j = 0; j < V; ++j)
-#pragma unroll
-            for (int e = 0; e < VEC; e += (VEC % 4 == 0 ? 4 : 1)) {
-                float* d = my_acc + k * slice + j * 32 * VEC + e;
-                if constexpr (VEC % 4 == 0)
-                    *reinterpret_cast<float4*>(d) = make_float4(0.f, 0.f, 0.f, 0.f);
-                else
-                    *d = 0.f;
-            }
-
-    // Rows ahead go to L2 by bulk prefetch: this CTA's contiguous slice of x
-    // and dy (16-byte vector rows only) and the row's statistics, issued by
-    // one thread, two rows ahead of the row being worked on.
-    const int64_t cta_first = static_cast<int64_t>(rank) * V * T_ * VEC;  // first element of the CTA's slice
-    const uint32_t slice_bytes = static_cast<uint32_t>(
-        (cta_first < N ? min(static_cast<int64_t>(V) * T_ * VEC, N - cta_first) : 0) * sizeof(T));
-    auto prefetch_row = [&](int64_t r) {
-        if (r >= a.M) return;
-        if constexpr (VEC > 1) {
-            if (slice_bytes > 0) {
-                prefetch_l2_bulk(static_cast<const T*>(a.x) + r * N + cta_first, slice_bytes);
-                prefetch_l2_bulk(static_cast<const T*>(a.dy) + r * N + cta_first, slice_bytes);
-            }
-        }
-        if constexpr (LN) {
-            prefetch_l2_line(a.mean + r);
-            prefetch_l2_line(a.rstd + r);
-        }
-    };
-    // Rows are prefetched `ahead` rows before their turn: 2 without a ring;
-    // with one, one row beyond those in the ring, so that each bulk copy
-    // into the ring reads L2. The first rows are requested before the
-    // dependent-launch wait, overlapping the previous grid's tail (a
-    // prefetch only moves data towards L2, where that grid's writes land).
-    const int ahead = RING ? stages + 1 : 2;
-    if (tid == 0)
-        for (int k = 0; k < ahead; ++k) prefetch_row(first_row + k * row_step);
-    if constexpr (RING) {
-        if (tid == 0) {
-            for (int k = 0; k < stages; ++k) mbar_init(&full[k], 1);
-            mbar_init_fence();
-        }
-        __syncthreads();
-    }
-
-    grid_release();
-    grid_wait();
-
-    // RING, thread 0: fill stage `st` with this CTA's slices of x and dy of
-    // row `r` (copies read memory: only after the wait above).
-    auto issue = [&](int64_t r, int st) {
-        mbar_arrive_expect(&full[st], 2u * slice_bytes);
-        if (slice_bytes > 0) {
-            bulk_load(ring + (2 * st) * V * T_, static_cast<const T*>(a.x) + r * N + cta_first, slice_bytes,
-                      &full[st]);
-            bulk_load(ring + (2 * st + 1) * V * T_, static_cast<const T*>(a.dy) + r * N + cta_first, slice_bytes,
-                      &full[st]);
-        }
-    };
-    if constexpr (RING) {
-        if (tid == 0)
-            for (int k = 0; k < stages; ++k)
-                if (first_row + k * row_step < a.M) issue(first_row + k * row_step, k);
-    }
-
+    using P = typename PairOf<T>::type;
+    static constexpr int NA = LN ? 2 : 1;
     // 16-bit rows work on fp32 pairs with the packed instructions and keep
     // gamma widened (gf); other rows work on scalars.
-    constexpr bool PAIRS = VEC == 8;
-    using P = typename PairOf<T>::type;
+    static constexpr bool PAIRS = VEC == 8;
+    static constexpr bool ACC_REG = !(VEC == 8 && V >= 4);
+
     Raw gv[V];
     float2 gf[PAIRS ? V : 1][4];
-    {
-        const T* gp = static_cast<const T*>(a.gamma) + f0 * VEC;
+    float acc[ACC_REG ? NA : 1][ACC_REG ? V : 1][ACC_REG ? VEC : 1];
+    float* my_acc;  // this thread's first accumulator slot in shared memory
+    int slice;      // floats per shared-memory accumulator array
+
+    __device__ __forceinline__ void init(const T* gp, int stride, int nv, float* acc_slot, int slice_floats) {
+        my_acc = acc_slot;
+        slice = slice_floats;
+#pragma unroll
+        for (int k = 0; k < (ACC_REG ? NA : 1); ++k)
+#pragma unroll
+            for (int j = 0; j < (ACC_REG ? V : 1); ++j)
+#pragma unroll
+                for (int e = 0; e < (ACC_REG ? VEC : 1); ++e) acc[k][j][e] = 0.f;
+        // Shared-memory accumulator slots start at zero.
+#pragma unroll
+        for (int k = 0; k < (ACC_REG ? 0 : NA); ++k)
+#pragma unroll
+            for (int j = 0; j < V; ++j)
+#pragma unroll
+                for (int e = 0; e < VEC; e += (VEC % 4 == 0 ? 4 : 1)) {
+                    float* d = my_acc + k * slice + j * 32 * VEC + e;
+                    if constexpr (VEC % 4 == 0)
+                        *reinterpret_cast<float4*>(d) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    else
+                        *d = 0.f;
+                }
 #pragma unroll
         for (int j = 0; j < V; ++j)
             if (j < nv) {
@@ -273,41 +180,12 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
                 }
             }
     }
-    const T* xbase = static_cast<const T*>(a.x) + f0 * VEC;
-    const T* dybase = static_cast<const T*>(a.dy) + f0 * VEC;
 
-    int it = 0;
-    int st = 0;            // RING: this row's stage
-    uint32_t parity = 0;   // ... and the phase parity to wait for
-    int64_t late = -1;     // RING: the row (count) whose wait ran out, if any
-    for (int64_t row = first_row; row < a.M; row += row_step, ++it) {
-        if (tid == 0) prefetch_row(row + ahead * row_step);
-        Raw xv[V], dv[V];
-        if constexpr (RING) {
-            // After one wait has run out this CTA neither waits nor copies
-            // any more (its outputs are void by then); the kernel still ends.
-            if (late < 0 && !mbar_wait(&full[st], parity)) late = it;
-            const uint4* xs = ring + (2 * st) * V * T_ + local;
-            const uint4* ds = xs + V * T_;
-#pragma unroll
-            for (int j = 0; j < V; ++j)
-                if (j < nv) {
-                    xv[j] = xs[j * 32];
-                    dv[j] = ds[j * 32];
-                }
-        } else {
-#pragma unroll
-            for (int j = 0; j < V; ++j)
-                if (j < nv) {
-                    xv[j] = O::load(xbase + row * N + j * stride);
-                    dv[j] = O::load(dybase + row * N + j * stride);
-                }
-        }
-        float mu = 0.f, rs = 0.f;
-        if constexpr (LN) {
-            mu = a.mean[row];
-            rs = a.rstd[row];
-        }
+    // This thread's share of the row's pair of sums: LayerNorm (sum g,
+    // sum g * xhat) with g = dy * gamma, xhat = (x - mean) * rstd; RMSNorm
+    // (sum x^2, sum dy * w * x).
+    __device__ __forceinline__ float2 partials(const Raw (&xv)[V], const Raw (&dv)[V], int nv, float mu,
+                                               float rs) const {
         float s0 = 0.f, s1 = 0.f;
         if constexpr (PAIRS) {
             const float2 nmu = f2_splat(-mu), rs2 = f2_splat(rs);
@@ -351,23 +229,19 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
                     }
                 }
         }
-        const float2 S = row_sum2(red, it & 1, make_float2(s0, s1), C, nwarps, wwidth);
-        if constexpr (RING) {
-            // Every thread has read this stage before the barrier above:
-            // refill it with the row `stages` turns ahead.
-            if (tid == 0 && late < 0 && row + stages * row_step < a.M) {
-                fence_proxy_async();
-                issue(row + stages * row_step, st);
-            }
-            if (++st == stages) st = 0, parity ^= 1u;
-        }
-        T* dxr = static_cast<T*>(a.dx) + row * N + f0 * VEC;
+        return make_float2(s0, s1);
+    }
+
+    // dx of the row from its pair of sums S, stored at dxr (this thread's
+    // first access), and the row's terms added to the column accumulators.
+    __device__ __forceinline__ void output(const Raw (&xv)[V], const Raw (&dv)[V], int nv, float mu, float rs,
+                                           float2 S, float invN, float eps, T* dxr, int stride) {
         float c0, c1;  // LayerNorm: mean(g), mean(g xhat); RMSNorm: rstd, rstd^3 mean(dy w x)
         if constexpr (LN) {
             c0 = S.x * invN;
             c1 = S.y * invN;
         } else {
-            c0 = rsqrtf(S.x * invN + a.eps);
+            c0 = rsqrtf(S.x * invN + eps);
             c1 = c0 * c0 * c0 * (S.y * invN);
         }
 #pragma unroll
@@ -387,8 +261,10 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
                             const float2 t = __fadd2_rn(__fmul2_rn(d2, gf[j][i]), nc0);
                             ov = __fmul2_rn(rs2, __ffma2_rn(xh, nc1, t));
                             if constexpr (ACC_REG) {
-                                const float2 ga = __ffma2_rn(d2, xh, make_float2(acc[0][j][2 * i], acc[0][j][2 * i + 1]));
-                                const float2 gb = __fadd2_rn(make_float2(acc[NA - 1][j][2 * i], acc[NA - 1][j][2 * i + 1]), d2);
+                                const float2 ga =
+                                    __ffma2_rn(d2, xh, make_float2(acc[0][j][2 * i], acc[0][j][2 * i + 1]));
+                                const float2 gb =
+                                    __fadd2_rn(make_float2(acc[NA - 1][j][2 * i], acc[NA - 1][j][2 * i + 1]), d2);
                                 acc[0][j][2 * i] = ga.x;
                                 acc[0][j][2 * i + 1] = ga.y;
                                 acc[NA - 1][j][2 * i] = gb.x;
@@ -448,7 +324,8 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
                             float4 v = *reinterpret_cast<float4*>(d + e);
                             if constexpr (PAIRS) {
                                 const float2 lo = __fadd2_rn(make_float2(v.x, v.y), make_float2(p[e], p[e + 1]));
-                                const float2 hi = __fadd2_rn(make_float2(v.z, v.w), make_float2(p[e + 2], p[e + 3]));
+                                const float2 hi =
+                                    __fadd2_rn(make_float2(v.z, v.w), make_float2(p[e + 2], p[e + 3]));
                                 v = make_float4(lo.x, lo.y, hi.x, hi.y);
                             } else {
                                 v.x += p[e];
@@ -466,42 +343,46 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
             }
     }
 
-    if constexpr (RING) {
-        if (late >= 0 && tid == 0) {
-            // Copies still in flight (rows late .. late+stages-1 of this CTA)
-            // get one more bounded wait each, so that none lands after this
-            // CTA has gone; then tell the host.
-            for (int64_t kk = late; kk < late + stages; ++kk)
-                if (first_row + kk * row_step < a.M)
-                    mbar_wait(&full[kk % stages], static_cast<uint32_t>((kk / stages) & 1));
-            atomicAdd(a.wait_timeouts, 1u);
+    // Hand the register accumulators to this thread's shared-memory slots
+    // (column positions), where the column-sum steps expect them.
+    __device__ __forceinline__ void acc_to_smem() const {
+        if constexpr (ACC_REG) {
+#pragma unroll
+            for (int k = 0; k < NA; ++k)
+#pragma unroll
+                for (int j = 0; j < V; ++j) {
+                    float* d = my_acc + k * slice + j * 32 * VEC;
+                    if constexpr (VEC % 4 == 0) {
+#pragma unroll
+                        for (int e = 0; e < VEC; e += 4)
+                            *reinterpret_cast<float4*>(d + e) =
+                                make_float4(acc[k][j][e], acc[k][j][e + 1], acc[k][j][e + 2], acc[k][j][e + 3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) d[e] = acc[k][j][e];
+                    }
+                }
         }
     }
+};
 
-    if constexpr (ACC_REG) {
-        // Hand the register accumulators to this thread's shared-memory
-        // slots (column positions), where the steps below expect them.
-#pragma unroll
-        for (int k = 0; k < NA; ++k)
-#pragma unroll
-            for (int j = 0; j < V; ++j) {
-                float* d = my_acc + k * slice + j * 32 * VEC;
-                if constexpr (VEC % 4 == 0) {
-#pragma unroll
-                    for (int e = 0; e < VEC; e += 4)
-                        *reinterpret_cast<float4*>(d + e) =
-                            make_float4(acc[k][j][e], acc[k][j][e + 1], acc[k][j][e + 2], acc[k][j][e + 3]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) d[e] = acc[k][j][e];
-                }
-            }
-    }
-
-    // Partial rows of the column gradients: one per cluster.
+// The end of every backward kernel: the CTA's column accumulators (in shared
+// memory at acc_s, [NA][slice] floats) become partial rows of the
+// workspace, one per launched cluster of Q CTAs. The CTAs of a row's cluster
+// (C > 1) own distinct columns and write them; the Q CTAs of a reduction
+// cluster (C == 1) own the same columns, and CTA q adds the Q copies of its
+// share of them in rank order. Ends with the cluster's last barrier.
+template <int VEC, int V, int NA>
+__device__ __forceinline__ void write_partials(const BwdArgs& a, const float* acc_s, int slice, int C, int f0, int nv) {
+    const int N = a.N;
+    const int T_ = blockDim.x;
+    const int tid = threadIdx.x;
+    const int local = (tid >> 5) * V * 32 + (tid & 31);
+    const float* my_acc = acc_s + local * VEC;
+    const uint32_t Q = cluster_size();
+    const uint32_t crank = cluster_rank();
     float* wsp = a.ws + static_cast<int64_t>(blockIdx.x / Q) * NA * N;
     if (C > 1 || Q == 1) {
-        // The CTAs of a row's cluster own distinct columns: write them.
 #pragma unroll
         for (int k = 0; k < NA; ++k)
 #pragma unroll
@@ -520,10 +401,6 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
                 }
         if (C > 1) cluster_barrier();  // no CTA exits while a peer may read its shared memory
     } else {
-        // The Q CTAs of this cluster own the same columns (each had its own
-        // rows), held at position = column in every CTA's accumulators: CTA
-        // q of the cluster adds the Q copies of its share of the columns, in
-        // rank order, and writes them.
         cluster_barrier();
         uint32_t peer[8];
 #pragma unroll
@@ -546,23 +423,384 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
     }
 }
 
-// Column sums of the partial rows: out_k[c] = sum over p, in order, of
-// ws[p][k][c]. With no partial rows (M == 0) the gradients are zero.
-template <int NA>
-__global__ void __launch_bounds__(256) norm_bwd_colsum(const float* ws, int64_t partials, int32_t N, float* out0,
-                                                       float* out1) {
+// ------------------------------------------------------------ main kernel
+// Layout as the forward's CTA mapping: CTA rank k of a row's cluster holds
+// accesses [k*V*T, (k+1)*V*T), warp-major. Launched as clusters of Q CTAs:
+// Q == row_cluster when a row spans a cluster; with row_cluster == 1 the Q
+// CTAs of a cluster each take their own rows and meet only at the end.
+//
+// Each thread keeps gamma (w) of its columns in registers for the whole
+// kernel. Rows two steps ahead are prefetched into L2 (bulk, by one thread),
+// so a row's own loads are L2 hits while HBM already serves the rows after
+// it.
+template <class T, int VEC, int V, bool LN, bool RING>
+__global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) {
+    static_assert(!RING || VEC > 1, "the ring moves 16-byte vectors");
+    using R = BwdRow<T, VEC, V, LN>;
+    using O = typename R::O;
+    using Raw = typename R::Raw;
+    constexpr int NA = R::NA;
+    __shared__ PairReduceSmem red;
+    extern __shared__ float4 acc_v[];
+    float* acc_s = reinterpret_cast<float*>(acc_v);
+
+    const int T_ = blockDim.x;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = T_ >> 5;
+    int wwidth = 1;
+    while (wwidth < nwarps) wwidth <<= 1;
+    const int C = a.row_cluster;
+    const int rank = C > 1 ? static_cast<int>(cluster_rank()) : 0;
+    const int64_t first_row = C > 1 ? blockIdx.x / C : blockIdx.x;
+    const int64_t row_step = C > 1 ? gridDim.x / C : gridDim.x;
+    const int N = a.N;
+    const int nacc = (N + VEC - 1) / VEC;
+    const int stride = 32 * VEC;
+    const int local = warp * V * 32 + lane;  // first access within this CTA's slice
+    const int f0 = rank * V * T_ + local;    // ... within the row
+    const int nv = valid_runs(nacc, f0, 32, V);
+    const float invN = 1.f / static_cast<float>(N);
+    const int slice = T_ * V * VEC;  // floats per accumulator array
+    // RING: after the accumulators, `stages` stages of this CTA's slices of
+    // an upcoming row, x then dy (V*T 16-byte slots each), then one mbarrier
+    // per stage.
+    const int stages = RING ? a.stages : 0;
+    uint4* ring = reinterpret_cast<uint4*>(acc_s + NA * slice);
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + 2 * stages * V * T_);
+
+    // Rows ahead go to L2 by bulk prefetch: this CTA's contiguous slice of x
+    // and dy (16-byte vector rows only) and the row's statistics, issued by
+    // one thread, two rows ahead of the row being worked on.
+    const int64_t cta_first = static_cast<int64_t>(rank) * V * T_ * VEC;  // first element of the CTA's slice
+    const uint32_t slice_bytes = static_cast<uint32_t>(
+        (cta_first < N ? min(static_cast<int64_t>(V) * T_ * VEC, N - cta_first) : 0) * sizeof(T));
+    auto prefetch_row = [&](int64_t r) {
+        if (r >= a.M) return;
+        if constexpr (VEC > 1) {
+            if (slice_bytes > 0) {
+                prefetch_l2_bulk(static_cast<const T*>(a.x) + r * N + cta_first, slice_bytes);
+                prefetch_l2_bulk(static_cast<const T*>(a.dy) + r * N + cta_first, slice_bytes);
+            }
+        }
+        if constexpr (LN) {
+            prefetch_l2_line(a.mean + r);
+            prefetch_l2_line(a.rstd + r);
+        }
+    };
+    // Rows are prefetched `ahead` rows before their turn: 2 without a ring;
+    // with one, one row beyond those in the ring, so that each bulk copy
+    // into the ring reads L2. The first rows are requested before the
+    // dependent-launch wait, overlapping the previous grid's tail (a
+    // prefetch only moves data towards L2, where that grid's writes land).
+    const int ahead = RING ? stages + 1 : 2;
+    if (tid == 0)
+        for (int k = 0; k < ahead; ++k) prefetch_row(first_row + k * row_step);
+    // RING: set by any thread whose wait for a stage ran out; read by every
+    // thread before its next wait and by thread 0 before its next copy, each
+    // after the barrier of the row's pair reduction, so that from the row
+    // after a timeout on the whole CTA neither waits nor copies.
+    __shared__ int s_late;
+    if constexpr (RING) {
+        if (tid == 0) {
+            for (int k = 0; k < stages; ++k) mbar_init(&full[k], 1);
+            mbar_init_fence();
+            s_late = 0;
+        }
+        __syncthreads();
+    }
+
     grid_release();
     grid_wait();
-    const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (c >= N) return;
+    const uint64_t limit = RING ? a.wait->limit_ns : 0;
+
+    // RING, thread 0: fill stage `st` with this CTA's slices of x and dy of
+    // row `r` (copies read memory: only after the wait above).
+    auto issue = [&](int64_t r, int st) {
+        mbar_arrive_expect(&full[st], 2u * slice_bytes);
+        if (slice_bytes > 0) {
+            bulk_load(ring + (2 * st) * V * T_, static_cast<const T*>(a.x) + r * N + cta_first, slice_bytes,
+                      &full[st]);
+            bulk_load(ring + (2 * st + 1) * V * T_, static_cast<const T*>(a.dy) + r * N + cta_first, slice_bytes,
+                      &full[st]);
+        }
+    };
+    int64_t issued = 0;  // RING, thread 0: rows of this CTA whose copies it issued
+    if constexpr (RING) {
+        if (tid == 0)
+            for (int k = 0; k < stages; ++k)
+                if (first_row + k * row_step < a.M) {
+                    issue(first_row + k * row_step, k);
+                    ++issued;
+                }
+    }
+
+    R rw;
+    rw.init(static_cast<const T*>(a.gamma) + f0 * VEC, stride, nv, acc_s + local * VEC, slice);
+    const T* xbase = static_cast<const T*>(a.x) + f0 * VEC;
+    const T* dybase = static_cast<const T*>(a.dy) + f0 * VEC;
+
+    int it = 0;
+    int st = 0;            // RING: this row's stage
+    uint32_t parity = 0;   // ... and the phase parity to wait for
+    volatile int& late = s_late;
+    int64_t seen = 0;      // RING, thread 0: leading rows whose copies it saw complete
+    bool waiting = true;   // RING: this thread still waits for its stages
+    for (int64_t row = first_row; row < a.M; row += row_step, ++it) {
+        if (tid == 0) prefetch_row(row + ahead * row_step);
+        Raw xv[V], dv[V];
+        if constexpr (RING) {
+            // After a wait has run out the CTA neither waits nor copies any
+            // more (its outputs are void by then); the kernel still ends.
+            if (waiting) {
+                if (late)
+                    waiting = false;
+                else if (!mbar_wait(&full[st], parity, limit))
+                    late = 1, waiting = false;
+                else
+                    seen = it + 1;
+            }
+            const uint4* xs = ring + (2 * st) * V * T_ + local;
+            const uint4* ds = xs + V * T_;
 #pragma unroll
-    for (int k = 0; k < NA; ++k) {
-        const float* p = ws + k * static_cast<int64_t>(N) + c;
-        const int64_t step = static_cast<int64_t>(NA) * N;
-        float s = 0.f;
-#pragma unroll 8
-        for (int64_t i = 0; i < partials; ++i) s += p[i * step];
-        (k == 0 ? out0 : out1)[c] = s;
+            for (int j = 0; j < V; ++j)
+                if (j < nv) {
+                    xv[j] = xs[j * 32];
+                    dv[j] = ds[j * 32];
+                }
+        } else {
+#pragma unroll
+            for (int j = 0; j < V; ++j)
+                if (j < nv) {
+                    xv[j] = O::load(xbase + row * N + j * stride);
+                    dv[j] = O::load(dybase + row * N + j * stride);
+                }
+        }
+        float mu = 0.f, rs = 0.f;
+        if constexpr (LN) {
+            mu = a.mean[row];
+            rs = a.rstd[row];
+        }
+        const float2 S = row_sum2(red, it & 1, rw.partials(xv, dv, nv, mu, rs), C, nwarps, wwidth);
+        if constexpr (RING) {
+            // Every thread has read this stage before the barrier above:
+            // refill it with the row `stages` turns ahead.
+            if (tid == 0 && !late && row + stages * row_step < a.M) {
+                fence_proxy_async();
+                issue(row + stages * row_step, st);
+                ++issued;
+            }
+            if (++st == stages) st = 0, parity ^= 1u;
+        }
+        rw.output(xv, dv, nv, mu, rs, S, invN, a.eps, static_cast<T*>(a.dx) + row * N + f0 * VEC, stride);
+    }
+
+    if constexpr (RING) {
+        if (tid == 0 && late) {
+            // Copies that may still be in flight (the rows issued after the
+            // last one thread 0 saw complete; a stage is refilled only after
+            // its previous row completed) get one more wait each, with the
+            // full limit, so that none lands after this CTA has gone; then
+            // tell the host.
+            for (int64_t kk = seen; kk < issued; ++kk)
+                mbar_wait(&full[kk % stages], static_cast<uint32_t>((kk / stages) & 1), kDefaultWaitLimitNs);
+            atomicAdd(&a.wait->timeouts, 1u);
+        }
+    }
+    rw.acc_to_smem();
+    write_partials<VEC, V, NA>(a, acc_s, slice, C, f0, nv);
+}
+
+// ------------------------------------------------------------ register pipeline
+// The backward for rows that one CTA covers (row_cluster == 1), with the
+// next row's loads in flight while the current row is reduced and written.
+// Each thread holds two register sets of its x and dy slices and alternates
+// between them (the loop body is unrolled twice, so no register is copied):
+// it loads row r + step into one set right after it has handed in its share
+// of row r's sums, while the other set still holds row r for the output
+// pass. The row's sums meet through an mbarrier instead of a block barrier:
+// lane 0 of each warp stores the warp's pair and arrives (release), every
+// thread then issues its next loads and waits for the phase (acquire) before
+// reading the pairs. A block barrier would order the loads issued before it
+// and so wait for them; the loads issued between an arrive and a wait are
+// ordered by neither. Rows two steps ahead are still bulk-prefetched into
+// L2, so the register loads are L2 hits.
+//
+// Slots and barriers alternate by row parity. A warp writes a row's pair
+// only after its wait on the previous row, which completes only after every
+// warp has arrived there, after reading the pairs of the row before; so a
+// slot is rewritten only after all its readers are done, and an mbarrier
+// phase never completes twice ahead of a waiter.
+struct PipeReduceSmem {
+    float2 warp_part[2][32];
+    uint64_t bar[2];
+};
+
+template <class T, int VEC, int V, bool LN>
+__global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_pipe(const BwdArgs a) {
+    using R = BwdRow<T, VEC, V, LN>;
+    using O = typename R::O;
+    using Raw = typename R::Raw;
+    constexpr int NA = R::NA;
+    __shared__ PipeReduceSmem red;
+    extern __shared__ float4 acc_v[];
+    float* acc_s = reinterpret_cast<float*>(acc_v);
+
+    const int T_ = blockDim.x;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = T_ >> 5;
+    int wwidth = 1;
+    while (wwidth < nwarps) wwidth <<= 1;
+    const int64_t first_row = blockIdx.x;
+    const int64_t row_step = gridDim.x;
+    const int N = a.N;
+    const int nacc = (N + VEC - 1) / VEC;
+    const int stride = 32 * VEC;
+    const int local = warp * V * 32 + lane;  // first access within the row
+    const int nv = valid_runs(nacc, local, 32, V);
+    const float invN = 1.f / static_cast<float>(N);
+    const int slice = T_ * V * VEC;
+
+    const uint32_t row_bytes = static_cast<uint32_t>(N * sizeof(T));
+    auto prefetch_row = [&](int64_t r) {
+        if (r >= a.M) return;
+        if constexpr (VEC > 1) {
+            prefetch_l2_bulk(static_cast<const T*>(a.x) + r * N, row_bytes);
+            prefetch_l2_bulk(static_cast<const T*>(a.dy) + r * N, row_bytes);
+        }
+        if constexpr (LN) {
+            prefetch_l2_line(a.mean + r);
+            prefetch_l2_line(a.rstd + r);
+        }
+    };
+    if (tid == 0) {
+        for (int k = 0; k < 3; ++k) prefetch_row(first_row + k * row_step);
+        mbar_init(&red.bar[0], nwarps);
+        mbar_init(&red.bar[1], nwarps);
+    }
+    __syncthreads();
+    grid_release();
+    grid_wait();
+    const uint64_t limit = a.wait->limit_ns;
+    bool late = false;  // a wait for the row's sums ran out (the outputs are then void)
+
+    R rw;
+    rw.init(static_cast<const T*>(a.gamma) + local * VEC, stride, nv, acc_s + local * VEC, slice);
+    const T* xbase = static_cast<const T*>(a.x) + local * VEC;
+    const T* dybase = static_cast<const T*>(a.dy) + local * VEC;
+
+    auto load = [&](Raw (&xv)[V], Raw (&dv)[V], int64_t row) {
+        if (row >= a.M) return;
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            if (j < nv) {
+                xv[j] = O::load(xbase + row * N + j * stride);
+                dv[j] = O::load(dybase + row * N + j * stride);
+            }
+    };
+    // One row: its sums handed in, the next row's loads issued into the
+    // other set, the sums collected, dx written.
+    auto step = [&](Raw (&xc)[V], Raw (&dc)[V], Raw (&xn)[V], Raw (&dn)[V], int64_t row, int it) {
+        if (tid == 0) prefetch_row(row + 3 * row_step);
+        float mu = 0.f, rs = 0.f;
+        if constexpr (LN) {
+            mu = a.mean[row];
+            rs = a.rstd[row];
+        }
+        float2 p = rw.partials(xc, dc, nv, mu, rs);
+        p.x = group_sum(p.x, 32);
+        p.y = group_sum(p.y, 32);
+        const int s = it & 1;
+        if (lane == 0) {
+            red.warp_part[s][warp] = p;
+            mbar_arrive(&red.bar[s]);
+        }
+        load(xn, dn, row + row_step);
+        // Every warp of the CTA arrives once per row, so the phase completes;
+        // the wait is bounded all the same (the device's wait limit).
+        if (!mbar_wait(&red.bar[s], static_cast<uint32_t>((it >> 1) & 1), limit)) late = true;
+        float2 w = lane < nwarps ? red.warp_part[s][lane] : make_float2(0.f, 0.f);
+        w.x = sum_first_lanes(w.x, wwidth);
+        w.y = sum_first_lanes(w.y, wwidth);
+        rw.output(xc, dc, nv, mu, rs, w, invN, a.eps, static_cast<T*>(a.dx) + row * N + local * VEC, stride);
+    };
+
+    Raw xa[V], da[V], xb[V], db[V];
+    load(xa, da, first_row);
+    int it = 0;
+    for (int64_t row = first_row; row < a.M; row += 2 * row_step, it += 2) {
+        step(xa, da, xb, db, row, it);
+        if (row + row_step >= a.M) break;
+        step(xb, db, xa, da, row + row_step, it + 1);
+    }
+    if (__syncthreads_or(late) && tid == 0) atomicAdd(&a.wait->timeouts, 1u);
+    rw.acc_to_smem();
+    write_partials<VEC, V, NA>(a, acc_s, slice, 1, local, nv);
+}
+
+// Column sums of the partial rows: out_k[c] = sum over p of ws[p][k][c]. A
+// CTA of 8 warps covers 32*W columns (W consecutive columns per lane, one
+// W-wide load per partial row): warp w adds partial rows w, w+8, w+16, ...
+// in that order, then the 8 warp sums of each column are added in warp
+// order. The order depends only on the number of partial rows, so the
+// result is deterministic for a plan; the partial rows are read by many
+// CTAs at once, with several loads in flight per thread. With no partial
+// rows (M == 0) the gradients are zero. W = 4 needs N % 4 == 0 (16-byte
+// aligned partial rows).
+template <int NA, int W>
+__global__ void __launch_bounds__(256) norm_bwd_colsum(const float* ws, int64_t partials, int32_t N, float* out0,
+                                                       float* out1) {
+    constexpr int kWarps = 8;
+    constexpr int kCols = 32 * W;
+    __shared__ float part[NA][kWarps][kCols];
+    grid_release();
+    grid_wait();
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int64_t cbase = static_cast<int64_t>(blockIdx.x) * kCols;
+    const int64_t c0 = cbase + lane * W;  // this lane's first column
+    const int64_t step = static_cast<int64_t>(NA) * N;
+    float s[NA][W];
+#pragma unroll
+    for (int k = 0; k < NA; ++k)
+#pragma unroll
+        for (int e = 0; e < W; ++e) s[k][e] = 0.f;
+    if (c0 < N) {
+#pragma unroll 4
+        for (int64_t p = warp; p < partials; p += kWarps) {
+#pragma unroll
+            for (int k = 0; k < NA; ++k) {
+                const float* src = ws + p * step + k * static_cast<int64_t>(N) + c0;
+                if constexpr (W == 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(src);
+                    s[k][0] += v.x;
+                    s[k][1] += v.y;
+                    s[k][2] += v.z;
+                    s[k][3] += v.w;
+                } else {
+                    s[k][0] += *src;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < NA; ++k)
+#pragma unroll
+        for (int e = 0; e < W; ++e) part[k][warp][lane * W + e] = s[k][e];
+    __syncthreads();
+    for (int i = threadIdx.x; i < NA * kCols; i += blockDim.x) {
+        const int k = i / kCols;
+        const int cc = i - k * kCols;
+        const int64_t c = cbase + cc;
+        if (c < N) {
+            float t = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) t += part[k][w][cc];
+            (k == 0 ? out0 : out1)[c] = t;
+        }
     }
 }
 
@@ -587,13 +825,27 @@ BwdKernel pick_bwd_r(int V) {
     }
 }
 
-// The ring variants exist for 16-byte vector rows only.
 template <class T, bool LN, int VEC>
-BwdKernel pick_bwd(int V, bool ring) {
-    if constexpr (VEC > 1) {
-        if (ring) return pick_bwd_r<T, LN, VEC, true>(V);
+BwdKernel pick_bwd_pipe(int V) {
+    constexpr int vmax = bwd_vmax(LN, sizeof(T), VEC);
+    switch (V) {
+        case 1: return norm_bwd_pipe<T, VEC, 1, LN>;
+        case 2: return vmax >= 2 ? norm_bwd_pipe<T, VEC, 2, LN> : nullptr;
+        case 4: if constexpr (vmax >= 4) return norm_bwd_pipe<T, VEC, 4, LN>; else return nullptr;
+        case 8: if constexpr (vmax >= 8) return norm_bwd_pipe<T, VEC, 8, LN>; else return nullptr;
+        default: return nullptr;
     }
-    return ring ? nullptr : pick_bwd_r<T, LN, VEC, false>(V);
+}
+
+// stages 0: rows from L2 after a bulk prefetch; 1: the register pipeline;
+// 2..4: the shared-memory ring (16-byte vector rows only).
+template <class T, bool LN, int VEC>
+BwdKernel pick_bwd(int V, int stages) {
+    if (stages == 1) return pick_bwd_pipe<T, LN, VEC>(V);
+    if constexpr (VEC > 1) {
+        if (stages >= 2) return pick_bwd_r<T, LN, VEC, true>(V);
+    }
+    return stages >= 2 ? nullptr : pick_bwd_r<T, LN, VEC, false>(V);
 }
 
 inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, unsigned cluster,
@@ -694,9 +946,9 @@ template <class T, bool LN>
 cudaError_t launch_norm_bwd(const norm_plan& p, const BwdArgs& a, cudaStream_t stream, int dev, int num_sms) {
     int64_t grid = 0;
     if (a.M > 0 && p.grid > 0) {
-        const bool ring = p.stages > 0;
-        const BwdKernel k = p.vec_elems == 1 ? pick_bwd<T, LN, 1>(p.per_thread, ring)
-                                             : pick_bwd<T, LN, ElemVec<T>::value>(p.per_thread, ring);
+        const bool ring = p.stages >= 2;
+        const BwdKernel k = p.vec_elems == 1 ? pick_bwd<T, LN, 1>(p.per_thread, p.stages)
+                                             : pick_bwd<T, LN, ElemVec<T>::value>(p.per_thread, p.stages);
         if (k == nullptr) return cudaErrorInvalidValue;
         const size_t smem = static_cast<size_t>(bwd_smem_bytes(LN, p.threads, p.per_thread, p.vec_elems, p.stages));
         int64_t resident = 0;
@@ -706,9 +958,9 @@ cudaError_t launch_norm_bwd(const norm_plan& p, const BwdArgs& a, cudaStream_t s
         grid = std::min<int64_t>(p.grid, resident);
         BwdArgs args = a;
         args.stages = p.stages;
-        if (ring) {
-            args.wait_timeouts = wait_counter(dev);
-            if (args.wait_timeouts == nullptr) return cudaErrorInvalidSymbol;
+        if (p.stages > 0) {
+            args.wait = wait_state(dev);
+            if (args.wait == nullptr) return cudaErrorInvalidSymbol;
         }
         void* kargs[] = {&args};
         const cudaError_t e = launch_pdl(reinterpret_cast<const void*>(k), dim3(static_cast<unsigned>(grid)),
@@ -722,8 +974,11 @@ cudaError_t launch_norm_bwd(const norm_plan& p, const BwdArgs& a, cudaStream_t s
     float* o0 = a.dgamma;
     float* o1 = LN ? a.dbeta : a.dgamma;
     void* cargs[] = {&ws, &parts, &N, &o0, &o1};
-    return launch_pdl(reinterpret_cast<const void*>(norm_bwd_colsum<LN ? 2 : 1>),
-                      dim3(static_cast<unsigned>((N + 255) / 256)), dim3(256), 0, 1, stream, cargs);
+    constexpr int NA = LN ? 2 : 1;
+    const bool wide = N % 4 == 0 && (reinterpret_cast<uintptr_t>(ws) & 15u) == 0;
+    const int cols = wide ? 128 : 32;
+    return launch_pdl(reinterpret_cast<const void*>(wide ? norm_bwd_colsum<NA, 4> : norm_bwd_colsum<NA, 1>),
+                      dim3(static_cast<unsigned>((N + cols - 1) / cols)), dim3(256), 0, 1, stream, cargs);
 }
 
 }  // namespace libnorm

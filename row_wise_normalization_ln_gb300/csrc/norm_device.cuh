@@ -135,6 +135,12 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t arrivals) {
 // names them).
 __device__ __forceinline__ void mbar_init_fence() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 
+// Arrive once (release at CTA scope: this thread's earlier writes are
+// visible to every thread that then sees the phase complete).
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // Arrive once, announcing `bytes` more bytes for the current phase.
 __device__ __forceinline__ void mbar_arrive_expect(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
@@ -153,26 +159,37 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     return done != 0;
 }
 
+// The same test without suspending: true if the phase has completed now.
+__device__ __forceinline__ bool mbar_test_now(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
 
-// A wait on a copy gives up after this long (the copies it waits for take
-// microseconds); the kernel then records the timeout for the host.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
-
 // Wait until the phase of parity `parity` of `bar` has completed; false if
-// it has not within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    if (mbar_test(bar, parity)) return true;
+// it has not within `limit_ns` nanoseconds of %globaltimer (the copies it
+// waits for take microseconds). A limit of 0 tests once, without waiting.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_test_now(bar, parity)) return true;
+    if (limit_ns == 0) return false;
     const uint64_t t0 = global_ns();
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_test(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
 }
 

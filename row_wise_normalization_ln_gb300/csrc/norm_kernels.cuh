@@ -1175,13 +1175,20 @@ __global__ void __launch_bounds__(kRingMaxThreads) norm_fwd_ring(const NormArgs 
     const T* g = static_cast<const T*>(a.gamma) + col;
     const T* b = static_cast<const T*>(a.beta) + col;
 
+    // Set by any thread whose wait for a stage ran out. Every thread reads
+    // it before its next wait, and thread 0 before its next copy, each after
+    // the barrier of the row reduction that follows the wait: from the row
+    // after a timeout on, the whole CTA neither waits nor copies.
+    __shared__ int s_late;
     if (tid == 0) {
         for (int k = 0; k < stages; ++k) mbar_init(&full[k], 1);
         mbar_init_fence();
+        s_late = 0;
     }
     __syncthreads();
     grid_release();
     grid_wait();
+    const uint64_t limit = a.wait->limit_ns;
 
     // Thread 0: fill stage `st` with this CTA's share of `row`.
     auto issue = [&](int64_t row, int st) {
@@ -1190,19 +1197,32 @@ __global__ void __launch_bounds__(kRingMaxThreads) norm_fwd_ring(const NormArgs 
         if (cbytes) bulk_load(ring + st * stage_slots, xr + cbase * VEC, cbytes, &full[st]);
         if (LN) bulk_load(kslot + st, xr, 16u, &full[st]);
     };
+    int64_t issued = 0;  // thread 0: rows of this CTA whose copies it issued
     if (tid == 0)
         for (int k = 0; k < stages; ++k)
-            if (first_row + k * row_step < a.M) issue(first_row + k * row_step, k);
+            if (first_row + k * row_step < a.M) {
+                issue(first_row + k * row_step, k);
+                ++issued;
+            }
 
+    volatile int& late = s_late;
     int st = 0;
     uint32_t parity = 0;
     int64_t k = 0;        // rows of this CTA done so far
-    int64_t late = -1;    // the row whose wait ran out, if any
+    int64_t seen = 0;     // thread 0: leading rows whose copies it saw complete
+    bool waiting = true;  // this thread still waits for its stages
     for (int64_t row = first_row; row < a.M; row += row_step, ++k) {
-        // After one wait has run out this CTA neither waits nor copies any
-        // more (its outputs are void by then), so the kernel still ends in
+        // After a wait has run out the CTA neither waits nor copies any more
+        // (its outputs are void by then), so the kernel still ends in
         // bounded time.
-        if (late < 0 && !mbar_wait(&full[st], parity)) late = k;
+        if (waiting) {
+            if (late)
+                waiting = false;
+            else if (!mbar_wait(&full[st], parity, limit))
+                late = 1, waiting = false;
+            else
+                seen = k + 1;
+        }
         float K = 0.f;
         if constexpr (LN) K = PairCodec<T>::first(kslot[st]);
         S s;
@@ -1222,24 +1242,26 @@ __global__ void __launch_bounds__(kRingMaxThreads) norm_fwd_ring(const NormArgs 
             if (a.mean) a.mean[row] = K + mu;
             if (a.rstd) a.rstd[row] = rs;
         }
-        if (tid == 0 && late < 0) {
+        if (tid == 0 && !late) {
             const int64_t next = row + stages * row_step;
             if (next < a.M) {
                 fence_proxy_async();
                 issue(next, st);
+                ++issued;
             }
         }
         s.emit(g, b, static_cast<T*>(a.y) + row * a.ldy + col, stride, nvalid, mu, rs);
         if (++st == stages) st = 0, parity ^= 1u;
     }
-    if (late >= 0 && tid == 0) {
-        // Copies still in flight (rows late .. late+stages-1 of this CTA)
-        // get one more bounded wait each, so that none lands after this CTA
-        // has gone; then tell the host.
-        for (int64_t kk = late; kk < late + stages; ++kk)
-            if (first_row + kk * row_step < a.M)
-                mbar_wait(&full[kk % stages], static_cast<uint32_t>((kk / stages) & 1));
-        atomicAdd(a.wait_timeouts, 1u);
+    if (tid == 0 && late) {
+        // Copies that may still be in flight (the rows issued after the last
+        // one thread 0 saw complete; a stage is refilled only after its
+        // previous row completed, so each has one outstanding phase) get one
+        // more wait each, with the full limit, so that none lands after this
+        // CTA has gone; then tell the host.
+        for (int64_t kk = seen; kk < issued; ++kk)
+            mbar_wait(&full[kk % stages], static_cast<uint32_t>((kk / stages) & 1), kDefaultWaitLimitNs);
+        atomicAdd(&a.wait->timeouts, 1u);
     }
     // No CTA may exit while a peer can still read its shared memory.
     if (C > 1) cluster_barrier();
@@ -1391,26 +1413,31 @@ cudaError_t launch_norm(const norm_plan& p, const NormArgs& a, cudaStream_t stre
         cfg.numAttrs = 2;
     }
     NormArgs args = a;
-    if (!ADD && p.mapping == NORM_MAP_CTA && p.stages == 0 && p.vec_elems > 1 &&
-        int64_t(a.N) * int64_t(sizeof(T)) >= kPrefetchMinRowBytes) {
-        // L2 prefetch (args.group = rows ahead + 1). One CTA per row: the row
-        // 3/8 of the resident CTAs ahead, just past the rows in flight
-        // (measured on GB300: 1/4 to 1/2 ahead gain 2-14 %, a whole resident
-        // set ahead loses). A cluster per row: its own row (a row ahead loses
-        // at any distance; its own row gains 2.6 % on 65536-wide rows). The
-        // fused add measured slower with it and has none.
+    if (!ADD && p.mapping == NORM_MAP_CTA && p.stages == 0 && p.vec_elems > 1) {
+        // L2 prefetch (args.group = rows ahead + 1). One CTA per row, rows of
+        // at least kPrefetchMinRowBytes: the row 3/8 of the resident CTAs
+        // ahead, just past the rows in flight (measured on GB300: 1/4 to 1/2
+        // ahead gain 2-14 %, a whole resident set ahead loses). A cluster per
+        // row: its own row (a row ahead loses at any distance; its own row
+        // gains 2.6 % on 65536-wide rows). A launch whose rows all fit in one
+        // wave of resident CTAs: each CTA its own row, so that the fetch
+        // overlaps the previous grid's tail. The fused add measured slower
+        // with it and has none.
         if (p.cluster > 1) {
             args.group = 1;
         } else {
             int64_t resident = 0;
             const cudaError_t e = resident_ctas(reinterpret_cast<const void*>(k), p.threads, dev, num_sms, &resident);
             if (e != cudaSuccess) return e;
-            args.group = static_cast<int32_t>(std::min<int64_t>(resident * 3 / 8, a.M) + 1);
+            if (a.M <= resident && p.grid >= a.M)
+                args.group = 1;
+            else if (int64_t(a.N) * int64_t(sizeof(T)) >= kPrefetchMinRowBytes)
+                args.group = static_cast<int32_t>(std::min<int64_t>(resident * 3 / 8, a.M) + 1);
         }
     }
     if (p.stages > 0) {
-        args.wait_timeouts = wait_counter(dev);
-        if (args.wait_timeouts == nullptr) return cudaErrorInvalidSymbol;
+        args.wait = wait_state(dev);
+        if (args.wait == nullptr) return cudaErrorInvalidSymbol;
     }
     if (p.stages > 0 && p.grid == 0) {
         // Persistent grid: as many CTAs (whole clusters) as can be resident at

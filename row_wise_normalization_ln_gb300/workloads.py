@@ -126,6 +126,13 @@ WORKLOADS = {
 
 BENCH_WORKLOAD = "rms_f32_8192x4096"
 
+# The forward configurations the headline metric is quoted on: the ROCm
+# LayerNorm README's 128 x 1024 example, the RMSNorm post's B*T x C shapes,
+# the T3 drill's N = 8192 with the cancellation recipe, and the long and the
+# non-power-of-two LayerNorm rows.
+BASELINE_CONFIGS = ("ln_f32_128x1024", "rms_f32_8192x4096", "ln_bf16_4096x8192_outliers", "rms_bf16_65536x2048",
+                    "ln_f32_2048x65536", "ln_f32_8192x5000")
+
 
 def _draw(recipe: str, M: int, N: int, g: torch.Generator) -> torch.Tensor:
     if recipe == "normal01":

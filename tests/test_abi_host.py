@@ -36,7 +36,8 @@ def test_header_declares_the_abi():
         "ln_bwd_noalloc",
         "ln_fwd_fp8", "rms_fwd_fp8", "ln_fwd_add_fp8", "rms_fwd_add_fp8", "ln_fwd_fp8_planned", "rms_fwd_fp8_planned",
         "ln_fwd_strided", "rms_fwd_strided",
-        "norm_status_string", "norm_last_cuda_error", "norm_abi_version", "norm_wait_timeouts"}
+        "norm_status_string", "norm_last_cuda_error", "norm_abi_version", "norm_wait_timeouts",
+        "norm_synchronize", "norm_set_wait_limit", "norm_wait_limit"}
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -46,7 +47,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in (0, -1, -2, -3, -4):
+    for code in (0, -1, -2, -3, -4, -5):
         assert lib.norm_status_string(code)
     assert lib.norm_status_string(0) == b"ok"
 
@@ -78,6 +79,28 @@ def test_null_pointers_rejected(lib):
         assert lib.ln_fwd(*args, None, None, 4, 8, 1e-5, rn.NORM_F32, None) == rn.NORM_ERR_ARG
     for args in [(None, P, P), (P, None, P), (P, P, None)]:
         assert lib.rms_fwd(*args, 4, 8, 1e-6, rn.NORM_F32, None) == rn.NORM_ERR_ARG
+
+
+def test_wait_limit_checked_on_the_host(lib):
+    assert lib.norm_set_wait_limit(60_000_000_001) == rn.NORM_ERR_ARG
+    assert lib.norm_set_wait_limit(2 ** 64 - 1) == rn.NORM_ERR_ARG
+    assert lib.norm_wait_limit(None) == rn.NORM_ERR_ARG
+    assert lib.norm_status_string(rn.NORM_ERR_TIMEOUT) != lib.norm_status_string(-99)
+
+
+def test_no_alloc_null_pointers_rejected_before_any_cuda_call(lib):
+    vp = ctypes.c_void_p
+    f = lib.ln_bwd_noalloc
+    f.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, vp]
+    f.restype = ctypes.c_int
+    # On a machine without a GPU any CUDA call would give NORM_ERR_CUDA
+    # instead: NORM_ERR_ARG shows the check came first.
+    for k in range(8):
+        args = [P] * 8
+        args[k] = None
+        assert f(*args, 4, 1024, rn.NORM_F32, None) == rn.NORM_ERR_ARG, k
+    assert f(P, P, P, P, P, P, None, P, 0, 1024, rn.NORM_F32, None) == rn.NORM_ERR_ARG   # dgamma even for M == 0
+    assert f(P, P, P, P, P, P, P, P, 4, 65540, rn.NORM_F32, None) == rn.NORM_ERR_ARG     # beyond the row limit
 
 
 def test_wait_timeouts_needs_a_destination(lib):
@@ -388,7 +411,7 @@ def test_bwd_workspace_checked_on_the_host(lib):
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on the fake pointers")
-@pytest.mark.parametrize("stages", [0, 2, 4])
+@pytest.mark.parametrize("stages", [0, 1, 2, 4])
 def test_bwd_valid_plan_passes_the_host_checks(lib, stages):
     p = _bwd_plan(stages=stages)
     need = rn.bwd_workspace_bytes(p, 1024, True)
@@ -396,7 +419,8 @@ def test_bwd_valid_plan_passes_the_host_checks(lib, stages):
 
 
 @pytest.mark.parametrize("kw", [
-    dict(mapping=rn.NORM_MAP_GROUP), dict(stages=1), dict(stages=5), dict(stages=-1),
+    dict(mapping=rn.NORM_MAP_GROUP), dict(stages=5), dict(stages=-1),
+    dict(stages=1, cluster=2, group=2, threads=64),  # the register pipeline: one CTA per row
     dict(stages=2, vec_elems=1),                # the ring moves 16-byte vectors
     dict(stages=4, threads=512, per_thread=4),  # 2*512*4*16 B per stage: the ring exceeds 225 KB
     dict(vec_elems=8), dict(per_thread=8), dict(per_thread=3),

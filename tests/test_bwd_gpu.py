@@ -186,6 +186,73 @@ def test_every_variant(dtype, ln, plan, N):
         check_rms_bwd(dy, x, g, 1e-6, dx, dw)
 
 
+def _pipe_variants():
+    out = []
+    for dtype, vec in (("f32", 4), ("bf16", 8), ("f16", 8)):
+        for ve in (vec, 1):
+            for ln in (True, False):
+                vmax = 8 if ve == 1 else (2 if (ln and dtype != "f32") else 4)
+                for per in (1, 2, 4, 8):
+                    if per > vmax or (dtype == "f16" and ve == 1 and per not in (1, 8)):
+                        continue
+                    for T in (32, 96, 512):
+                        cap = T * per * ve
+                        for Q in (1, 2, 8):
+                            for N in sorted({cap, max(ve, cap - 3 * ve)}):
+                                out.append((dtype, ln, dict(mapping=rn.NORM_MAP_CTA, vec_elems=ve, per_thread=per,
+                                                            group=Q, threads=T, cluster=1, stages=1, grid=2 * Q), N))
+    return out
+
+
+PIPE = _pipe_variants()
+
+
+@pytest.mark.parametrize("dtype,ln,plan,N", PIPE,
+                         ids=[f"{d}-{'ln' if ln else 'rms'}-v{p['vec_elems']}-p{p['per_thread']}-t{p['threads']}"
+                              f"-q{p['group']}-N{n}" for d, ln, p, n in PIPE])
+def test_pipe_variants(dtype, ln, plan, N):
+    """The register pipeline (stages 1: a CTA per row, the next row's loads
+    in flight while the current one is reduced): every width, accesses per
+    thread, CTA size and reduction cluster, exact and ragged rows, and
+    grids whose CTAs walk an odd and an even number of rows."""
+    x, dy, g = _rand(11, N, DT[dtype], seed=N + plan["threads"] + 1, loc=0.5, scale=2.0)
+    if ln:
+        dx, dg, db = run_ln_bwd(dy, x, g, 1e-5, plan=plan)
+        check_ln_bwd(dy, x, g, 1e-5, dx, dg, db)
+    else:
+        dx, dw = run_rms_bwd(dy, x, g, 1e-6, plan=plan)
+        check_rms_bwd(dy, x, g, 1e-6, dx, dw)
+    assert rn.wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 152, 153, 3001])
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_pipe_many_rows(M, dtype):
+    """The register pipeline on a persistent grid over up to 3001 rows (each
+    row-parity slot and barrier phase reused many times), against the
+    backward without the pipeline on the same inputs: dx bit for bit (the
+    arithmetic is the same), the column gradients against the oracle."""
+    N = 8192 if dtype != "f32" else 4096
+    x, dy, g = _rand(M, N, DT[dtype], seed=M, loc=2.0, scale=1.5)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for ln in (True, False):
+        base = rn.make_bwd_plan(M, N, DT[dtype], ln, True, sms)
+        if base["cluster"] != 1:
+            continue
+        pipe = dict(base, stages=1)
+        plain = dict(base, stages=0)
+        if ln:
+            dx1, dg, db = run_ln_bwd(dy, x, g, 1e-5, plan=pipe)
+            dx0, _, _ = run_ln_bwd(dy, x, g, 1e-5, plan=plain)
+            check_ln_bwd(dy, x, g, 1e-5, dx1, dg, db, rows=sample_rows(M, 24))
+        else:
+            dx1, dw = run_rms_bwd(dy, x, g, 1e-6, plan=pipe)
+            dx0, _ = run_rms_bwd(dy, x, g, 1e-6, plan=plain)
+            check_rms_bwd(dy, x, g, 1e-6, dx1, dw, rows=sample_rows(M, 24))
+        assert torch.equal(dx1.cpu(), dx0.cpu())
+    assert rn.wait_timeouts() == 0
+
+
 # ------------------------------------------------------------ layouts and errors
 
 def _ring_variants():
