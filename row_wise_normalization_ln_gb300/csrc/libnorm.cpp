@@ -260,6 +260,18 @@ norm_status bwd_make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_align
     const int vec = (all_aligned && (N * elem_size(dtype)) % 16 == 0) ? 16 / elem_size(dtype) : 1;
     const int64_t nacc = ceil_div(N, vec);
     int per = bwd_vmax(ln, dtype, vec);
+    if (vec > 1) {
+        // Vector rows: the fewest accesses per thread, from 2, that let one
+        // CTA of at most 512 threads cover the row (sweeps on GB300: RMSNorm
+        // fp32 8192x4096 72.1 -> 64.3 us with 512 x 2 instead of 256 x 4,
+        // RMSNorm bf16 65536x2048 161 -> 127 us with 128 x 2 instead of
+        // 64 x 4; one access per thread was slower).
+        for (int q = std::min(2, per); q <= per; q *= 2)
+            if (round_up(ceil_div(nacc, q), 32) <= kBwdMaxThreads) {
+                per = q;
+                break;
+            }
+    }
     int64_t cluster = 1;
     int64_t threads = round_up(ceil_div(nacc, per), 32);
     while (threads > kBwdMaxThreads && cluster < kMaxCluster) {
@@ -279,14 +291,19 @@ norm_status bwd_make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_align
     p->rounds = 1;
     // fp32 vector rows take a 2-stage ring of upcoming rows in shared memory
     // (measured on GB300: 10-15 % faster at 8192x4096, 8192x5000 and
-    // 2048x65536); 16-bit rows are bound by instruction issue and keep
-    // loading from L2.
-    if (vec == 4 && libnorm::bwd_smem_bytes(ln, p->threads, per, vec, 2) <= kMaxSmem) p->stages = 2;
+    // 2048x65536; 3 or 4 stages slower); 16-bit vector rows of one CTA take
+    // the register pipeline (LayerNorm bf16 4096x8192 54.6 -> 42.6 us,
+    // RMSNorm bf16 65536x2048 146 -> 127 us).
+    if (vec == 4 && libnorm::bwd_smem_bytes(ln, p->threads, per, vec, 2) <= kMaxSmem)
+        p->stages = 2;
+    else if (vec > 1 && cluster == 1)
+        p->stages = 1;
     // Persistent grid of at most 1024 threads and 6 CTAs per SM in whole
     // clusters (the launch takes fewer if fewer fit at once). CTAs that each
-    // take their own rows add their column sums in clusters of 4 (of 8 for
-    // small CTAs, many of which share an SM): fewer partial rows, and such
-    // clusters are easy to place (measured faster than 2 or 8).
+    // take their own rows add their column sums in clusters of 4, 2 with a
+    // ring: fewer partial rows, and such clusters are easy to place
+    // (measured: RMSNorm bf16 65536x2048 127 us at 4, 129 at 2, 138 at 8;
+    // with a ring, RMSNorm fp32 8192x4096 64.3 us at 2, 69.8 at 4).
     const int64_t per_sm = std::max<int64_t>(1, std::min<int64_t>(6, 1024 / threads));
     if (cluster > 1) {
         const int64_t clusters = std::max<int64_t>(1, std::min<int64_t>(M, num_sms * per_sm / cluster));
@@ -294,7 +311,7 @@ norm_status bwd_make_plan(int64_t M, int64_t N, norm_dtype dtype, bool all_align
         p->grid = M > 0 ? clusters * cluster : 0;
     } else {
         const int64_t ctas = std::min<int64_t>(M, num_sms * per_sm);
-        const int64_t want = threads <= 128 ? kMaxCluster : 4;
+        const int64_t want = p->stages >= 2 ? 2 : 4;
         const int64_t q = std::min<int64_t>(want, pow2_ceil(std::max<int64_t>(ctas, 1)));
         p->group = static_cast<int32_t>(q);
         p->grid = M > 0 ? round_up(ctas, q) : 0;

@@ -102,12 +102,18 @@ inline int64_t ring_smem_bytes(int stages, int per_thread, int threads) {
 WaitState* wait_state(int dev);
 
 // Dynamic shared memory of a backward launch: the column accumulators
-// ([2 for LayerNorm | 1][threads * per_thread * vec] fp32), then, for a ring
+// ([2 for LayerNorm | 1][threads * per_thread * vec] fp32) and, for a ring
 // (stages >= 2), per stage two slices of 16-byte slots (x, dy) and an 8-byte
-// mbarrier.
+// mbarrier: after the accumulators, or over them when those stay in
+// registers until the last row.
 inline int64_t bwd_smem_bytes(bool ln, int threads, int per_thread, int vec, int stages) {
-    const int64_t ring = stages >= 2 ? stages : 0;  // stages 1, the register pipeline, keeps no rows here
-    return int64_t(ln ? 2 : 1) * threads * per_thread * vec * 4 + ring * (2 * int64_t(threads) * per_thread * 16 + 8);
+    const int64_t acc = int64_t(ln ? 2 : 1) * threads * per_thread * vec * 4;
+    if (stages < 2) return acc;  // stages 1, the register pipeline, keeps no rows here
+    const int64_t ring = int64_t(stages) * (2 * int64_t(threads) * per_thread * 16 + 8);
+    // Accumulators held in registers until the end (all but the 16-bit
+    // variants of 4 accesses per thread) share their slots with the ring.
+    const bool acc_in_registers = !(vec == 8 && per_thread >= 4);
+    return acc_in_registers ? (acc > ring ? acc : ring) : acc + ring;
 }
 
 // Partial rows of the column gradients a backward plan produces (one per

@@ -463,11 +463,12 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
     const int nv = valid_runs(nacc, f0, 32, V);
     const float invN = 1.f / static_cast<float>(N);
     const int slice = T_ * V * VEC;  // floats per accumulator array
-    // RING: after the accumulators, `stages` stages of this CTA's slices of
-    // an upcoming row, x then dy (V*T 16-byte slots each), then one mbarrier
-    // per stage.
+    // RING: `stages` stages of this CTA's slices of an upcoming row, x then
+    // dy (V*T 16-byte slots each), then one mbarrier per stage; after the
+    // shared-memory accumulators, or over them when the accumulators are in
+    // registers until the end (they reach their slots after the last row).
     const int stages = RING ? a.stages : 0;
-    uint4* ring = reinterpret_cast<uint4*>(acc_s + NA * slice);
+    uint4* ring = reinterpret_cast<uint4*>(acc_s + (R::ACC_REG ? 0 : NA * slice));
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + 2 * stages * V * T_);
 
     // Rows ahead go to L2 by bulk prefetch: this CTA's contiguous slice of x
@@ -608,6 +609,10 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
             atomicAdd(&a.wait->timeouts, 1u);
         }
     }
+    // With register accumulators the ring overlaps their shared-memory
+    // slots: every thread is past its last read of the ring (and thread 0
+    // past its drain) before any slot is written.
+    __syncthreads();
     rw.acc_to_smem();
     write_partials<VEC, V, NA>(a, acc_s, slice, C, f0, nv);
 }
@@ -692,7 +697,8 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_pipe(const BwdArgs a)
     const T* xbase = static_cast<const T*>(a.x) + local * VEC;
     const T* dybase = static_cast<const T*>(a.dy) + local * VEC;
 
-    auto load = [&](Raw (&xv)[V], Raw (&dv)[V], int64_t row) {
+    // A row's slices of x and dy and (LayerNorm) its mean and rstd.
+    auto load = [&](Raw (&xv)[V], Raw (&dv)[V], float2& ms, int64_t row) {
         if (row >= a.M) return;
 #pragma unroll
         for (int j = 0; j < V; ++j)
@@ -700,16 +706,14 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_pipe(const BwdArgs a)
                 xv[j] = O::load(xbase + row * N + j * stride);
                 dv[j] = O::load(dybase + row * N + j * stride);
             }
+        if constexpr (LN) ms = make_float2(a.mean[row], a.rstd[row]);
     };
     // One row: its sums handed in, the next row's loads issued into the
     // other set, the sums collected, dx written.
-    auto step = [&](Raw (&xc)[V], Raw (&dc)[V], Raw (&xn)[V], Raw (&dn)[V], int64_t row, int it) {
+    auto step = [&](Raw (&xc)[V], Raw (&dc)[V], float2& mc, Raw (&xn)[V], Raw (&dn)[V], float2& mn, int64_t row,
+                    int it) {
         if (tid == 0) prefetch_row(row + 3 * row_step);
-        float mu = 0.f, rs = 0.f;
-        if constexpr (LN) {
-            mu = a.mean[row];
-            rs = a.rstd[row];
-        }
+        const float mu = mc.x, rs = mc.y;
         float2 p = rw.partials(xc, dc, nv, mu, rs);
         p.x = group_sum(p.x, 32);
         p.y = group_sum(p.y, 32);
@@ -718,7 +722,7 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_pipe(const BwdArgs a)
             red.warp_part[s][warp] = p;
             mbar_arrive(&red.bar[s]);
         }
-        load(xn, dn, row + row_step);
+        load(xn, dn, mn, row + row_step);
         // Every warp of the CTA arrives once per row, so the phase completes;
         // the wait is bounded all the same (the device's wait limit).
         if (!mbar_wait(&red.bar[s], static_cast<uint32_t>((it >> 1) & 1), limit)) late = true;
@@ -729,12 +733,13 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_pipe(const BwdArgs a)
     };
 
     Raw xa[V], da[V], xb[V], db[V];
-    load(xa, da, first_row);
+    float2 ma = make_float2(0.f, 0.f), mb = ma;  // (mean, rstd) of the rows in xa/da and xb/db
+    load(xa, da, ma, first_row);
     int it = 0;
     for (int64_t row = first_row; row < a.M; row += 2 * row_step, it += 2) {
-        step(xa, da, xb, db, row, it);
+        step(xa, da, ma, xb, db, mb, row, it);
         if (row + row_step >= a.M) break;
-        step(xb, db, xa, da, row + row_step, it + 1);
+        step(xb, db, mb, xa, da, ma, row + row_step, it + 1);
     }
     if (__syncthreads_or(late) && tid == 0) atomicAdd(&a.wait->timeouts, 1u);
     rw.acc_to_smem();
@@ -958,10 +963,8 @@ cudaError_t launch_norm_bwd(const norm_plan& p, const BwdArgs& a, cudaStream_t s
         grid = std::min<int64_t>(p.grid, resident);
         BwdArgs args = a;
         args.stages = p.stages;
-        if (p.stages > 0) {
-            args.wait = wait_state(dev);
-            if (args.wait == nullptr) return cudaErrorInvalidSymbol;
-        }
+        args.wait = wait_state(dev);
+        if (args.wait == nullptr) return cudaErrorInvalidSymbol;
         void* kargs[] = {&args};
         const cudaError_t e = launch_pdl(reinterpret_cast<const void*>(k), dim3(static_cast<unsigned>(grid)),
                                          dim3(static_cast<unsigned>(p.threads)), smem,

@@ -797,8 +797,14 @@ __device__ __forceinline__ void prefetch_row_share(const NormArgs& a, int64_t ro
     }
 }
 
-template <class T, int VEC, int V, bool LN, bool CL, bool ADD, bool Q8, bool SHIFT>
+// FULL: one CTA per row in one round whose accesses exactly cover the row
+// (N == threads * V * VEC; no cluster, no shift): every access of every
+// thread is valid, so the accesses carry no bounds predicates. (The round
+// count stays a runtime value: with both known, ptxas spilled the 16-bit
+// LayerNorm variants at the 64-register cap.)
+template <class T, int VEC, int V, bool LN, bool CL, bool ADD, bool Q8, bool SHIFT, bool FULL>
 __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(const NormArgs a) {
+    static_assert(!FULL || (!CL && !SHIFT && VEC > 1), "FULL rows: one CTA, 16-byte vectors, no shift");
     using S = Slice<T, VEC, V, LN>;
     using SO = ScalarOps<T>;
     __shared__ std::conditional_t<CL, RowReduceSmemCl, RowReduceSmem> red;
@@ -871,7 +877,7 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
         for (int i = 0; i < rounds; ++i) {
             const int r = ADD ? rounds - 1 - i : i;
             const int f = (r * static_cast<int>(C) + rank) * V * T_ + in_slice;
-            nv = valid_runs(nb, f, 32, V);
+            nv = FULL ? V : valid_runs(nb, f, 32, V);
             if constexpr (ADD) {
                 s.load_add(xb + f * VEC, rb + f * VEC, stride, nv);
                 if (r != 0) s.store_h(hb + f * VEC, stride, nv);
@@ -949,7 +955,7 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
             for (int r = 0; r < rounds; ++r) {
                 const int f = (r * static_cast<int>(C) + rank) * V * T_ + in_slice;
                 if (r != 0) {
-                    nv = valid_runs(nb, f, 32, V);
+                    nv = FULL ? V : valid_runs(nb, f, 32, V);
                     s.load(hb + f * VEC, stride, nv);  // only this thread wrote h there
                 }
                 s.template out<Q8>(gb + f * VEC, bb + f * VEC, a.y, yb + f * VEC, stride, nv, mu, rs, inv, sp);
@@ -959,7 +965,7 @@ __global__ void __launch_bounds__(ADD ? kFusedMaxThreads : 1024) norm_fwd_cta(co
             for (int r = rounds - 1; r >= 0; --r) {
                 const int f = (r * static_cast<int>(C) + rank) * V * T_ + in_slice;
                 if (r != rounds - 1) {
-                    nv = valid_runs(nb, f, 32, V);
+                    nv = FULL ? V : valid_runs(nb, f, 32, V);
                     s.load(xb + f * VEC, stride, nv);
                 }
                 s.template out<Q8>(gb + f * VEC, bb + f * VEC, a.y, yb + f * VEC, stride, nv, mu, rs, inv, sp);
@@ -1274,22 +1280,27 @@ using KernelFn = void (*)(const NormArgs);
 // SHIFT variants exist for the 16-byte vector width only (element rows
 // need no alignment).
 template <class T, bool LN, bool ADD, bool Q8, int VEC, int V>
-KernelFn<T, LN> pick_cta(bool cl, bool shift) {
+KernelFn<T, LN> pick_cta(bool cl, bool shift, bool full) {
     if constexpr (VEC > 1) {
         if (shift)
-            return cl ? norm_fwd_cta<T, VEC, V, LN, true, ADD, Q8, true> : norm_fwd_cta<T, VEC, V, LN, false, ADD, Q8, true>;
+            return cl ? norm_fwd_cta<T, VEC, V, LN, true, ADD, Q8, true, false>
+                      : norm_fwd_cta<T, VEC, V, LN, false, ADD, Q8, true, false>;
+        if constexpr (Q8) {
+            if (full && !cl) return norm_fwd_cta<T, VEC, V, LN, false, ADD, Q8, false, true>;
+        }
     }
-    return cl ? norm_fwd_cta<T, VEC, V, LN, true, ADD, Q8, false> : norm_fwd_cta<T, VEC, V, LN, false, ADD, Q8, false>;
+    return cl ? norm_fwd_cta<T, VEC, V, LN, true, ADD, Q8, false, false>
+              : norm_fwd_cta<T, VEC, V, LN, false, ADD, Q8, false, false>;
 }
 
 template <class T, bool LN, bool ADD, bool Q8, int VEC>
-KernelFn<T, LN> pick_kernel(int mapping, int per_thread, bool cl, bool shift) {
+KernelFn<T, LN> pick_kernel(int mapping, int per_thread, bool cl, bool shift, bool full) {
     const bool group = mapping == NORM_MAP_GROUP;
     switch (per_thread) {
-        case 1: return group ? norm_fwd_group<T, VEC, 1, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 1>(cl, shift);
-        case 2: return group ? norm_fwd_group<T, VEC, 2, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 2>(cl, shift);
-        case 4: return group ? norm_fwd_group<T, VEC, 4, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 4>(cl, shift);
-        case 8: return group ? norm_fwd_group<T, VEC, 8, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 8>(cl, shift);
+        case 1: return group ? norm_fwd_group<T, VEC, 1, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 1>(cl, shift, full);
+        case 2: return group ? norm_fwd_group<T, VEC, 2, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 2>(cl, shift, full);
+        case 4: return group ? norm_fwd_group<T, VEC, 4, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 4>(cl, shift, full);
+        case 8: return group ? norm_fwd_group<T, VEC, 8, LN, ADD, Q8> : pick_cta<T, LN, ADD, Q8, VEC, 8>(cl, shift, full);
         default: return nullptr;
     }
 }
@@ -1391,8 +1402,15 @@ cudaError_t launch_norm(const norm_plan& p, const NormArgs& a, cudaStream_t stre
             if (e != cudaSuccess) return e;
         }
     } else {
-        k = p.vec_elems == 1 ? pick_kernel<T, LN, ADD, Q8, 1>(p.mapping, p.per_thread, cl, false)
-                             : pick_kernel<T, LN, ADD, Q8, ElemVec<T>::value>(p.mapping, p.per_thread, cl, a.shift != 0);
+        // Rows exactly covered by one round of one CTA's accesses, FP8
+        // output only (A/B on GB300: FP8 LayerNorm bf16 4096x8192 21.67 ->
+        // 20.98 us; the row-dtype outputs measured slower without the
+        // predicates, LayerNorm bf16 21.78 -> 22.73 us).
+        const bool full = Q8 && p.mapping == NORM_MAP_CTA && p.cluster == 1 && p.rounds == 1 && a.shift == 0 &&
+                          p.vec_elems > 1 && int64_t(a.N) == int64_t(p.threads) * p.per_thread * p.vec_elems;
+        k = p.vec_elems == 1 ? pick_kernel<T, LN, ADD, Q8, 1>(p.mapping, p.per_thread, cl, false, false)
+                             : pick_kernel<T, LN, ADD, Q8, ElemVec<T>::value>(p.mapping, p.per_thread, cl,
+                                                                               a.shift != 0, full);
         if (k == nullptr) return cudaErrorInvalidValue;
     }
     cudaLaunchConfig_t cfg = {};

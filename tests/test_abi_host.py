@@ -450,9 +450,20 @@ def test_bwd_plans_are_consistent(lib, dtype, ln, M):
             continue
         p = rn.make_bwd_plan(M, N, dtype, ln, True, 152)
         assert p["vec_elems"] == vec and p["rounds"] == 1
-        # a 2-stage ring for fp32 vector rows whose ring fits; none otherwise
-        smem = (2 if ln else 1) * p["threads"] * p["per_thread"] * vec * 4 + 2 * (2 * p["threads"] * p["per_thread"] * 16 + 8)
-        assert p["stages"] == (2 if (vec == 4 and smem <= 225 * 1024) else 0)
+        # a 2-stage ring for fp32 vector rows (it overlaps the register
+        # accumulators' slots), the register pipeline for 16-bit vector rows
+        # of one CTA, neither otherwise
+        acc = (2 if ln else 1) * p["threads"] * p["per_thread"] * vec * 4
+        ring = 2 * (2 * p["threads"] * p["per_thread"] * 16 + 8)
+        if vec == 4:
+            assert max(acc, ring) <= 225 * 1024 and p["stages"] == 2
+        elif vec == 8 and p["cluster"] == 1:
+            assert p["stages"] == 1
+        else:
+            assert p["stages"] == 0
+        if vec > 1 and p["cluster"] == 1 and p["per_thread"] > 2:
+            # fewer accesses per thread would need more than 512 threads
+            assert -(-N // (vec * p["per_thread"] // 2)) > 480
         assert p["cluster"] * p["threads"] * p["per_thread"] * vec >= N
         assert p["threads"] % 32 == 0 and 32 <= p["threads"] <= 512
         assert p["cluster"] in (1, 2, 4, 8) and p["group"] in (1, 2, 4, 8)
