@@ -43,6 +43,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", default="libnorm", choices=["libnorm", "reference"])
     p.add_argument("--workload", default=None)
+    p.add_argument("--rows", type=int, default=None,
+                   help="run the workload with this many rows instead of its own (a small case for profiling)")
     p.add_argument("--e2e-steps", type=int, default=30)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-table", action="store_true", help="skip the per-workload table")
@@ -676,6 +678,8 @@ def main():
     args = parse_args()
     from row_wise_normalization_ln_gb300 import workloads as wl
     w = wl.WORKLOADS[args.workload or wl.BENCH_WORKLOAD]
+    if args.rows:
+        w = w.scaled(M=args.rows)
     if args.impl == "reference":
         run_reference(args, w)
         return
@@ -705,7 +709,7 @@ def main():
     value = job_gbs(bytes_per_call, args.steps, world, total_ms)
     achieved = bytes_per_call / (kern_ms / 1e3) / 1e9
     peak, peak_src = measured_peak()
-    traffic = ncu_traffic(w.name)
+    traffic = ncu_traffic(w.name) if not args.rows else None  # the captures are of full-size launches
 
     e2e_ms, h2d, d2h = time_e2e(w, rn, inp, device, args.e2e_steps)
 

@@ -423,6 +423,47 @@ __device__ __forceinline__ void write_partials(const BwdArgs& a, const float* ac
     }
 }
 
+// Rows over a cluster (C > 1): the row's pair of sums meets without a
+// cluster barrier (whose release waited for every earlier store of the CTA,
+// the row's dx included, to reach L2). Each CTA reduces its pair in shared
+// memory; thread 0 then sends it to every CTA of the cluster with an
+// asynchronous store counted on that CTA's mbarrier (slot [rank]), and
+// announces the C pairs it expects on its own. Every thread waits for the
+// phase and adds the C pairs in rank order. Slots and barriers alternate by
+// row parity: a CTA sends a row's pair only after its wait on the previous
+// row, which needs every peer's pair of that row, which each peer sends
+// only after reading the pairs of the row before.
+struct ClusterPairSmem {
+    float2 part[2][8];
+    uint64_t bar[2];
+};
+
+__device__ __forceinline__ float2 cluster_row_sum2(PairReduceSmem& red, ClusterPairSmem& cred, int it, float2 v,
+                                                   int C, int rank, int nwarps, int wwidth, uint64_t limit,
+                                                   bool& late) {
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int s = it & 1;
+    v.x = group_sum(v.x, 32);
+    v.y = group_sum(v.y, 32);
+    if (lane == 0) red.warp_part[s][tid >> 5] = v;
+    __syncthreads();
+    if (tid < 32) {
+        float2 w = lane < nwarps ? red.warp_part[s][lane] : make_float2(0.f, 0.f);
+        w.x = sum_first_lanes(w.x, wwidth);
+        w.y = sum_first_lanes(w.y, wwidth);
+        if (tid == 0) {
+            mbar_arrive_expect(&cred.bar[s], static_cast<uint32_t>(C) * 8u);
+            for (int q = 0; q < C; ++q)
+                st_async_peer_f32x2(peer_smem_addr(&cred.part[s][rank], static_cast<uint32_t>(q)), w,
+                                    peer_smem_addr(&cred.bar[s], static_cast<uint32_t>(q)));
+        }
+    }
+    if (!mbar_wait(&cred.bar[s], static_cast<uint32_t>((it >> 1) & 1), limit)) late = true;
+    const float2 p = lane < C ? cred.part[s][lane] : make_float2(0.f, 0.f);
+    return make_float2(sum_first_lanes(p.x, C), sum_first_lanes(p.y, C));
+}
+
 // ------------------------------------------------------------ main kernel
 // Layout as the forward's CTA mapping: CTA rank k of a row's cluster holds
 // accesses [k*V*T, (k+1)*V*T), warp-major. Launched as clusters of Q CTAs:
@@ -503,18 +544,31 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
     // after the barrier of the row's pair reduction, so that from the row
     // after a timeout on the whole CTA neither waits nor copies.
     __shared__ int s_late;
-    if constexpr (RING) {
+    __shared__ ClusterPairSmem cred;  // rows over a cluster
+    if (RING || C > 1) {
         if (tid == 0) {
-            for (int k = 0; k < stages; ++k) mbar_init(&full[k], 1);
+            if (RING) {
+                for (int k = 0; k < stages; ++k) mbar_init(&full[k], 1);
+                s_late = 0;
+            }
+            if (C > 1) {
+                mbar_init(&cred.bar[0], 1);
+                mbar_init(&cred.bar[1], 1);
+            }
             mbar_init_fence();
-            s_late = 0;
         }
-        __syncthreads();
+        // Every barrier is initialised before any CTA of the cluster
+        // addresses it.
+        if (C > 1)
+            cluster_barrier();
+        else
+            __syncthreads();
     }
 
     grid_release();
     grid_wait();
-    const uint64_t limit = RING ? a.wait->limit_ns : 0;
+    const uint64_t limit = a.wait->limit_ns;
+    bool rlate = false;  // C > 1: a wait for the row's pairs ran out (the outputs are then void)
 
     // RING, thread 0: fill stage `st` with this CTA's slices of x and dy of
     // row `r` (copies read memory: only after the wait above).
@@ -542,6 +596,14 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
     const T* xbase = static_cast<const T*>(a.x) + f0 * VEC;
     const T* dybase = static_cast<const T*>(a.dy) + f0 * VEC;
 
+    // LayerNorm: the row's mean and rstd. Without a ring they are loaded a
+    // row ahead (a load at the row's start would stall all of its
+    // arithmetic on an L2 round trip); with one, at the row's start, before
+    // the wait for its stage.
+    float2 ms = make_float2(0.f, 0.f);
+    if constexpr (LN && !RING) {
+        if (first_row < a.M) ms = make_float2(a.mean[first_row], a.rstd[first_row]);
+    }
     int it = 0;
     int st = 0;            // RING: this row's stage
     uint32_t parity = 0;   // ... and the phase parity to wait for
@@ -552,6 +614,9 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
         if (tid == 0) prefetch_row(row + ahead * row_step);
         Raw xv[V], dv[V];
         if constexpr (RING) {
+            // The row's statistics: loaded here, their latency hidden behind
+            // the wait for the row's stage.
+            if constexpr (LN) ms = make_float2(a.mean[row], a.rstd[row]);
             // After a wait has run out the CTA neither waits nor copies any
             // more (its outputs are void by then); the kernel still ends.
             if (waiting) {
@@ -578,12 +643,16 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
                     dv[j] = O::load(dybase + row * N + j * stride);
                 }
         }
-        float mu = 0.f, rs = 0.f;
-        if constexpr (LN) {
-            mu = a.mean[row];
-            rs = a.rstd[row];
+        const float mu = ms.x, rs = ms.y;
+        const float2 pr = rw.partials(xv, dv, nv, mu, rs);
+        const float2 S = C > 1 ? cluster_row_sum2(red, cred, it, pr, C, rank, nwarps, wwidth, limit, rlate)
+                               : row_sum2(red, it & 1, pr, 1, nwarps, wwidth);
+        // Without a ring: the next row's statistics, issued after the row's
+        // block barrier (a barrier would wait for a load issued before it)
+        // and needed only after this row's output pass.
+        if constexpr (LN && !RING) {
+            if (row + row_step < a.M) ms = make_float2(a.mean[row + row_step], a.rstd[row + row_step]);
         }
-        const float2 S = row_sum2(red, it & 1, rw.partials(xv, dv, nv, mu, rs), C, nwarps, wwidth);
         if constexpr (RING) {
             // Every thread has read this stage before the barrier above:
             // refill it with the row `stages` turns ahead.
@@ -612,7 +681,7 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
     // With register accumulators the ring overlaps their shared-memory
     // slots: every thread is past its last read of the ring (and thread 0
     // past its drain) before any slot is written.
-    __syncthreads();
+    if (__syncthreads_or(rlate) && tid == 0) atomicAdd(&a.wait->timeouts, 1u);
     rw.acc_to_smem();
     write_partials<VEC, V, NA>(a, acc_s, slice, C, f0, nv);
 }

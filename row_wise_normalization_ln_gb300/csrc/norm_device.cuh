@@ -141,6 +141,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// Asynchronous store of a float2 into a cluster peer's shared memory
+// (`addr`, from mapa), counted as 8 bytes against the peer's mbarrier
+// (`bar`, from mapa): the peer sees the value once that barrier's phase
+// completes. Weakly ordered: no fence with this thread's other accesses.
+__device__ __forceinline__ void st_async_peer_f32x2(uint32_t addr, float2 v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+                 "f"(v.x), "f"(v.y), "r"(bar)
+                 : "memory");
+}
+
 // Arrive once, announcing `bytes` more bytes for the current phase.
 __device__ __forceinline__ void mbar_arrive_expect(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
