@@ -260,8 +260,11 @@ norm_status rms_bwd(const void* dy, const void* x, const void* w, void* dx, floa
  * backward has no shifted-row mode: other rows use element accesses).
  * `stages` 2..4 (16-byte vector rows): each CTA keeps its slices of x and dy
  * of that many upcoming rows in a shared-memory ring filled by bulk copies
- * (bounded waits, counted by norm_wait_timeouts); 0: rows are read from
- * L2 after a prefetch. The planner takes 2 stages for fp32 rows.
+ * (bounded waits, counted by norm_wait_timeouts); 1 (one CTA per row,
+ * cluster == 1): the register pipeline, each thread loading the next row's
+ * slices into a second set of registers while the current row is reduced
+ * and written; 0: rows are read from L2 after a prefetch. The planner takes
+ * 2 stages for fp32 vector rows and 1 for 16-bit vector rows of one CTA.
  * Returns NORM_ERR_ARG for rows beyond the backward's limit.
  */
 norm_status norm_bwd_make_plan(int64_t M, int64_t N, norm_dtype dtype, int layer_norm,

@@ -474,7 +474,9 @@ __device__ __forceinline__ float2 cluster_row_sum2(PairReduceSmem& red, ClusterP
 // kernel. Rows two steps ahead are prefetched into L2 (bulk, by one thread),
 // so a row's own loads are L2 hits while HBM already serves the rows after
 // it.
-template <class T, int VEC, int V, bool LN, bool RING>
+// CL: launched for rows over a cluster (row_cluster > 1); the kernels for
+// one CTA per row carry none of the cluster code.
+template <class T, int VEC, int V, bool LN, bool RING, bool CL>
 __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) {
     static_assert(!RING || VEC > 1, "the ring moves 16-byte vectors");
     using R = BwdRow<T, VEC, V, LN>;
@@ -492,7 +494,7 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
     const int nwarps = T_ >> 5;
     int wwidth = 1;
     while (wwidth < nwarps) wwidth <<= 1;
-    const int C = a.row_cluster;
+    const int C = CL ? a.row_cluster : 1;
     const int rank = C > 1 ? static_cast<int>(cluster_rank()) : 0;
     const int64_t first_row = C > 1 ? blockIdx.x / C : blockIdx.x;
     const int64_t row_step = C > 1 ? gridDim.x / C : gridDim.x;
@@ -544,14 +546,14 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
     // after the barrier of the row's pair reduction, so that from the row
     // after a timeout on the whole CTA neither waits nor copies.
     __shared__ int s_late;
-    __shared__ ClusterPairSmem cred;  // rows over a cluster
-    if (RING || C > 1) {
+    __shared__ std::conditional_t<CL, ClusterPairSmem, char> cred;  // rows over a cluster
+    if (RING || CL) {
         if (tid == 0) {
             if (RING) {
                 for (int k = 0; k < stages; ++k) mbar_init(&full[k], 1);
                 s_late = 0;
             }
-            if (C > 1) {
+            if constexpr (CL) {
                 mbar_init(&cred.bar[0], 1);
                 mbar_init(&cred.bar[1], 1);
             }
@@ -559,7 +561,7 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
         }
         // Every barrier is initialised before any CTA of the cluster
         // addresses it.
-        if (C > 1)
+        if constexpr (CL)
             cluster_barrier();
         else
             __syncthreads();
@@ -567,8 +569,8 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
 
     grid_release();
     grid_wait();
-    const uint64_t limit = a.wait->limit_ns;
-    bool rlate = false;  // C > 1: a wait for the row's pairs ran out (the outputs are then void)
+    const uint64_t limit = (RING || CL) ? a.wait->limit_ns : 0;
+    bool rlate = false;  // CL: a wait for the row's pairs ran out (the outputs are then void)
 
     // RING, thread 0: fill stage `st` with this CTA's slices of x and dy of
     // row `r` (copies read memory: only after the wait above).
@@ -645,8 +647,11 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
         }
         const float mu = ms.x, rs = ms.y;
         const float2 pr = rw.partials(xv, dv, nv, mu, rs);
-        const float2 S = C > 1 ? cluster_row_sum2(red, cred, it, pr, C, rank, nwarps, wwidth, limit, rlate)
-                               : row_sum2(red, it & 1, pr, 1, nwarps, wwidth);
+        float2 S;
+        if constexpr (CL)
+            S = cluster_row_sum2(red, cred, it, pr, C, rank, nwarps, wwidth, limit, rlate);
+        else
+            S = row_sum2(red, it & 1, pr, 1, nwarps, wwidth);
         // Without a ring: the next row's statistics, issued after the row's
         // block barrier (a barrier would wait for a load issued before it)
         // and needed only after this row's output pass.
@@ -681,7 +686,11 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
     // With register accumulators the ring overlaps their shared-memory
     // slots: every thread is past its last read of the ring (and thread 0
     // past its drain) before any slot is written.
-    if (__syncthreads_or(rlate) && tid == 0) atomicAdd(&a.wait->timeouts, 1u);
+    if constexpr (CL) {
+        if (__syncthreads_or(rlate) && tid == 0) atomicAdd(&a.wait->timeouts, 1u);
+    } else {
+        __syncthreads();
+    }
     rw.acc_to_smem();
     write_partials<VEC, V, NA>(a, acc_s, slice, C, f0, nv);
 }
@@ -689,29 +698,30 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_cta(const BwdArgs a) 
 // ------------------------------------------------------------ register pipeline
 // The backward for rows that one CTA covers (row_cluster == 1), with the
 // next row's loads in flight while the current row is reduced and written.
-// Each thread holds two register sets of its x and dy slices and alternates
-// between them (the loop body is unrolled twice, so no register is copied):
-// it loads row r + step into one set right after it has handed in its share
-// of row r's sums, while the other set still holds row r for the output
-// pass. The row's sums meet through an mbarrier instead of a block barrier:
-// lane 0 of each warp stores the warp's pair and arrives (release), every
-// thread then issues its next loads and waits for the phase (acquire) before
-// reading the pairs. A block barrier would order the loads issued before it
-// and so wait for them; the loads issued between an arrive and a wait are
-// ordered by neither. Rows two steps ahead are still bulk-prefetched into
-// L2, so the register loads are L2 hits.
+// Each thread holds two register sets of its x and dy slices (and the row's
+// mean and rstd) and alternates between them (the loop body is unrolled
+// twice, so no register is copied): it loads row r + step into one set right
+// after it has handed in its share of row r's sums, while the other set
+// still holds row r for the output pass. Lane 0 of each warp stores the
+// warp's pair; then every thread issues its next loads and meets the others,
+// at a block barrier (CTAs of 8 or more warps) or on an mbarrier (lane 0
+// arrives with release before the loads, every thread waits with acquire
+// after them), and reads the pairs. Rows three steps ahead are still
+// bulk-prefetched into L2, so the register loads are L2 hits.
 //
 // Slots and barriers alternate by row parity. A warp writes a row's pair
-// only after its wait on the previous row, which completes only after every
-// warp has arrived there, after reading the pairs of the row before; so a
-// slot is rewritten only after all its readers are done, and an mbarrier
-// phase never completes twice ahead of a waiter.
+// only after it has passed the previous row's meeting, which every warp
+// reaches only after reading the pairs of the row before; so a slot is
+// rewritten only after all its readers are done, and an mbarrier phase
+// never completes twice ahead of a waiter.
 struct PipeReduceSmem {
     float2 warp_part[2][32];
     uint64_t bar[2];
 };
 
-template <class T, int VEC, int V, bool LN>
+// BAR: the warps meet at a block barrier (launched for CTAs of 8 or more
+// warps); otherwise on the mbarrier.
+template <class T, int VEC, int V, bool LN, bool BAR>
 __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_pipe(const BwdArgs a) {
     using R = BwdRow<T, VEC, V, LN>;
     using O = typename R::O;
@@ -789,12 +799,17 @@ __global__ void __launch_bounds__(kBwdMaxThreads) norm_bwd_pipe(const BwdArgs a)
         const int s = it & 1;
         if (lane == 0) {
             red.warp_part[s][warp] = p;
-            mbar_arrive(&red.bar[s]);
+            if constexpr (!BAR) mbar_arrive(&red.bar[s]);
         }
         load(xn, dn, mn, row + row_step);
-        // Every warp of the CTA arrives once per row, so the phase completes;
-        // the wait is bounded all the same (the device's wait limit).
-        if (!mbar_wait(&red.bar[s], static_cast<uint32_t>((it >> 1) & 1), limit)) late = true;
+        if constexpr (BAR) {
+            __syncthreads();
+        } else {
+            // Every warp of the CTA arrives once per row, so the phase
+            // completes; the wait is bounded all the same (the device's
+            // wait limit).
+            if (!mbar_wait(&red.bar[s], static_cast<uint32_t>((it >> 1) & 1), limit)) late = true;
+        }
         float2 w = lane < nwarps ? red.warp_part[s][lane] : make_float2(0.f, 0.f);
         w.x = sum_first_lanes(w.x, wwidth);
         w.y = sum_first_lanes(w.y, wwidth);
@@ -887,39 +902,54 @@ constexpr int bwd_vmax(bool ln, int elem_size, int vec) {
     return vec == 1 ? 8 : (ln && elem_size == 2) ? 2 : 4;
 }
 
-template <class T, bool LN, int VEC, bool RING>
-BwdKernel pick_bwd_r(int V) {
+template <class T, bool LN, int VEC, bool RING, bool CL>
+BwdKernel pick_bwd_c(int V) {
     constexpr int vmax = bwd_vmax(LN, sizeof(T), VEC);
     switch (V) {
-        case 1: return norm_bwd_cta<T, VEC, 1, LN, RING>;
-        case 2: return vmax >= 2 ? norm_bwd_cta<T, VEC, 2, LN, RING> : nullptr;
-        case 4: if constexpr (vmax >= 4) return norm_bwd_cta<T, VEC, 4, LN, RING>; else return nullptr;
-        case 8: if constexpr (vmax >= 8) return norm_bwd_cta<T, VEC, 8, LN, RING>; else return nullptr;
+        case 1: return norm_bwd_cta<T, VEC, 1, LN, RING, CL>;
+        case 2: return vmax >= 2 ? norm_bwd_cta<T, VEC, 2, LN, RING, CL> : nullptr;
+        case 4: if constexpr (vmax >= 4) return norm_bwd_cta<T, VEC, 4, LN, RING, CL>; else return nullptr;
+        case 8: if constexpr (vmax >= 8) return norm_bwd_cta<T, VEC, 8, LN, RING, CL>; else return nullptr;
         default: return nullptr;
     }
 }
 
-template <class T, bool LN, int VEC>
-BwdKernel pick_bwd_pipe(int V) {
+template <class T, bool LN, int VEC, bool RING>
+BwdKernel pick_bwd_r(int V, bool cl) {
+    return cl ? pick_bwd_c<T, LN, VEC, RING, true>(V) : pick_bwd_c<T, LN, VEC, RING, false>(V);
+}
+
+template <class T, bool LN, int VEC, bool BAR>
+BwdKernel pick_bwd_pipe_b(int V) {
     constexpr int vmax = bwd_vmax(LN, sizeof(T), VEC);
     switch (V) {
-        case 1: return norm_bwd_pipe<T, VEC, 1, LN>;
-        case 2: return vmax >= 2 ? norm_bwd_pipe<T, VEC, 2, LN> : nullptr;
-        case 4: if constexpr (vmax >= 4) return norm_bwd_pipe<T, VEC, 4, LN>; else return nullptr;
-        case 8: if constexpr (vmax >= 8) return norm_bwd_pipe<T, VEC, 8, LN>; else return nullptr;
+        case 1: return norm_bwd_pipe<T, VEC, 1, LN, BAR>;
+        case 2: return vmax >= 2 ? norm_bwd_pipe<T, VEC, 2, LN, BAR> : nullptr;
+        case 4: if constexpr (vmax >= 4) return norm_bwd_pipe<T, VEC, 4, LN, BAR>; else return nullptr;
+        case 8: if constexpr (vmax >= 8) return norm_bwd_pipe<T, VEC, 8, LN, BAR>; else return nullptr;
         default: return nullptr;
     }
+}
+
+// CTAs of 8 or more warps meet at a block barrier, smaller ones on the
+// mbarrier (measured on GB300: LayerNorm bf16 4096x8192, 512 threads, 42.3 us
+// with the mbarrier and 40.7 with the block barrier; RMSNorm bf16 65536x2048,
+// 128 threads, 126.5 and 135.2 us).
+template <class T, bool LN, int VEC>
+BwdKernel pick_bwd_pipe(int V, int threads) {
+    return threads >= 256 ? pick_bwd_pipe_b<T, LN, VEC, true>(V) : pick_bwd_pipe_b<T, LN, VEC, false>(V);
 }
 
 // stages 0: rows from L2 after a bulk prefetch; 1: the register pipeline;
-// 2..4: the shared-memory ring (16-byte vector rows only).
+// 2..4: the shared-memory ring (16-byte vector rows only). `cl`: rows over
+// a cluster of CTAs.
 template <class T, bool LN, int VEC>
-BwdKernel pick_bwd(int V, int stages) {
-    if (stages == 1) return pick_bwd_pipe<T, LN, VEC>(V);
+BwdKernel pick_bwd(int V, int stages, bool cl, int threads) {
+    if (stages == 1) return cl ? nullptr : pick_bwd_pipe<T, LN, VEC>(V, threads);
     if constexpr (VEC > 1) {
-        if (stages >= 2) return pick_bwd_r<T, LN, VEC, true>(V);
+        if (stages >= 2) return pick_bwd_r<T, LN, VEC, true>(V, cl);
     }
-    return stages >= 2 ? nullptr : pick_bwd_r<T, LN, VEC, false>(V);
+    return stages >= 2 ? nullptr : pick_bwd_r<T, LN, VEC, false>(V, cl);
 }
 
 inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, unsigned cluster,
@@ -1021,8 +1051,10 @@ cudaError_t launch_norm_bwd(const norm_plan& p, const BwdArgs& a, cudaStream_t s
     int64_t grid = 0;
     if (a.M > 0 && p.grid > 0) {
         const bool ring = p.stages >= 2;
-        const BwdKernel k = p.vec_elems == 1 ? pick_bwd<T, LN, 1>(p.per_thread, p.stages)
-                                             : pick_bwd<T, LN, ElemVec<T>::value>(p.per_thread, p.stages);
+        const bool cl = p.cluster > 1;
+        const BwdKernel k = p.vec_elems == 1
+                                ? pick_bwd<T, LN, 1>(p.per_thread, p.stages, cl, p.threads)
+                                : pick_bwd<T, LN, ElemVec<T>::value>(p.per_thread, p.stages, cl, p.threads);
         if (k == nullptr) return cudaErrorInvalidValue;
         const size_t smem = static_cast<size_t>(bwd_smem_bytes(LN, p.threads, p.per_thread, p.vec_elems, p.stages));
         int64_t resident = 0;
