@@ -109,10 +109,13 @@ def measured_peak():
 # capture summarised in profiles/ (workload -> (kernel source hash at capture,
 # bytes per launch, summary file)).
 NCU_TRAFFIC = {
-    "rms_f32_8192x4096": ("46ce0b042e1bfeb1", 207_114_496, "profiles/norm_fwd_cta_rms_f32_8192x4096.md"),
-    "ln_bf16_4096x8192_outliers": ("46ce0b042e1bfeb1", 85_719_552, "profiles/norm_fwd_cta_ln_bf16_4096x8192.md"),
-    "ln_f32_8192x5001": ("46ce0b042e1bfeb1", 278_216_960, "profiles/norm_fwd_cta_shift_ln_f32_8192x5001.md"),
-    "ln_f32_2048x65536": ("46ce0b042e1bfeb1", 1_033_014_528, "profiles/norm_fwd_cta_ln_f32_2048x65536.md"),
+    "rms_f32_8192x4096": ("e96c0bd524878b47", 207_030_784, "profiles/norm_fwd_cta_rms_f32_8192x4096.md"),
+    "ln_bf16_4096x8192_outliers": ("e96c0bd524878b47", 86_715_136, "profiles/norm_fwd_cta_ln_bf16_4096x8192.md"),
+    "rms_bf16_65536x2048": ("e96c0bd524878b47", 479_597_824, "profiles/norm_fwd_cta_rms_bf16_65536x2048.md"),
+    "ln_f32_2048x65536": ("e96c0bd524878b47", 1_033_511_680, "profiles/norm_fwd_cta_ln_f32_2048x65536.md"),
+    "ln_f32_8192x5000": ("e96c0bd524878b47", 268_637_184, "profiles/norm_fwd_cta_ln_f32_8192x5000.md"),
+    "ln_f32_128x1024": ("e96c0bd524878b47", 544_512, "profiles/norm_fwd_cta_ln_f32_128x1024.md"),
+    "fp8_ln_bf16_4096x8192_outliers": ("e96c0bd524878b47", 71_504_640, "profiles/norm_fwd_cta_fp8_ln_bf16_4096x8192.md"),
 }
 
 
