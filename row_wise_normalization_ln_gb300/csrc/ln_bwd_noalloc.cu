@@ -86,8 +86,14 @@ extern "C" norm_status ln_bwd_noalloc(const void* dy, const void* x, const void*
     if (st != NORM_OK) return st;
     st = norm_bwd_make_plan(M, N, dtype, 1, al, sms, &plan);
     if (st != NORM_OK) return st;
-    // At most as many partial rows (grid / group) as the scratch holds.
+    // At most as many partial rows (grid / group) as the scratch holds: where
+    // one partial row per CTA would not fit, CTAs of one row each first add
+    // their columns in reduction clusters of up to 8, then the grid is capped.
     const int64_t rows_fit = static_cast<int64_t>(kScratchFloats / static_cast<size_t>(2 * N));
+    if (plan.cluster == 1) {
+        while (plan.grid / plan.group > rows_fit && plan.group < 8 && plan.group * 2 <= plan.grid) plan.group *= 2;
+        plan.grid -= plan.grid % plan.group;
+    }
     const int64_t cap = rows_fit * plan.group;
     if (plan.grid > cap) plan.grid = cap;
     return ln_bwd_planned(dy, x, gamma, mean, rstd, dx, dgamma, dbeta, scratch, kScratchFloats * sizeof(float), M, N,
