@@ -297,10 +297,11 @@ norm_status rms_bwd_planned(const void* dy, const void* x, const void* w, void* 
  * synchronisation cudaFree may cause. The call allocates nothing: the
  * backward's partial column sums go to one static device array of 4 MiB,
  * which every GPU that loads this library holds until the process exits.
- * The plan's grid is capped so that its partial rows (2 * N floats each)
- * fit; a row whose single partial row would not fit (N > 524288, beyond the
- * backward's own limits anyway) returns NORM_ERR_ARG, as do the sizes
- * ln_bwd refuses.
+ * Where one partial row (2 * N floats) per CTA would not fit, CTAs of one
+ * row each are grouped into reduction clusters of up to 8, and then the
+ * plan's grid is capped so that its partial rows fit; a row whose single
+ * partial row would not fit (N > 524288, beyond the backward's own limits
+ * anyway) returns NORM_ERR_ARG, as do the sizes ln_bwd refuses.
  * The first call on each device looks up that array's device address (with
  * the device current) and the SM count; make that first call before any
  * stream capture. The address is kept for the life of the process: a

@@ -55,8 +55,10 @@ def test_no_alloc_backward_matches_ln_bwd_twice(lib):
     """Two calls in a row (different shapes and data, so that stale scratch
     from the first would show in the second): dx equal to ln_bwd's, the
     column gradients within the backward bound of ln_bwd's and of the
-    oracle. The first case has more partial rows by default than the
-    scratch holds (its grid is capped); the second spans 8-CTA clusters."""
+    oracle. In the first case one partial row per CTA would not fit the
+    scratch, so its CTAs add their columns in reduction clusters of 8
+    first; the second spans 8-CTA clusters and its grid is capped to the
+    scratch."""
     for (M, N, dtype, seed) in ((4096, 8192, torch.bfloat16, 1), (256, 65536, torch.float32, 2)):
         x, dy, gamma = _case(M, N, dtype, seed)
         mean, rstd = ln_stats_f32(x, gamma, 1e-5)
