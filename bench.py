@@ -767,7 +767,7 @@ def main():
                      "kernel_hash": kernel_source_hash()},
         "e2e": {"value": round(bytes_per_call / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if w.bwd else 1),  # the backward adds its column-sum kernel
         "clocks": clocks,
         "cpu_baseline": cpu,
         "cpu_baseline_all_cores": cpu_all,
