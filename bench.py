@@ -480,7 +480,10 @@ def time_e2e(w, rn, inp, device, steps):
     every step copies the parameters to the device and runs the call over
     the rows with ``host_rows_pipeline`` (row chunks copied in, normalised
     and copied back on three streams, so the two copy directions and the
-    kernels overlap): x (and r) in, y (and h, and the statistics) out."""
+    kernels overlap): x (and r) in, y (and h, and the statistics) out. The
+    steps are a stream of batches (``wait=False``): a step's last copies
+    back overlap the next step's first copies in; the timed region ends
+    after every copy back of every step (``host_rows_wait``)."""
     if w.bwd:
         return time_e2e_bwd(w, rn, inp, device, steps)
     import torch
@@ -519,10 +522,11 @@ def time_e2e(w, rn, inp, device, steps):
     def one():
         for k in params:
             dpar[k].copy_(hin[k], non_blocking=True)
-        rn.host_rows_pipeline([hin[k] for k in rowin], outs, call, device=device)
+        rn.host_rows_pipeline([hin[k] for k in rowin], outs, call, device=device, wait=False)
 
     for _ in range(3):
         one()
+    rn.host_rows_wait(device)
     torch.cuda.synchronize(device)
     stream = torch.cuda.current_stream(device)
     t0 = torch.cuda.Event(enable_timing=True)
@@ -530,6 +534,7 @@ def time_e2e(w, rn, inp, device, steps):
     t0.record(stream)
     for _ in range(steps):
         one()
+    rn.host_rows_wait(device)
     t1.record(stream)
     torch.cuda.synchronize(device)
     ms = t0.elapsed_time(t1) / steps

@@ -20,6 +20,7 @@ import torch
 __all__ = [
     "ln_fwd", "rms_fwd", "ln_fwd_add", "rms_fwd_add", "ln_fwd_fp8", "rms_fwd_fp8", "ln_bwd", "rms_bwd",
     "make_plan", "make_bwd_plan", "NormPlan", "NormError", "LibraryNotBuilt", "library", "host_rows_pipeline",
+    "host_rows_wait",
     "NORM_F32", "NORM_BF16", "NORM_F16", "NORM_MAP_GROUP", "NORM_MAP_CTA",
 ]
 
@@ -591,7 +592,7 @@ def _pipeline_streams(dev: torch.device):
 
 
 def host_rows_pipeline(inputs, outputs, call, *, chunk_rows: Optional[int] = None,
-                       device: Optional[torch.device] = None):
+                       device: Optional[torch.device] = None, wait: bool = True):
     """Run a row-wise library call over pinned host tensors, overlapping the
     copies in both directions with the kernels.
 
@@ -607,8 +608,13 @@ def host_rows_pipeline(inputs, outputs, call, *, chunk_rows: Optional[int] = Non
     out=o[0])`` with ``w`` already on the device. Returns when all work is
     queued; the current stream waits for the last copy back, so a
     ``torch.cuda.synchronize()`` (or an event on the current stream) makes
-    the host outputs readable. Not for calls that reduce over rows (the
-    backward's column gradients)."""
+    the host outputs readable. With ``wait=False`` it does not: the copies
+    back of this call may then still run while the next call's rows are
+    copied in and normalised (a stream of batches keeps both copy
+    directions busy), and ``host_rows_wait()`` (or a device
+    synchronisation) orders them before later work on the current stream.
+    Not for calls that reduce over rows (the backward's column
+    gradients)."""
     if not inputs or not outputs:
         raise ValueError("inputs and outputs must be non-empty lists of pinned host tensors")
     M = inputs[0].shape[0]
@@ -626,14 +632,24 @@ def host_rows_pipeline(inputs, outputs, call, *, chunk_rows: Optional[int] = Non
     comp = torch.cuda.current_stream(dev)
     s_in, s_out, in_ready, done, copied, lock = _pipeline_streams(dev)
     with lock:
-        _enqueue_pipeline(inputs, outputs, call, M, chunk, dev, comp, s_in, s_out, in_ready, done, copied)
+        _enqueue_pipeline(inputs, outputs, call, M, chunk, dev, comp, s_in, s_out, in_ready, done, copied, wait)
 
 
-def _enqueue_pipeline(inputs, outputs, call, M, chunk, dev, comp, s_in, s_out, in_ready, done, copied):
+def host_rows_wait(device: Optional[torch.device] = None) -> None:
+    """Make the current stream wait for every copy back that
+    ``host_rows_pipeline`` has queued on ``device`` (for calls made with
+    ``wait=False``)."""
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    s_in, s_out, _, _, _, lock = _pipeline_streams(dev)
+    with lock:
+        torch.cuda.current_stream(dev).wait_stream(s_out)
+
+
+def _enqueue_pipeline(inputs, outputs, call, M, chunk, dev, comp, s_in, s_out, in_ready, done, copied, wait):
     d_in = [[torch.empty((chunk,) + tuple(t.shape[1:]), dtype=t.dtype, device=dev) for t in inputs] for _ in range(2)]
     d_out = [[torch.empty((chunk,) + tuple(t.shape[1:]), dtype=t.dtype, device=dev) for t in outputs] for _ in range(2)]
     s_in.wait_stream(comp)                            # staging memory and inputs as of now
-    s_out.wait_stream(comp)
+    s_out.wait_stream(comp)                           # (a call without wait: not its copies back)
     for c, r0 in enumerate(range(0, M, chunk)):
         b = c % 2
         n = min(M, r0 + chunk) - r0
@@ -653,7 +669,8 @@ def _enqueue_pipeline(inputs, outputs, call, M, chunk, dev, comp, s_in, s_out, i
             for h, d in zip(outputs, d_out[b]):
                 h[r0:r0 + n].copy_(d[:n], non_blocking=True)
             copied[b].record(s_out)
-    comp.wait_stream(s_out)
+    if wait:
+        comp.wait_stream(s_out)
     comp.wait_stream(s_in)
     # keep the staging buffers alive until the queued work has used them
     for bufs in d_in + d_out:

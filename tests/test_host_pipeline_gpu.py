@@ -121,3 +121,24 @@ def test_two_host_threads_at_once():
     torch.cuda.synchronize()
     for x, g, hx, hy, gd in cases:
         check_rms(x, g, 1e-6, hy)
+
+
+def test_a_stream_of_batches_without_waits():
+    """Calls with wait=False: each call's copies back may overlap the next
+    call's copies in; host_rows_wait then orders all of them before a
+    consumer on the current stream. Three batches, three host outputs, each
+    checked against the oracle."""
+    N = 2048
+    x_list = [_rand(700, N, torch.float32, seed=60 + k)[0] for k in range(3)]
+    g = _rand(1, N, torch.float32, seed=63)[2]
+    gd = g.cuda()
+    hxs = [x.pin_memory() for x in x_list]
+    hys = [torch.empty_like(hx).pin_memory() for hx in hxs]
+    for hx, hy in zip(hxs, hys):
+        rn.host_rows_pipeline([hx], [hy], lambda i, o: rn.rms_fwd(i[0], gd, 1e-6, out=o[0]), chunk_rows=160,
+                              wait=False)
+    rn.host_rows_wait()
+    backs = [hy.to("cuda", non_blocking=True) for hy in hys]   # ordered after every copy back
+    torch.cuda.synchronize()
+    for x, back in zip(x_list, backs):
+        check_rms(x, g, 1e-6, back)
