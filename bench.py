@@ -109,13 +109,13 @@ def measured_peak():
 # capture summarised in profiles/ (workload -> (kernel source hash at capture,
 # bytes per launch, summary file)).
 NCU_TRAFFIC = {
-    "rms_f32_8192x4096": ("88f9c1c753d8c2fd", 207_131_392, "profiles/norm_fwd_cta_rms_f32_8192x4096.md"),
-    "ln_bf16_4096x8192_outliers": ("88f9c1c753d8c2fd", 86_725_632, "profiles/norm_fwd_cta_ln_bf16_4096x8192.md"),
-    "rms_bf16_65536x2048": ("88f9c1c753d8c2fd", 480_149_248, "profiles/norm_fwd_cta_rms_bf16_65536x2048.md"),
-    "ln_f32_2048x65536": ("88f9c1c753d8c2fd", 1_033_129_472, "profiles/norm_fwd_cta_ln_f32_2048x65536.md"),
-    "ln_f32_8192x5000": ("88f9c1c753d8c2fd", 269_134_592, "profiles/norm_fwd_cta_ln_f32_8192x5000.md"),
-    "ln_f32_128x1024": ("88f9c1c753d8c2fd", 544_512, "profiles/norm_fwd_cta_ln_f32_128x1024.md"),
-    "fp8_ln_bf16_4096x8192_outliers": ("88f9c1c753d8c2fd", 71_518_720, "profiles/norm_fwd_cta_fp8_ln_bf16_4096x8192.md"),
+    "rms_f32_8192x4096": ("6827a1cb9770479f", 206_823_936, "profiles/norm_fwd_cta_rms_f32_8192x4096.md"),
+    "ln_bf16_4096x8192_outliers": ("6827a1cb9770479f", 86_684_928, "profiles/norm_fwd_cta_ln_bf16_4096x8192.md"),
+    "rms_bf16_65536x2048": ("6827a1cb9770479f", 480_300_800, "profiles/norm_fwd_cta_rms_bf16_65536x2048.md"),
+    "ln_f32_2048x65536": ("6827a1cb9770479f", 1_034_413_568, "profiles/norm_fwd_cta_ln_f32_2048x65536.md"),
+    "ln_f32_8192x5000": ("6827a1cb9770479f", 269_315_328, "profiles/norm_fwd_cta_ln_f32_8192x5000.md"),
+    "ln_f32_128x1024": ("6827a1cb9770479f", 544_512, "profiles/norm_fwd_cta_ln_f32_128x1024.md"),
+    "fp8_ln_bf16_4096x8192_outliers": ("6827a1cb9770479f", 71_389_184, "profiles/norm_fwd_cta_fp8_ln_bf16_4096x8192.md"),
 }
 
 
